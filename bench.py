@@ -1,0 +1,377 @@
+#!/usr/bin/env python3
+"""Benchmark: GDN prefill tokens/s over a 36-layer stack at T=2048.
+
+Workload: 36 independent GDN layers (hk=16, hv=48, dk=dv=128, 10240 packed
+q|k|v channels, per-layer seeded weights and activations), one 2048-token
+prompt each, fp16 activations, fp32 state, fp16 output.  One step runs every
+layer's pre, scan and post in stream order: the prompt's tokens per second
+through the whole stack.  The 36 layers' inputs (~2.3 GB) are larger than
+the 129 MB L2, so no flush is needed between steps.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
+
+Under torchrun (N > 1) every rank runs its own replica of the stack on its
+own GPU (weak scaling, no collective on the data path); rank 0 prints one
+JSON line.  ``--impl reference`` times the fp64 CPU oracle on a bounded
+sample of the same workload instead.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+from concurrent.futures import ThreadPoolExecutor
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from gated_deltanet_linear_pre_gb300 import inputs as gin  # noqa: E402
+
+LAYERS = 36
+T_PROMPT = 2048
+HK, HV, DK, DV = gin.HK, gin.HV, gin.DK, gin.DV
+C = gin.channels()
+METRIC = "GDN prefill tokens/s (36 layers, T=2048, pre+scan+post); % of roofline"
+PAGES_TOKENS_PER_S = 2048 / 0.269724  # pages' 36-layer pre+scan+post at T=2048, fp16 out (Apple M5)
+WORKLOAD = ("36 independent GDN layers x one T=2048 prompt (hk=16, hv=48, dk=dv=128, C=10240), "
+            "fp16 activations, fp32 state, fp16 output")
+
+# algorithmic HBM bytes per token per layer (fp16 activations, fp32 stage tensors)
+PRE_BYTES_TOK = C * 2 + 2 * HV * 2 + 2 * HK * DK * 4 + HV * DV * 4 + 2 * HV * 4
+SCAN_BYTES_TOK = 2 * HK * DK * 4 + HV * DV * 4 + 2 * HV * 4 + HV * DV * 4
+SCAN_BYTES_SEQ = 2 * HV * DK * DV * 4          # S_in + S_out
+POST_BYTES_TOK = HV * DV * 4 + HV * DV * 2 + HV * DV * 2
+PRE_BYTES_SEQ = C * 16 + 2 * C * 3 * 2 + 2 * HV * 4   # conv_w, hist in+out, A_log, dt_bias
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    return ap.parse_args()
+
+
+def dist_info():
+    return int(os.environ.get("RANK", 0)), int(os.environ.get("WORLD_SIZE", 1)), int(os.environ.get("LOCAL_RANK", 0))
+
+
+def max_over_ranks(x: float, world: int) -> float:
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device="cuda" if dist.get_backend() == "nccl" else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(world: int):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def make_layers(rank: int):
+    # replicas on different ranks draw different seeds (independent prompts)
+    with ThreadPoolExecutor(max_workers=min(16, os.cpu_count() or 1)) as ex:
+        return list(ex.map(lambda l: gin.stack_layer(l + 1000 * rank), range(LAYERS)))
+
+
+# ---- clocks --------------------------------------------------------------------------
+class ClockSampler:
+    """nvidia-smi sampling of SM clock and throttle reasons during the timed region."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "200"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.reader = threading.Thread(target=self._read, daemon=True)
+            self.reader.start()
+        except (OSError, FileNotFoundError):
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+            self.reader.join(timeout=2)
+
+    def summary(self):
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in self.lines:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx.append(float(parts[1]))
+            except ValueError:
+                continue
+            for name, flag in zip(names, parts[4:8]):
+                if flag.lower() == "active":
+                    reasons.add(name)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            pk = json.load(f)
+        return float(pk["hbm_gbs"]), float(pk["bf16_tflops"]), "measured"
+    return 6800.0, 1900.0, "fallback"
+
+
+# ---- CPU baseline (the fp64 oracle, as it stands) ----------------------------------------
+def cpu_baseline(layers_np, tokens: int, n_layers: int):
+    """Time the oracle on `n_layers` layers x the first `tokens` tokens; returns the
+    stack's prompt tokens/s it implies and a description of the sample."""
+    import oracle
+    oracle.build()
+    t0 = time.perf_counter()
+    for layer in layers_np[:n_layers]:
+        sub = gin.LayerInputs(qkv=layer.qkv[:tokens], conv_w=layer.conv_w, hist=layer.hist, a=layer.a[:tokens],
+                              b=layer.b[:tokens], A_log=layer.A_log, dt_bias=layer.dt_bias, z=layer.z[:tokens],
+                              gamma=layer.gamma, S0=layer.S0, cu_seqlens=np.array([0, tokens], np.int32))
+        oracle.layer(sub)
+    dt = time.perf_counter() - t0
+    # tokens through the whole 36-layer stack per second
+    value = tokens * n_layers / dt / LAYERS
+    return {"value": value, "unit": "tokens/s", "cores": oracle.threads(), "kind": "oracle",
+            "sample": f"{n_layers} of the 36 layers x first {tokens} tokens, all 48 heads, fp64 token-sequential "
+                      f"oracle ({dt:.1f} s wall), scaled to the 36-layer stack"}
+
+
+def run_reference(args, rank, world):
+    if rank != 0:
+        return 0
+    import oracle
+    oracle.build()
+    tokens = 256
+    layers = [gin.stack_layer(l) for l in range(min(LAYERS, args.steps + args.warmup))]
+    times = []
+    for step in range(args.warmup + args.steps):
+        layer = layers[step % len(layers)]
+        sub = gin.LayerInputs(qkv=layer.qkv[:tokens], conv_w=layer.conv_w, hist=layer.hist, a=layer.a[:tokens],
+                              b=layer.b[:tokens], A_log=layer.A_log, dt_bias=layer.dt_bias, z=layer.z[:tokens],
+                              gamma=layer.gamma, S0=layer.S0, cu_seqlens=np.array([0, tokens], np.int32))
+        t0 = time.perf_counter()
+        oracle.layer(sub)
+        dt = time.perf_counter() - t0
+        if step >= args.warmup:
+            times.append(dt)
+    # one step = one layer x `tokens`; the stack needs 36 such layers per token
+    per_layer = sum(times) / len(times)
+    value = tokens / (per_layer * LAYERS)
+    sample = f"each step: one layer x first {tokens} tokens of the T=2048 workload, all 48 heads, fp64 oracle"
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": per_layer * 1e3,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "config": {"workload": WORKLOAD, "layers": LAYERS, "seq_len": T_PROMPT},
+            "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": oracle.threads(), "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ---- GPU arm ----------------------------------------------------------------------------------
+def main():
+    args = parse()
+    rank, world, local = dist_info()
+    if world > 1:
+        import torch.distributed as dist
+        if args.impl == "reference":
+            dist.init_process_group("gloo")
+        else:
+            import torch
+            torch.cuda.set_device(local)
+            dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    if args.impl == "reference":
+        rc = run_reference(args, rank, world)
+        if world > 1:
+            import torch.distributed as dist
+            dist.destroy_process_group()
+        return rc
+
+    import torch
+    from gated_deltanet_linear_pre_gb300 import build as gbuild
+    import gated_deltanet_linear_pre_gb300 as gdn
+
+    gbuild.build()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    d = gdn.dims(HK, HV, DK, DV, 1e-6)
+
+    layers_np = make_layers(rank)
+    pin = lambda a: torch.from_numpy(np.ascontiguousarray(a)).pin_memory()
+    host = [dict(qkv=pin(L.qkv), conv_w=pin(L.conv_w), hist=pin(L.hist), a=pin(L.a), b=pin(L.b),
+                 A_log=pin(L.A_log), dt_bias=pin(L.dt_bias), z=pin(L.z), gamma=pin(L.gamma), S0=pin(L.S0))
+            for L in layers_np]
+    devl = [{k: v.to(dev) for k, v in h.items()} for h in host]
+    cu = torch.tensor([0, T_PROMPT], dtype=torch.int32, device=dev)
+    T = T_PROMPT
+    f32 = dict(device=dev, dtype=torch.float32)
+    y = [torch.empty((T, HV, DV), device=dev, dtype=torch.float16) for _ in range(LAYERS)]
+    hist_out = [torch.empty_like(x["hist"]) for x in devl]
+    S_out = [torch.empty_like(x["S0"]) for x in devl]
+    # stage tensors shared by all layers (the layers run in stream order)
+    qn, kn = torch.empty((T, HK, DK), **f32), torch.empty((T, HK, DK), **f32)
+    vc, o = torch.empty((T, HV, DV), **f32), torch.empty((T, HV, DV), **f32)
+    glog, beta = torch.empty((T, HV), **f32), torch.empty((T, HV), **f32)
+    scan_ws_bytes = gdn.gdn_scan_workspace_bytes(d, 1, T)
+    scan_ws = torch.empty(max(scan_ws_bytes, 1), device=dev, dtype=torch.uint8) if scan_ws_bytes else None
+    layer_ws = torch.empty(gdn.gdn_layer_workspace_bytes(d, 1, T), device=dev, dtype=torch.uint8)
+    stream = torch.cuda.current_stream(dev)
+
+    def step(events=None):
+        for l, x in enumerate(devl):
+            if events is not None:
+                events[l][0].record(stream)
+            gdn.gdn_pre(d, cu, T, x["qkv"], x["conv_w"], x["hist"], hist_out[l], x["a"], x["b"], x["A_log"],
+                        x["dt_bias"], qn, kn, vc, glog, beta)
+            if events is not None:
+                events[l][1].record(stream)
+            gdn.gdn_scan(d, cu, T, qn, kn, vc, glog, beta, x["S0"], S_out[l], o, scan_ws)
+            if events is not None:
+                events[l][2].record(stream)
+            gdn.gdn_post(d, T, o, x["z"], x["gamma"], False, y[l])
+            if events is not None:
+                events[l][3].record(stream)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    barrier(world)
+
+    ev = [[[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(LAYERS)]
+          for _ in range(args.steps)]
+    clocks = ClockSampler(local)
+    with clocks:
+        barrier(world)
+        torch.cuda.synchronize()
+        for k in range(args.steps):
+            step(ev[k])
+        torch.cuda.synchronize()
+    barrier(world)
+    total_ms = ev[0][0][0].elapsed_time(ev[-1][-1][3])
+    stage_ms = {"pre": 0.0, "scan": 0.0, "post": 0.0}
+    for k in range(args.steps):
+        for l in range(LAYERS):
+            e = ev[k][l]
+            stage_ms["pre"] += e[0].elapsed_time(e[1])
+            stage_ms["scan"] += e[1].elapsed_time(e[2])
+            stage_ms["post"] += e[2].elapsed_time(e[3])
+    launches = args.steps * LAYERS
+    per_launch_ms = {k: v / launches for k, v in stage_ms.items()}
+    total_ms = max_over_ranks(total_ms, world)
+    ms_per_step = total_ms / args.steps
+    value = world * T * args.steps / (total_ms / 1e3)
+
+    # ---- end to end through gdn_layer with pinned host buffers -------------------------
+    e2e = None
+    if not args.no_e2e:
+        y_host = [torch.empty((T, HV, DV), dtype=torch.float16).pin_memory() for _ in range(LAYERS)]
+        S_host = [torch.empty_like(h["S0"]).pin_memory() for h in host]
+        hist_host = [torch.empty_like(h["hist"]).pin_memory() for h in host]
+        acts = ("qkv", "a", "b", "z", "hist", "S0")
+        h2d = sum(host[l][k].numel() * host[l][k].element_size() for l in range(LAYERS) for k in acts)
+        d2h = sum(t.numel() * t.element_size() for ts in (y_host, S_host, hist_host) for t in ts)
+
+        def e2e_step():
+            for l in range(LAYERS):
+                x = devl[l]
+                for k in acts:
+                    x[k].copy_(host[l][k], non_blocking=True)
+                gdn.gdn_layer(d, cu, T, x["qkv"], x["conv_w"], x["hist"], hist_out[l], x["a"], x["b"], x["z"],
+                              x["A_log"], x["dt_bias"], x["gamma"], x["S0"], S_out[l], False, y[l], layer_ws)
+                y_host[l].copy_(y[l], non_blocking=True)
+                S_host[l].copy_(S_out[l], non_blocking=True)
+                hist_host[l].copy_(hist_out[l], non_blocking=True)
+
+        for _ in range(max(1, args.warmup)):
+            e2e_step()
+        torch.cuda.synchronize()
+        barrier(world)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(args.steps):
+            e2e_step()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        e2e_ms = max_over_ranks(e0.elapsed_time(e1), world)
+        e2e = {"value": world * T * args.steps / (e2e_ms / 1e3), "unit": "tokens/s",
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
+
+    hbm_peak, tf_peak, peak_src = load_peaks()
+    stage_bytes = {"pre": PRE_BYTES_TOK * T + PRE_BYTES_SEQ, "scan": SCAN_BYTES_TOK * T + SCAN_BYTES_SEQ,
+                   "post": POST_BYTES_TOK * T + DV * 4}
+    stages = {}
+    for k in ("pre", "scan", "post"):
+        gbs = stage_bytes[k] / (per_launch_ms[k] * 1e-3) / 1e9
+        stages[k] = {"ms_per_launch": per_launch_ms[k], "alg_bytes_per_launch": stage_bytes[k],
+                     "achieved_gbs": gbs, "frac_of_hbm": gbs / hbm_peak}
+    dom = max(per_launch_ms, key=per_launch_ms.get)
+    traffic = None
+    prof_path = os.path.join(ROOT, "profiles", "traffic.json")
+    if os.path.exists(prof_path):
+        with open(prof_path) as f:
+            traffic = json.load(f).get(dom)
+    roofline = {"bound": "hbm", "kernel": f"gdn_{dom}", "achieved": stages[dom]["achieved_gbs"], "peak": hbm_peak,
+                "unit": "GB/s", "frac": stages[dom]["frac_of_hbm"], "traffic": traffic,
+                "peak_source": f"{peak_src} (MEASURED_PEAKS.json hbm_gbs)" if peak_src == "measured" else "fallback"}
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cpu = cpu_baseline(layers_np, T, 3)
+
+    if rank == 0:
+        line = {"metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+                "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
+                "vs_baseline": value / PAGES_TOKENS_PER_S, "dtype": "f32", "data": "synthetic",
+                "config": {"workload": WORKLOAD, "layers": LAYERS, "seq_len": T, "global_batch": world,
+                           "parallelism": f"replicas{world}", "l2": "inputs larger than L2 (36-layer set ~2.3 GB)"},
+                "roofline": roofline, "stages": stages, "cpu_baseline": cpu, "e2e": e2e,
+                "gpu_launches": 3 * LAYERS * args.steps, "clocks": clocks.summary()}
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,24 @@
+"""GB300-native Gated DeltaNet prompt-prefill path.
+
+The product is the CUDA library libgdn.so (C ABI: include/gdn.h), built for
+sm_103a by ``gated_deltanet_linear_pre_gb300.build``.  This package re-exports
+its thin ctypes binding under the ABI's names:
+
+    gdn_pre, gdn_scan, gdn_post, gdn_layer,
+    gdn_scan_workspace_bytes, gdn_layer_workspace_bytes, dims, GdnError
+
+``inputs`` draws the seeded synthetic workloads.  Nothing here computes the
+method on the CPU.
+"""
+_BINDING = ("gdn_pre", "gdn_scan", "gdn_post", "gdn_layer", "gdn_scan_workspace_bytes",
+            "gdn_layer_workspace_bytes", "dims", "gdn_dims", "GdnError", "lib", "library_path")
+
+__all__ = list(_BINDING) + ["inputs", "build"]
+
+
+def __getattr__(name):
+    # the binding (and torch) load on first use, so `inputs` stays light
+    if name in _BINDING:
+        from . import _native
+        return getattr(_native, name)
+    raise AttributeError(name)

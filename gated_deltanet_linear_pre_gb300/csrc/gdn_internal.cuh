@@ -1,0 +1,82 @@
+// gdn_internal.cuh -- declarations shared by the library's translation units.
+// Nothing here is part of the public ABI (include/gdn.h is).
+#pragma once
+
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace gdn {
+
+constexpr int kHeadDim = 128;  // dk == dv == 128: one head is 32 lanes x 4 channels
+constexpr int kChunk = 64;     // tokens per scan chunk
+
+struct PreParams {
+    int hk, hv, C, T, n_seq;
+    float eps;
+    const int32_t* cu_seqlens;
+    const __half* qkv;
+    const float* conv_w;
+    const __half* hist_in;
+    __half* hist_out;
+    const __half* a;
+    const __half* b;
+    const float* A_log;
+    const float* dt_bias;
+    float* qn;
+    float* kn;
+    float* vc;
+    float* glog;
+    float* beta;
+};
+
+struct ScanParams {
+    int hk, hv, T, n_seq;
+    const int32_t* cu_seqlens;
+    const float* qn;
+    const float* kn;
+    const float* vc;
+    const float* glog;
+    const float* beta;
+    const float* S_in;
+    float* S_out;
+    float* o;
+    void* workspace;
+    size_t workspace_bytes;
+};
+
+struct PostParams {
+    int hv, T;
+    float eps;
+    const float* o;
+    const __half* z;
+    const float* gamma;
+    int out_f32;
+    void* y;
+};
+
+cudaError_t launch_pre(const PreParams& p, cudaStream_t stream);
+size_t scan_workspace_bytes(int hk, int hv, int n_seq, int T);
+cudaError_t launch_scan(const ScanParams& p, cudaStream_t stream);
+cudaError_t launch_post(const PostParams& p, cudaStream_t stream);
+
+// ---- small device helpers ---------------------------------------------------
+__device__ __forceinline__ float warp_sum(float v)
+{
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
+    return v;
+}
+
+// cu_seqlens[s] clamped into [0, T]: a malformed offsets array gives wrong
+// results, never an out-of-bounds access
+__device__ __forceinline__ int cu_at(const int32_t* cu, int s, int T)
+{
+    return min(max(__ldg(cu + s), 0), T);
+}
+
+__device__ __forceinline__ float sigmoidf_(float x) { return 1.0f / (1.0f + expf(-x)); }
+
+__device__ __forceinline__ float siluf_(float x) { return x / (1.0f + expf(-x)); }
+
+}  // namespace gdn

@@ -1,0 +1,96 @@
+// gdn_post.cu -- stage 3 of the GDN prefill path: gated RMSNorm.
+//
+//   y = o / sqrt(mean(o^2) + eps) * gamma * SiLU(z)    per (token, value head)
+//
+// ("Round 30 Track C Audit: gdn_pre, gdn_post, and gdn_scanr_4", section 1:
+// gdn_post's per-head sum-of-squares reduction and the switch between fp16
+// and fp32 output; "opus_r25_gdn -- round 25 track A", shipped: the sigmoid
+// gate and gamma are loaded before the reduction.)
+//
+// HBM-bound.  One warp per 128-value row: each lane owns 4 consecutive values
+// (16-byte o load, 8-byte z load, 8- or 16-byte y store), the sum of squares
+// is a warp reduction.  Each warp handles kRows rows per iteration with all
+// their loads issued before any arithmetic, in a grid-stride loop over rows.
+#include "gdn_internal.cuh"
+
+namespace gdn {
+namespace {
+
+constexpr int kWarps = 8;
+constexpr int kThreads = kWarps * 32;
+constexpr int kRows = 4;
+
+template <bool kF32>
+__global__ void __launch_bounds__(kThreads) post_kernel(PostParams p, long long n_rows)
+{
+    const int lane = threadIdx.x & 31;
+    const long long warp_global = (long long)blockIdx.x * kWarps + (threadIdx.x >> 5);
+    const long long n_warps = (long long)gridDim.x * kWarps;
+    const float4 gm = __ldg(reinterpret_cast<const float4*>(p.gamma) + lane);
+    const float inv_dv = 1.0f / (float)kHeadDim;
+
+    for (long long r0 = warp_global * kRows; r0 < n_rows; r0 += n_warps * kRows) {
+        float4 ov[kRows];
+        uint2 zv[kRows];
+#pragma unroll
+        for (int i = 0; i < kRows; ++i) {
+            const long long r = r0 + i;
+            if (r < n_rows) {
+                ov[i] = __ldcs(reinterpret_cast<const float4*>(p.o + r * kHeadDim) + lane);
+                zv[i] = __ldcs(reinterpret_cast<const uint2*>(p.z + r * kHeadDim) + lane);
+            } else {
+                ov[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+                zv[i] = make_uint2(0u, 0u);
+            }
+        }
+#pragma unroll
+        for (int i = 0; i < kRows; ++i) {
+            const long long r = r0 + i;
+            const float2 z01 = __half22float2(*reinterpret_cast<__half2*>(&zv[i].x));
+            const float2 z23 = __half22float2(*reinterpret_cast<__half2*>(&zv[i].y));
+            // gate and gamma first, then the reduction
+            const float g0 = gm.x * siluf_(z01.x), g1 = gm.y * siluf_(z01.y);
+            const float g2 = gm.z * siluf_(z23.x), g3 = gm.w * siluf_(z23.y);
+            const float4 o = ov[i];
+            float ss = o.x * o.x + o.y * o.y + o.z * o.z + o.w * o.w;
+            ss = warp_sum(ss);
+            const float inv = 1.0f / sqrtf(ss * inv_dv + p.eps);
+            const float y0 = o.x * inv * g0, y1 = o.y * inv * g1;
+            const float y2 = o.z * inv * g2, y3 = o.w * inv * g3;
+            if (r < n_rows) {
+                if (kF32) {
+                    __stcs(reinterpret_cast<float4*>(static_cast<float*>(p.y) + r * kHeadDim) + lane,
+                           make_float4(y0, y1, y2, y3));
+                } else {
+                    __half2 h01 = __floats2half2_rn(y0, y1), h23 = __floats2half2_rn(y2, y3);
+                    uint2 out;
+                    out.x = *reinterpret_cast<uint32_t*>(&h01);
+                    out.y = *reinterpret_cast<uint32_t*>(&h23);
+                    __stcs(reinterpret_cast<uint2*>(static_cast<__half*>(p.y) + r * kHeadDim) + lane, out);
+                }
+            }
+        }
+    }
+}
+
+}  // namespace
+
+cudaError_t launch_post(const PostParams& p, cudaStream_t stream)
+{
+    const long long n_rows = (long long)p.T * p.hv;
+    if (n_rows == 0) return cudaSuccess;
+    int dev = 0, sms = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    // enough warps for ~8 blocks per SM; each warp then loops over rows
+    const long long want = (n_rows + (long long)kWarps * kRows - 1) / ((long long)kWarps * kRows);
+    const long long cap = (long long)sms * 8;
+    const int grid = (int)(want < cap ? want : cap);
+    if (p.out_f32)
+        post_kernel<true><<<grid, kThreads, 0, stream>>>(p, n_rows);
+    else
+        post_kernel<false><<<grid, kThreads, 0, stream>>>(p, n_rows);
+    return cudaGetLastError();
+}
+
+}  // namespace gdn

@@ -1,0 +1,195 @@
+// gdn_pre.cu -- stage 1 of the GDN prefill path.
+//
+// Width-4 causal depthwise conv over the packed q|k|v channels with a carried
+// 3-token history, SiLU, L2 normalisation of each q/k head, and the gates
+// lam = -exp(A_log) * softplus(a + dt_bias), beta = sigmoid(b).
+// ("Round 30 Track C Audit: gdn_pre, gdn_post, and gdn_scanr_4", section 1:
+// gdn_pre's 4-tap conv loop, its history write at the last token and its
+// per-key-head sum-of-squares reductions; "round 10 track b: gdn
+// vectorization and scan", variants: four multiply-adds per output in tap
+// order, vectorised tap loads, history kept channel by channel.)
+//
+// HBM-bound.  One warp owns one 128-channel head for a block of kTokBlk
+// consecutive tokens: each lane holds 4 channels' taps in registers, reads
+// each qkv row once (8-byte loads, 256 B per warp per row, fully coalesced),
+// slides the 3-token window in registers and writes 16-byte fp32 stores.
+// The q/k norms are warp reductions.  A separate row of blocks writes the
+// carried history of every sequence.
+#include "gdn_internal.cuh"
+
+namespace gdn {
+namespace {
+
+constexpr int kTokBlk = 16;   // tokens per warp task
+constexpr int kWarps = 8;     // warps (heads) per block
+constexpr int kThreads = kWarps * 32;
+
+struct F4 {
+    float x, y, z, w;
+};
+
+__device__ __forceinline__ F4 unpack_half4(uint2 raw)
+{
+    __half2 lo = *reinterpret_cast<__half2*>(&raw.x);
+    __half2 hi = *reinterpret_cast<__half2*>(&raw.y);
+    float2 a = __half22float2(lo), b = __half22float2(hi);
+    return {a.x, a.y, b.x, b.y};
+}
+
+__device__ __forceinline__ F4 load_half4(const __half* p)
+{
+    return unpack_half4(__ldg(reinterpret_cast<const uint2*>(p)));
+}
+
+// The 4 channels [c, c+4) of the input at position `pos` of sequence `seq`
+// (pos < 0 reads the carried history, slot 3 + pos).
+__device__ __forceinline__ F4 tap4(const PreParams& p, int seq, int seq_start, int pos, int c)
+{
+    if (pos >= 0) return load_half4(p.qkv + (size_t)min(seq_start + pos, p.T - 1) * p.C + c);
+    const __half* h = p.hist_in + ((size_t)seq * p.C + c) * 3 + (3 + max(pos, -3));
+    return {__half2float(h[0]), __half2float(h[3]), __half2float(h[6]), __half2float(h[9])};
+}
+
+__device__ __forceinline__ int find_seq(const int32_t* cu, int n_seq, int t)
+{
+    // last s with cu[s] <= t (skips empty sequences)
+    int lo = 0, hi = n_seq - 1;
+    while (lo < hi) {
+        int mid = (lo + hi + 1) >> 1;
+        if (__ldg(cu + mid) <= t) lo = mid; else hi = mid - 1;
+    }
+    return lo;  // in [0, n_seq - 1] whatever cu holds
+}
+
+__device__ __forceinline__ float conv4(float w0, float w1, float w2, float w3, float x0, float x1,
+                                       float x2, float x3)
+{
+    // taps in order: oldest first, current token last
+    float acc = w0 * x0;
+    acc = fmaf(w1, x1, acc);
+    acc = fmaf(w2, x2, acc);
+    acc = fmaf(w3, x3, acc);
+    return acc;
+}
+
+__global__ void __launch_bounds__(kThreads) pre_kernel(PreParams p, int n_slots, int n_tblocks)
+{
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+    if (blockIdx.y == gridDim.y - 1) {
+        // ---- carried history of sequence blockIdx.x: last 3 inputs --------
+        const int s = blockIdx.x;
+        if (s >= p.n_seq) return;
+        const int start = cu_at(p.cu_seqlens, s, p.T);
+        const int len = max(cu_at(p.cu_seqlens, s + 1, p.T) - start, 0);
+        for (int c = threadIdx.x; c < p.C; c += blockDim.x) {
+#pragma unroll
+            for (int i = 0; i < 3; ++i) {
+                const int pos = len - 3 + i;
+                __half v = pos >= 0 ? p.qkv[(size_t)(start + pos) * p.C + c]
+                                    : p.hist_in[((size_t)s * p.C + c) * 3 + (3 + pos)];
+                p.hist_out[((size_t)s * p.C + c) * 3 + i] = v;
+            }
+        }
+        return;
+    }
+
+    const int slot = blockIdx.y * kWarps + warp;  // head slot: q heads | k heads | v heads
+    const int tb = blockIdx.x;
+    if (slot >= n_slots || tb >= n_tblocks) return;
+    const int c = slot * kHeadDim + lane * 4;
+    const int t_begin = tb * kTokBlk;
+    const int t_end = min(p.T, t_begin + kTokBlk);
+
+    // taps of my 4 channels
+    const float4 w0 = __ldg(reinterpret_cast<const float4*>(p.conv_w) + c + 0);
+    const float4 w1 = __ldg(reinterpret_cast<const float4*>(p.conv_w) + c + 1);
+    const float4 w2 = __ldg(reinterpret_cast<const float4*>(p.conv_w) + c + 2);
+    const float4 w3 = __ldg(reinterpret_cast<const float4*>(p.conv_w) + c + 3);
+
+    // issue every row load of the block first (memory-level parallelism);
+    // kept as raw fp16 pairs to hold register use down
+    uint2 cur[kTokBlk];
+#pragma unroll
+    for (int i = 0; i < kTokBlk; ++i)
+        cur[i] = t_begin + i < t_end
+                     ? __ldg(reinterpret_cast<const uint2*>(p.qkv + (size_t)(t_begin + i) * p.C + c))
+                     : make_uint2(0u, 0u);
+
+    const int hk = p.hk;
+    const bool is_q = slot < hk, is_k = !is_q && slot < 2 * hk;
+    const int vh = slot - 2 * hk;  // value head (valid when >= 0)
+
+    int seq = find_seq(p.cu_seqlens, p.n_seq, t_begin);
+    int seq_start = min(cu_at(p.cu_seqlens, seq, p.T), t_begin);
+    int seq_end = cu_at(p.cu_seqlens, seq + 1, p.T);
+    F4 win0, win1, win2;  // inputs at positions pos-3, pos-2, pos-1
+    {
+        const int pos = t_begin - seq_start;
+        win0 = tap4(p, seq, seq_start, pos - 3, c);
+        win1 = tap4(p, seq, seq_start, pos - 2, c);
+        win2 = tap4(p, seq, seq_start, pos - 1, c);
+    }
+
+#pragma unroll
+    for (int i = 0; i < kTokBlk; ++i) {
+        const int t = t_begin + i;
+        if (t >= t_end) break;
+        if (t >= seq_end) {
+            // first token of a new sequence: window comes from that sequence's history
+            while (t >= seq_end && seq + 1 < p.n_seq) {
+                ++seq;
+                seq_start = seq_end;
+                seq_end = cu_at(p.cu_seqlens, seq + 1, p.T);
+            }
+            seq_start = min(seq_start, t);
+            win0 = tap4(p, seq, seq_start, -3, c);
+            win1 = tap4(p, seq, seq_start, -2, c);
+            win2 = tap4(p, seq, seq_start, -1, c);
+        }
+        const F4 x = unpack_half4(cur[i]);
+        float y0 = siluf_(conv4(w0.x, w0.y, w0.z, w0.w, win0.x, win1.x, win2.x, x.x));
+        float y1 = siluf_(conv4(w1.x, w1.y, w1.z, w1.w, win0.y, win1.y, win2.y, x.y));
+        float y2 = siluf_(conv4(w2.x, w2.y, w2.z, w2.w, win0.z, win1.z, win2.z, x.z));
+        float y3 = siluf_(conv4(w3.x, w3.y, w3.z, w3.w, win0.w, win1.w, win2.w, x.w));
+        win0 = win1;
+        win1 = win2;
+        win2 = x;
+        float* dst;
+        if (vh >= 0) {
+            dst = p.vc + ((size_t)t * p.hv + vh) * kHeadDim + lane * 4;
+        } else {
+            float ss = y0 * y0 + y1 * y1 + y2 * y2 + y3 * y3;
+            ss = warp_sum(ss);
+            const float inv = 1.0f / sqrtf(ss + p.eps);
+            y0 *= inv; y1 *= inv; y2 *= inv; y3 *= inv;
+            const int j = is_q ? slot : slot - hk;
+            dst = (is_k ? p.kn : p.qn) + ((size_t)t * hk + j) * kHeadDim + lane * 4;
+        }
+        *reinterpret_cast<float4*>(dst) = make_float4(y0, y1, y2, y3);
+    }
+
+    // gates of value head vh for the block's tokens: one lane per token
+    if (vh >= 0 && lane < t_end - t_begin) {
+        const int t = t_begin + lane;
+        const float av = __half2float(p.a[(size_t)t * p.hv + vh]) + __ldg(p.dt_bias + vh);
+        const float bv = __half2float(p.b[(size_t)t * p.hv + vh]);
+        const float sp = fmaxf(av, 0.0f) + log1pf(expf(-fabsf(av)));  // softplus
+        p.glog[(size_t)t * p.hv + vh] = -expf(__ldg(p.A_log + vh)) * sp;
+        p.beta[(size_t)t * p.hv + vh] = sigmoidf_(bv);
+    }
+}
+
+}  // namespace
+
+cudaError_t launch_pre(const PreParams& p, cudaStream_t stream)
+{
+    const int n_slots = 2 * p.hk + p.hv;
+    const int n_tblocks = (p.T + kTokBlk - 1) / kTokBlk;
+    const int head_groups = (n_slots + kWarps - 1) / kWarps;
+    dim3 grid((unsigned)max(max(n_tblocks, p.n_seq), 1), (unsigned)(head_groups + 1));
+    pre_kernel<<<grid, kThreads, 0, stream>>>(p, n_slots, n_tblocks);
+    return cudaGetLastError();
+}
+
+}  // namespace gdn

@@ -1,0 +1,186 @@
+/*
+ * gdn.h -- C ABI of the Gated DeltaNet (GDN) prompt-prefill library for one
+ * NVIDIA GB300 GPU (sm_103a).
+ *
+ * The path has three stages, after the three kernels the pages benchmark
+ * ("Round 30 Track C Audit: gdn_pre, gdn_post, and gdn_scanr_4", sections 1
+ * and 2: gdn_pre, the gdn_scan_r recurrence and gdn_post, timed separately
+ * and as one pre+scan+post total over 36 layers):
+ *
+ *   gdn_pre   width-4 causal depthwise conv over the packed q|k|v channels
+ *             with a carried 3-token history, SiLU, L2 normalisation of every
+ *             q and k head (eps), and the per-(token, value head) gates
+ *             lam = log g = -exp(A_log) * softplus(a + dt_bias),
+ *             beta = sigmoid(b).
+ *   gdn_scan  the gated delta rule, per value head h with key head
+ *             h / (hv/hk) and fp32 state S in R^{dk x dv}:
+ *               S <- g S;  u = beta (v - S^T k);  S <- S + k u^T;
+ *               o = S^T q / sqrt(dk).
+ *   gdn_post  y = o / sqrt(mean(o^2) + eps) * gamma * SiLU(z), fp16 or fp32.
+ *   gdn_layer the three stages back to back on one stream.
+ *
+ * Conventions shared by every entry point
+ * ----------------------------------------
+ *  - Every array pointer is a DEVICE pointer (memory of the current CUDA
+ *    device), owned by the caller, dense and row-major in the layout stated.
+ *    The library allocates no device memory and keeps no pointer after the
+ *    call returns; the work runs asynchronously on `stream` (NULL = legacy
+ *    default stream), so buffers must stay valid until the stream reaches it.
+ *  - fp16 arrays are IEEE binary16 bit patterns (uint16_t).
+ *  - Shapes: hk key heads, hv value heads (hv a multiple of hk), dk = dv =
+ *    128, C = 2*hk*dk + hv*dv packed channels ordered q (hk heads) | k (hk
+ *    heads) | v (hv heads).  T = total tokens of a packed variable-length
+ *    batch of n_seq sequences; sequence s owns tokens
+ *    [cu_seqlens[s], cu_seqlens[s+1]).  cu_seqlens is a DEVICE int32 array of
+ *    n_seq+1 entries, non-decreasing, cu_seqlens[0] = 0,
+ *    cu_seqlens[n_seq] = T (not read on the host; a violation is undefined).
+ *    Zero-length sequences are allowed: their history and state pass
+ *    through unchanged.
+ *  - Every pointer must be 16-byte aligned.
+ *  - Errors: argument problems are detected on the host before anything is
+ *    launched and return a status with nothing enqueued.  A failed launch
+ *    returns GDN_ERR_CUDA (the CUDA error string is kept for
+ *    gdn_last_error_string).  Asynchronous faults surface at the caller's
+ *    next synchronisation, as with any CUDA library.
+ *  - Thread safety: calls may be made from several host threads on
+ *    different streams; they share no mutable state except the last-error
+ *    string, which is per host thread.
+ */
+#ifndef GDN_H
+#define GDN_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+struct CUstream_st; /* cudaStream_t is `struct CUstream_st *` */
+
+#if defined(__GNUC__)
+#define GDN_API __attribute__((visibility("default")))
+#else
+#define GDN_API
+#endif
+
+typedef enum gdn_status {
+    GDN_OK = 0,
+    GDN_ERR_INVALID_ARG = 1, /* null pointer, negative size, overlap, bad value */
+    GDN_ERR_UNSUPPORTED = 2, /* shape outside what the kernels implement       */
+    GDN_ERR_ALIGNMENT = 3,   /* a pointer is not 16-byte aligned               */
+    GDN_ERR_WORKSPACE = 4,   /* workspace missing or smaller than required     */
+    GDN_ERR_CUDA = 5         /* a CUDA runtime call or launch failed            */
+} gdn_status;
+
+/* Model shape.  Implemented: dk == dv == 128, 1 <= hk, hv % hk == 0,
+ * hv <= 4096, eps > 0 (the pages' layer: hk=16, hv=48, eps=1e-6 -- "round 10
+ * track b: gdn vectorization and scan", source and execution). */
+typedef struct gdn_dims {
+    int32_t hk;  /* key (and query) heads                              */
+    int32_t hv;  /* value heads                                        */
+    int32_t dk;  /* key head dimension (128)                           */
+    int32_t dv;  /* value head dimension (128)                         */
+    float eps;   /* epsilon of the L2 norms and of the RMSNorm         */
+} gdn_dims;
+
+/* Human-readable name of a status code (static storage). */
+GDN_API const char* gdn_status_string(gdn_status s);
+
+/* Detail of the last non-OK status returned on this host thread. */
+GDN_API const char* gdn_last_error_string(void);
+
+/*
+ * gdn_pre -- stage 1 ("Round 30 Track C Audit", section 1, gdn_pre: the
+ * 4-tap conv loop, the history write at the last token, the per-key-head
+ * q/k sum-of-squares reductions; "round 10 track b", variants: each conv
+ * output is four multiply-adds in tap order, history kept channel by
+ * channel).
+ *
+ * In:  qkv      fp16 [T][C]             raw projections, q | k | v
+ *      conv_w   fp32 [C][4]             taps; tap 3 multiplies the current
+ *                                       token, tap 0 the token 3 back
+ *      hist_in  fp16 [n_seq][C][3]      the 3 inputs before each sequence,
+ *                                       oldest first
+ *      a, b     fp16 [T][hv]            gate pre-activations
+ *      A_log, dt_bias fp32 [hv]
+ * Out: hist_out fp16 [n_seq][C][3]      last 3 inputs of each sequence
+ *                                       (old history shifted in when the
+ *                                       sequence is shorter than 3); bit
+ *                                       copies, never rounded.  Must not
+ *                                       overlap hist_in.
+ *      qn, kn   fp32 [T][hk][dk]        SiLU(conv) / sqrt(|.|^2 + eps)
+ *      vc       fp32 [T][hv][dv]        SiLU(conv) of the v channels
+ *      glog     fp32 [T][hv]            lam = log g (<= 0)
+ *      beta     fp32 [T][hv]            sigmoid(b)
+ */
+GDN_API gdn_status gdn_pre(const gdn_dims* dims, int32_t n_seq, int32_t total_tokens,
+                   const int32_t* cu_seqlens, const uint16_t* qkv, const float* conv_w,
+                   const uint16_t* hist_in, uint16_t* hist_out, const uint16_t* a,
+                   const uint16_t* b, const float* A_log, const float* dt_bias, float* qn,
+                   float* kn, float* vc, float* glog, float* beta, struct CUstream_st* stream);
+
+/* Workspace bytes gdn_scan needs for this batch shape (0 is a valid answer). */
+GDN_API size_t gdn_scan_workspace_bytes(const gdn_dims* dims, int32_t n_seq, int32_t total_tokens);
+
+/*
+ * gdn_scan -- stage 2, the gated delta-rule recurrence ("Round 30 Track C
+ * Audit", section 1: gdn_scan_r keeps the fp32 state on chip, decays and
+ * updates it per token and forms the k and q products against it).
+ * Computed chunk-wise (64 tokens), exact in exact arithmetic.
+ *
+ * In:  qn, kn   fp32 [T][hk][dk]        unit-norm q and k (as gdn_pre writes)
+ *      vc       fp32 [T][hv][dv]
+ *      glog     fp32 [T][hv]            log-decay, <= 0 (-inf allowed: g = 0)
+ *      beta     fp32 [T][hv]
+ *      S_in     fp32 [n_seq][hv][dk][dv]  state before each sequence
+ * Out: S_out    fp32 [n_seq][hv][dk][dv]  state after each sequence; may be
+ *                                       the same buffer as S_in
+ *      o        fp32 [T][hv][dv]        S^T q / sqrt(dk) after each token
+ * workspace: device scratch of at least gdn_scan_workspace_bytes() bytes
+ *            (may be NULL when that is 0); contents on entry are ignored.
+ */
+GDN_API gdn_status gdn_scan(const gdn_dims* dims, int32_t n_seq, int32_t total_tokens,
+                    const int32_t* cu_seqlens, const float* qn, const float* kn,
+                    const float* vc, const float* glog, const float* beta, const float* S_in,
+                    float* S_out, float* o, void* workspace, size_t workspace_bytes,
+                    struct CUstream_st* stream);
+
+/*
+ * gdn_post -- stage 3, gated RMSNorm ("Round 30 Track C Audit", section 1,
+ * gdn_post: per-head sum-of-squares reduction and the f32 output switch;
+ * "opus_r25_gdn -- round 25 track A", shipped: the sigmoid gate and gamma).
+ *
+ * In:  o        fp32 [T][hv][dv]
+ *      z        fp16 [T][hv][dv]
+ *      gamma    fp32 [dv]               shared by all heads
+ * Out: y        fp16 [T][hv][dv] when out_f32 == 0, else fp32 [T][hv][dv]
+ */
+GDN_API gdn_status gdn_post(const gdn_dims* dims, int32_t total_tokens, const float* o,
+                    const uint16_t* z, const float* gamma, int32_t out_f32, void* y,
+                    struct CUstream_st* stream);
+
+/* Workspace bytes gdn_layer needs: the stage tensors qn, kn, vc, glog, beta,
+ * o plus the scan's own workspace, each 256-byte aligned. */
+GDN_API size_t gdn_layer_workspace_bytes(const gdn_dims* dims, int32_t n_seq, int32_t total_tokens);
+
+/*
+ * gdn_layer -- the whole prefill layer: gdn_pre, gdn_scan and gdn_post on
+ * `stream`, the stage tensors kept in `workspace` (the pages time the three
+ * stages back to back as one pre+scan+post total, "Round 30 Track C Audit",
+ * section 2).  Arguments as in the three stage calls.  S_out may equal S_in;
+ * hist_out must not overlap hist_in.
+ */
+GDN_API gdn_status gdn_layer(const gdn_dims* dims, int32_t n_seq, int32_t total_tokens,
+                     const int32_t* cu_seqlens, const uint16_t* qkv, const float* conv_w,
+                     const uint16_t* hist_in, uint16_t* hist_out, const uint16_t* a,
+                     const uint16_t* b, const uint16_t* z, const float* A_log,
+                     const float* dt_bias, const float* gamma, const float* S_in, float* S_out,
+                     int32_t out_f32, void* y, void* workspace, size_t workspace_bytes,
+                     struct CUstream_st* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GDN_H */

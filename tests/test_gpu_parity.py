@@ -1,0 +1,206 @@
+"""GPU parity: the CUDA path, called through the C ABI, against the fp64 oracle
+on the same seeded inputs.
+
+Metric per output tensor: max |gpu - oracle| / max |oracle|.  Bars: fp16
+outputs 2e-3, fp32 outputs and the final fp32 state 1e-4, carried conv
+history bit-exact.
+"""
+import numpy as np
+import pytest
+
+import oracle
+from gated_deltanet_linear_pre_gb300 import inputs as gin
+
+pytestmark = pytest.mark.gpu
+
+torch = pytest.importorskip("torch")
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from gated_deltanet_linear_pre_gb300 import build
+    build.build()
+
+
+def U():
+    import gpu_util
+    return gpu_util
+
+
+# ---- stage 1 ---------------------------------------------------------------------
+PRE_CASES = {
+    "t37": lambda: gin.single_layer_t37(),
+    "t1_hist": lambda: gin.single_layer_boundary(1, False),
+    "t3_hist": lambda: gin.single_layer_boundary(3, False),
+    "t300_hist": lambda: gin.single_layer_boundary(300, False),
+    "varlen_small": lambda: gin.make_layer(5, [5, 0, 1, 2, 70, 3, 17], hist_nonzero=True, S0_std=0.02),
+}
+
+
+@pytest.mark.parametrize("case", list(PRE_CASES))
+def test_pre_matches_oracle(case):
+    u = U()
+    inp = PRE_CASES[case]()
+    ref = oracle.layer(inp, heads=[0])
+    got = u.run_pre(inp)
+    for key in ("q", "k", "v", "beta"):
+        assert u.max_rel(got[key], ref[key]) <= u.TOL_STAGE, key
+    assert u.max_rel(got["lam"], ref["lam"]) <= u.TOL_STAGE
+    np.testing.assert_array_equal(got["hist_out"].view(np.uint16), inp_hist_bits(ref["hist_out"]))
+
+
+def inp_hist_bits(h64):
+    # history values are copies of fp16 inputs, so fp64 -> fp16 is exact
+    h16 = h64.astype(np.float16)
+    assert np.array_equal(h16.astype(np.float64), h64)
+    return h16.view(np.uint16)
+
+
+# ---- stage 2 (isolated: oracle stage tensors in, as fp32) -----------------------
+def _scan_case(inp, heads=None):
+    u = U()
+    ref_pre = oracle.layer(inp, heads=[0])
+    f32 = lambda a: np.asarray(a, np.float32)
+    q, k, v, lam, beta = (f32(ref_pre[x]) for x in ("q", "k", "v", "lam", "beta"))
+    S0 = f32(inp.S0)
+    # the oracle runs on exactly the fp32 values the GPU receives
+    cu = inp.cu_seqlens
+    o_ref = np.full(v.shape, np.nan)
+    S_ref = np.full(S0.shape, np.nan)
+    for s in range(inp.n_seq):
+        sl = slice(int(cu[s]), int(cu[s + 1]))
+        o_s, S_s = oracle.scan(q[sl], k[sl], v[sl], np.exp(lam[sl].astype(np.float64)), beta[sl], S0[s],
+                               heads=heads)
+        o_ref[sl] = o_s
+        S_ref[s] = S_s
+    o, S = u.run_scan(u.dims_of(inp), cu, q, k, v, lam, beta, S0)
+    return o, S, o_ref, S_ref
+
+
+@pytest.mark.parametrize("T", [1, 3, 37, 64, 65, 300, 512])
+def test_scan_matches_oracle(T):
+    u = U()
+    inp = gin.single_layer_boundary(T, True) if T != 37 else gin.single_layer_t37()
+    o, S, o_ref, S_ref = _scan_case(inp)
+    assert u.max_rel(o, o_ref) <= u.TOL_F32
+    assert u.max_rel(S, S_ref) <= u.TOL_F32
+
+
+def test_scan_varlen_with_empty_sequences():
+    u = U()
+    inp = gin.make_layer(6, [0, 130, 1, 0, 64, 200], hist_nonzero=True, S0_std=0.02)
+    o, S, o_ref, S_ref = _scan_case(inp)
+    assert u.max_rel(o, o_ref) <= u.TOL_F32
+    assert u.max_rel(S, S_ref) <= u.TOL_F32
+    # empty sequences pass their state through untouched
+    np.testing.assert_array_equal(S[0], inp.S0[0])
+    np.testing.assert_array_equal(S[3], inp.S0[3])
+
+
+def test_scan_in_place_state():
+    u = U()
+    inp = gin.single_layer_boundary(300, True)
+    ref_pre = oracle.layer(inp, heads=[0])
+    f32 = lambda a: np.asarray(a, np.float32)
+    args = [f32(ref_pre[x]) for x in ("q", "k", "v", "lam", "beta")]
+    d = u.dims_of(inp)
+    o1, S1 = u.run_scan(d, inp.cu_seqlens, *args, f32(inp.S0))
+    o2, S2 = u.run_scan(d, inp.cu_seqlens, *args, f32(inp.S0), in_place=True)
+    np.testing.assert_array_equal(o1, o2)
+    np.testing.assert_array_equal(S1, S2)
+
+
+def test_scan_degenerate_gates():
+    # g = 0 (log-decay -inf) resets the state; beta = 0 leaves pure decay
+    u = U()
+    inp = gin.single_layer_boundary(150, True)
+    ref = oracle.layer(inp, heads=[0])
+    f32 = lambda a: np.asarray(a, np.float32)
+    q, k, v = f32(ref["q"]), f32(ref["k"]), f32(ref["v"])
+    lam, beta = f32(ref["lam"]).copy(), f32(ref["beta"]).copy()
+    lam[::7] = -np.inf
+    beta[3::5] = 0.0
+    o, S = u.run_scan(u.dims_of(inp), inp.cu_seqlens, q, k, v, lam, beta, f32(inp.S0))
+    o_ref, S_ref = oracle.scan(q, k, v, np.exp(lam.astype(np.float64)), beta, f32(inp.S0)[0])
+    assert np.isfinite(o).all() and np.isfinite(S).all()
+    assert u.max_rel(o, o_ref) <= u.TOL_F32
+    assert u.max_rel(S[0], S_ref) <= u.TOL_F32
+
+
+# ---- stage 3 (isolated) --------------------------------------------------------------
+@pytest.mark.parametrize("out_f32", [False, True])
+@pytest.mark.parametrize("T", [1, 37, 300])
+def test_post_matches_oracle(T, out_f32):
+    u = U()
+    rng = np.random.default_rng(T)
+    o = (rng.standard_normal((T, 48, 128)) * rng.uniform(0.01, 3.0, (T, 48, 1))).astype(np.float32)
+    inp = gin.single_layer_boundary(T, out_f32)
+    y = u.run_post(u.dims_of(inp), o, inp.z, inp.gamma, out_f32)
+    y_ref = oracle.post(o, inp.z, inp.gamma, 1e-6)
+    assert u.max_rel(y, y_ref) <= (u.TOL_F32 if out_f32 else u.TOL_F16)
+
+
+# ---- whole layer ------------------------------------------------------------------------
+def _check_layer(inp, heads=None):
+    u = U()
+    got = u.run_layer(inp)
+    ref = oracle.layer(inp, heads=heads)
+    hsel = slice(None) if heads is None else list(heads)
+    tol = u.TOL_F32 if inp.out_f32 else u.TOL_F16
+    assert u.max_rel(got["y"][:, hsel], ref["y"][:, hsel]) <= tol
+    assert u.max_rel(got["S_out"][:, hsel], ref["S_out"][:, hsel]) <= u.TOL_F32
+    np.testing.assert_array_equal(got["hist_out"].view(np.uint16), inp_hist_bits(ref["hist_out"]))
+    return got, ref
+
+
+def test_layer_t37():
+    _check_layer(gin.single_layer_t37())
+
+
+@pytest.mark.parametrize("out_f32", [False, True])
+@pytest.mark.parametrize("T", [1, 3, 300, 512])
+def test_layer_boundary_lengths(T, out_f32):
+    _check_layer(gin.single_layer_boundary(T, out_f32))
+
+
+@pytest.mark.parametrize("out_f32", [False, True])
+def test_layer_varlen_batch(out_f32):
+    _check_layer(gin.varlen_batch(out_f32=out_f32))
+
+
+def test_layer_empty_batch_passes_state_through():
+    u = U()
+    inp = gin.make_layer(9, [0, 0], hist_nonzero=True, S0_std=0.02)
+    got = u.run_layer(inp)
+    np.testing.assert_array_equal(got["hist_out"], inp.hist)
+    np.testing.assert_array_equal(got["S_out"], inp.S0)
+
+
+def test_layer_in_place_state_and_resume():
+    # S_out may alias S_in; and two calls chained through the returned history
+    # and state equal one call over the concatenation
+    u = U()
+    full = gin.make_layer(12, [300], hist_nonzero=True, S0_std=0.02)
+    one = u.run_layer(full, in_place_state=True)
+    ref = u.run_layer(full)
+    np.testing.assert_array_equal(one["S_out"], ref["S_out"])
+    T1 = 131
+
+    def part(sl, hist, S0):
+        return gin.LayerInputs(qkv=full.qkv[sl], conv_w=full.conv_w, hist=hist, a=full.a[sl], b=full.b[sl],
+                               A_log=full.A_log, dt_bias=full.dt_bias, z=full.z[sl], gamma=full.gamma,
+                               S0=S0, cu_seqlens=np.array([0, sl.stop - sl.start], np.int32))
+
+    r1 = u.run_layer(part(slice(0, T1), full.hist, full.S0))
+    r2 = u.run_layer(part(slice(T1, 300), r1["hist_out"], r1["S_out"]))
+    np.testing.assert_array_equal(r2["hist_out"], ref["hist_out"])
+    assert u.max_rel(r2["S_out"], ref["S_out"]) <= u.TOL_F32
+    assert u.max_rel(np.concatenate([r1["y"], r2["y"]]), ref["y"]) <= u.TOL_F16
+
+
+def test_layer_long_prompt_decays_near_one():
+    # T = 32768, g close to 1: fp32 state accumulation over the whole prompt,
+    # final state and sampled heads' outputs against the fp64 oracle
+    _check_layer(gin.long_prompt(), heads=list(range(0, 48, 5)))
