@@ -34,7 +34,8 @@ sys.path.insert(0, ROOT)
 
 from gated_deltanet_linear_pre_gb300 import inputs as gin  # noqa: E402
 
-LAYERS = 36
+LAYERS = 36          # layers actually run (``--layers`` lowers it for profiling only)
+METRIC_LAYERS = 36   # layers of the stack the metric is defined on
 T_PROMPT = 2048
 HK, HV, DK, DV = gin.HK, gin.HV, gin.DK, gin.DV
 C = gin.channels()
@@ -59,6 +60,8 @@ def parse():
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--layers", type=int, default=LAYERS,
+                    help="layers in the stack (fewer only for profiling captures; the metric is 36)")
     return ap.parse_args()
 
 
@@ -82,10 +85,10 @@ def barrier(world: int):
         dist.barrier()
 
 
-def make_layers(rank: int):
+def make_layers(rank: int, n_layers: int = LAYERS):
     # replicas on different ranks draw different seeds (independent prompts)
     with ThreadPoolExecutor(max_workers=min(16, os.cpu_count() or 1)) as ex:
-        return list(ex.map(lambda l: gin.stack_layer(l + 1000 * rank), range(LAYERS)))
+        return list(ex.map(lambda l: gin.stack_layer(l + 1000 * rank), range(n_layers)))
 
 
 # ---- clocks --------------------------------------------------------------------------
@@ -169,7 +172,7 @@ def cpu_baseline(layers_np, tokens: int, n_layers: int):
         oracle.layer(sub)
     dt = time.perf_counter() - t0
     # tokens through the whole 36-layer stack per second
-    value = tokens * n_layers / dt / LAYERS
+    value = tokens * n_layers / dt / METRIC_LAYERS
     return {"value": value, "unit": "tokens/s", "cores": oracle.threads(), "kind": "oracle",
             "sample": f"{n_layers} of the 36 layers x first {tokens} tokens, all 48 heads, fp64 token-sequential "
                       f"oracle ({dt:.1f} s wall), scaled to the 36-layer stack"}
@@ -195,7 +198,7 @@ def run_reference(args, rank, world):
             times.append(dt)
     # one step = one layer x `tokens`; the stack needs 36 such layers per token
     per_layer = sum(times) / len(times)
-    value = tokens / (per_layer * LAYERS)
+    value = tokens / (per_layer * METRIC_LAYERS)
     sample = f"each step: one layer x first {tokens} tokens of the T=2048 workload, all 48 heads, fp64 oracle"
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": per_layer * 1e3,
@@ -236,7 +239,9 @@ def main():
     dev = torch.device("cuda", local)
     d = gdn.dims(HK, HV, DK, DV, 1e-6)
 
-    layers_np = make_layers(rank)
+    global LAYERS
+    LAYERS = args.layers
+    layers_np = make_layers(rank, LAYERS)
     pin = lambda a: torch.from_numpy(np.ascontiguousarray(a)).pin_memory()
     host = [dict(qkv=pin(L.qkv), conv_w=pin(L.conv_w), hist=pin(L.hist), a=pin(L.a), b=pin(L.b),
                  A_log=pin(L.A_log), dt_bias=pin(L.dt_bias), z=pin(L.z), gamma=pin(L.gamma), S0=pin(L.S0))
@@ -356,7 +361,7 @@ def main():
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        cpu = cpu_baseline(layers_np, T, 3)
+        cpu = cpu_baseline(layers_np, T, min(18, LAYERS))
 
     if rank == 0:
         line = {"metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,

@@ -9,8 +9,8 @@
 //
 // HBM-bound.  One warp per 128-value row: each lane owns 4 consecutive values
 // (16-byte o load, 8-byte z load, 8- or 16-byte y store), the sum of squares
-// is a warp reduction.  Each warp handles kRows rows per iteration with all
-// their loads issued before any arithmetic, in a grid-stride loop over rows.
+// is a warp reduction.  Each warp handles kRows rows with all their loads
+// issued before any arithmetic; the grid covers every row once.
 #include "gdn_internal.cuh"
 
 namespace gdn {
@@ -26,7 +26,6 @@ __global__ void __launch_bounds__(kThreads) post_kernel(PostParams p, long long 
     const int lane = threadIdx.x & 31;
     const long long warp_global = (long long)blockIdx.x * kWarps + (threadIdx.x >> 5);
     const long long n_warps = (long long)gridDim.x * kWarps;
-    const float4 gm = __ldg(reinterpret_cast<const float4*>(p.gamma) + lane);
     const float inv_dv = 1.0f / (float)kHeadDim;
 
     for (long long r0 = warp_global * kRows; r0 < n_rows; r0 += n_warps * kRows) {
@@ -43,6 +42,7 @@ __global__ void __launch_bounds__(kThreads) post_kernel(PostParams p, long long 
                 zv[i] = make_uint2(0u, 0u);
             }
         }
+        const float4 gm = __ldg(reinterpret_cast<const float4*>(p.gamma) + lane);
 #pragma unroll
         for (int i = 0; i < kRows; ++i) {
             const long long r = r0 + i;
@@ -79,13 +79,10 @@ cudaError_t launch_post(const PostParams& p, cudaStream_t stream)
 {
     const long long n_rows = (long long)p.T * p.hv;
     if (n_rows == 0) return cudaSuccess;
-    int dev = 0, sms = 0;
-    cudaGetDevice(&dev);
-    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-    // enough warps for ~8 blocks per SM; each warp then loops over rows
+    // one pass of kRows rows per warp; the grid-stride loop only engages for
+    // batches beyond 2^31 blocks
     const long long want = (n_rows + (long long)kWarps * kRows - 1) / ((long long)kWarps * kRows);
-    const long long cap = (long long)sms * 8;
-    const int grid = (int)(want < cap ? want : cap);
+    const int grid = (int)(want < 0x7fffffffLL ? want : 0x7fffffffLL);
     if (p.out_f32)
         post_kernel<true><<<grid, kThreads, 0, stream>>>(p, n_rows);
     else

@@ -20,9 +20,10 @@
 namespace gdn {
 namespace {
 
-constexpr int kTokBlk = 16;   // tokens per warp task
+constexpr int kTokBlk = 8;    // tokens per warp task
 constexpr int kWarps = 8;     // warps (heads) per block
 constexpr int kThreads = kWarps * 32;
+constexpr int kHistThreads = kThreads;  // one history channel per thread
 
 struct F4 {
     float x, y, z, w;
@@ -72,31 +73,34 @@ __device__ __forceinline__ float conv4(float w0, float w1, float w2, float w3, f
     return acc;
 }
 
-__global__ void __launch_bounds__(kThreads) pre_kernel(PreParams p, int n_slots, int n_tblocks)
+__global__ void __launch_bounds__(kThreads, 4)
+pre_kernel(PreParams p, int n_slots, int head_groups, int n_conv_blocks)
 {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
-    if (blockIdx.y == gridDim.y - 1) {
-        // ---- carried history of sequence blockIdx.x: last 3 inputs --------
-        const int s = blockIdx.x;
+    if ((int)blockIdx.x >= n_conv_blocks) {
+        // ---- carried history: the last 3 inputs of sequence s, channel c --
+        const long long idx = (long long)(blockIdx.x - n_conv_blocks) * kHistThreads + threadIdx.x;
+        const int s = (int)(idx / p.C), c = (int)(idx % p.C);
         if (s >= p.n_seq) return;
         const int start = cu_at(p.cu_seqlens, s, p.T);
         const int len = max(cu_at(p.cu_seqlens, s + 1, p.T) - start, 0);
-        for (int c = threadIdx.x; c < p.C; c += blockDim.x) {
+        __half v[3];
 #pragma unroll
-            for (int i = 0; i < 3; ++i) {
-                const int pos = len - 3 + i;
-                __half v = pos >= 0 ? p.qkv[(size_t)(start + pos) * p.C + c]
-                                    : p.hist_in[((size_t)s * p.C + c) * 3 + (3 + pos)];
-                p.hist_out[((size_t)s * p.C + c) * 3 + i] = v;
-            }
+        for (int i = 0; i < 3; ++i) {  // all loads first, then the stores
+            const int pos = len - 3 + i;
+            v[i] = pos >= 0 ? p.qkv[(size_t)(start + pos) * p.C + c]
+                            : p.hist_in[((size_t)s * p.C + c) * 3 + (3 + pos)];
         }
+#pragma unroll
+        for (int i = 0; i < 3; ++i) p.hist_out[((size_t)s * p.C + c) * 3 + i] = v[i];
         return;
     }
 
-    const int slot = blockIdx.y * kWarps + warp;  // head slot: q heads | k heads | v heads
-    const int tb = blockIdx.x;
-    if (slot >= n_slots || tb >= n_tblocks) return;
+    // head slot (q heads | k heads | v heads) and token block of this warp
+    const int slot = (blockIdx.x % head_groups) * kWarps + warp;
+    const int tb = blockIdx.x / head_groups;
+    if (slot >= n_slots) return;
     const int c = slot * kHeadDim + lane * 4;
     const int t_begin = tb * kTokBlk;
     const int t_end = min(p.T, t_begin + kTokBlk);
@@ -185,10 +189,14 @@ __global__ void __launch_bounds__(kThreads) pre_kernel(PreParams p, int n_slots,
 cudaError_t launch_pre(const PreParams& p, cudaStream_t stream)
 {
     const int n_slots = 2 * p.hk + p.hv;
-    const int n_tblocks = (p.T + kTokBlk - 1) / kTokBlk;
+    const long long n_tblocks = (p.T + kTokBlk - 1) / kTokBlk;
     const int head_groups = (n_slots + kWarps - 1) / kWarps;
-    dim3 grid((unsigned)max(max(n_tblocks, p.n_seq), 1), (unsigned)(head_groups + 1));
-    pre_kernel<<<grid, kThreads, 0, stream>>>(p, n_slots, n_tblocks);
+    const long long n_conv_blocks = n_tblocks * head_groups;
+    const long long n_hist_blocks = ((long long)p.n_seq * p.C + kHistThreads - 1) / kHistThreads;
+    const long long blocks = n_conv_blocks + n_hist_blocks;
+    if (blocks == 0) return cudaSuccess;
+    if (blocks > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
+    pre_kernel<<<(unsigned)blocks, kThreads, 0, stream>>>(p, n_slots, head_groups, (int)n_conv_blocks);
     return cudaGetLastError();
 }
 
