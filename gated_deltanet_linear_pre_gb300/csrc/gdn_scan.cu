@@ -8,154 +8,604 @@
 // and forms the k and q products against it.)
 //
 // Chunk algebra (exact in exact arithmetic; 64-token chunks, S0 = state at
-// the chunk start, G_i = running sum of lam = log g inside the chunk):
+// the chunk start, G_i = running sum of lam = log g inside the chunk, L the
+// last row):
 //   A_ij = beta_i e^{G_i-G_j} (k_i.k_j) (j < i),   T = (I + A)^-1
 //   P_ij = e^{G_i-G_j} (q_i.k_j) / sqrt(dk) (j <= i)
 //   X    = beta (V - e^G (K S0))                   U = T X
-//   O    = e^G (Q S0) / sqrt(dk) + P U             S = e^{G_L} S0 + Kd^T U
-// with Kd = diag(e^{G_L - G_j}) K.  Every dense product runs on the tensor
-// core with bf16 operands split as x = hi + lo (hi = bf16(x), lo = bf16(x -
-// hi)) and three MMAs hi*hi + hi*lo + lo*hi accumulated in fp32 in TMEM,
-// which keeps ~16 significant bits per operand.  Two products are stacked to
-// fill the M = 128 rows of one MMA:
+//   O    = e^G (Q S0) / sqrt(dk) + P U             S = e^{G_L} S0 + K^T (e^{G_L-G} U)
+// Every dense product runs on the tensor core with bf16 operands split as
+// x = hi + lo (hi = bf16(x), lo = bf16(x - hi)) and three MMAs hi*hi + hi*lo
+// + lo*hi accumulated in fp32 in TMEM (about 16 significant bits per operand).
+// Products are stacked to fill the 128 rows of one MMA:
 //   [K; Q] K^T -> (K K^T ; Q K^T)          [I; P] T -> (T ; P T)
 //   [K; Q] S0  -> (K S0 ; Q S0)            [T; P T] X -> (U ; P U)
-//   Kd^T U     -> the state update
 // so (Q S0) and (P U) land in the same TMEM lanes and O needs no exchange.
-// The 64x64 unit lower-triangular inverse is a blocked forward substitution
-// (16x16 diagonal blocks, then off-diagonal blocks by distance) on CUDA cores.
 //
-// One CTA (128 threads, thread i <-> TMEM lane i) owns DVS value columns of
-// one (sequence, value head) and carries its fp32 state slice in registers
-// through every chunk of the sequence.  Each MMA is issued by thread 0 and
-// completes on an mbarrier; every wait is bounded and, on expiry, the CTA
-// records an error code in the workspace and stops.
+// Two kernels:
+//  * scan_prep_kernel, one CTA per (chunk, value head), fully parallel: the
+//    state-independent part.  It splits [K; Q] into the tensor-core layout,
+//    forms K K^T and Q K^T, A and P, inverts I + A (blocked forward
+//    substitution on CUDA cores, 16x16 diagonal blocks), forms [T; P T] and
+//    writes two operand images to the workspace: [T; P T] per (chunk, value
+//    head) and [K; Q] per (chunk, key head).
+//  * scan_chain_kernel, one CTA per (sequence, value head, 64-column slice):
+//    the state-dependent part, chunk after chunk, with the fp32 state slice
+//    in registers.  The images stream in with bulk asynchronous copies one
+//    chunk ahead ([K; Q] double-buffered), V and the gates through registers
+//    one chunk ahead, so each chunk costs three MMA groups and three short
+//    CUDA-core phases.  K^T for the state update is
+//    the K half of the [K; Q] image read through an MN-major descriptor.
+//
+// Every MMA is issued by one thread and completes on an mbarrier; every wait
+// is bounded and, on expiry, the CTA records an error code in the workspace,
+// drains its own copies in flight (bounded), frees its TMEM and stops.
 #include "gdn_internal.cuh"
 #include "umma.cuh"
 
 namespace gdn {
 namespace {
 
-constexpr int kThreads = 128;
 constexpr float kLamFloor = -110.0f;  // e^-110 is below the smallest fp32 denormal: g = 0 exactly
 constexpr uint32_t kErrTimeout = 1u;
+constexpr size_t kAmBytes = 128 * 64 * 2 * 2;     // [T; P T] image, bf16 hi + lo
+constexpr size_t kKqBytes = 128 * 128 * 2 * 2;    // [K; Q] image, bf16 hi + lo
+constexpr size_t kWsHeader = 4096;                // error words
+constexpr int kDVS = 64;                          // value columns per chain CTA
 
 // element offsets inside no-swizzle core-matrix tiles (bf16, 64 elements per core matrix)
 __device__ __forceinline__ int kmaj(int r, int k, int Kd) { return ((r >> 3) * (Kd >> 3) + (k >> 3)) * 64 + (r & 7) * 8 + (k & 7); }
 __device__ __forceinline__ int mnmaj(int mn, int k, int Kd) { return ((mn >> 3) * (Kd >> 3) + (k >> 3)) * 64 + (k & 7) * 8 + (mn & 7); }
 
-// split 8 fp32 values into bf16 hi and lo and store them as two 16-byte vectors
+__device__ __forceinline__ uint32_t bf2_bits(__nv_bfloat162 v) { return *reinterpret_cast<uint32_t*>(&v); }
+
+// split 8 fp32 values into bf16 hi / lo vectors (packed conversions)
+__device__ __forceinline__ void split8(const float* x, uint4& hi, uint4& lo)
+{
+    uint32_t h[4], l[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+        const __nv_bfloat162 hh = __floats2bfloat162_rn(x[2 * e], x[2 * e + 1]);
+        const float2 hf = __bfloat1622float2(hh);
+        h[e] = bf2_bits(hh);
+        l[e] = bf2_bits(__floats2bfloat162_rn(x[2 * e] - hf.x, x[2 * e + 1] - hf.y));
+    }
+    hi = make_uint4(h[0], h[1], h[2], h[3]);
+    lo = make_uint4(l[0], l[1], l[2], l[3]);
+}
+
 __device__ __forceinline__ void store_split8(uint16_t* hi, uint16_t* lo, const float* x)
 {
-    uint16_t h[8], l[8];
-#pragma unroll
-    for (int e = 0; e < 8; ++e) umma::split_bf16(x[e], h[e], l[e]);
     uint4 vh, vl;
-    vh.x = h[0] | ((uint32_t)h[1] << 16); vh.y = h[2] | ((uint32_t)h[3] << 16);
-    vh.z = h[4] | ((uint32_t)h[5] << 16); vh.w = h[6] | ((uint32_t)h[7] << 16);
-    vl.x = l[0] | ((uint32_t)l[1] << 16); vl.y = l[2] | ((uint32_t)l[3] << 16);
-    vl.z = l[4] | ((uint32_t)l[5] << 16); vl.w = l[6] | ((uint32_t)l[7] << 16);
+    split8(x, vh, vl);
     *reinterpret_cast<uint4*>(hi) = vh;
     *reinterpret_cast<uint4*>(lo) = vl;
 }
 
-template <int DVS>
-struct __align__(1024) ScanSmem {
-    uint16_t akq[2][128 * 128];  // [K; Q] (K-major, 128 rows x dk): A of KK^T/QK^T and of KS/QS; rows 0-63 are B of KK^T
-    uint16_t akt[2][128 * 64];   // Kd^T (MN-major, dk x 64 tokens): A of the state update
-    struct { float A[64 * 64]; float T[64 * 64]; } f;  // fp32 A and T while solving
-    uint16_t am[2][128 * 64];    // [I; P] (A of P T), then [T; P T] (A of U / P U); K-major
+// Three-pass split product D = A * B over `ksteps` 16-wide K steps; a_kstep /
+// b_kstep are the byte advances of one K step in each tile.  Descriptors are
+// built once per operand and advanced by adding to their start-address field.
+__device__ __forceinline__ void mma_split(uint32_t d, uint32_t a_hi, uint32_t a_lo, uint32_t a_lbo, uint32_t a_sbo,
+                                          uint32_t a_kstep, uint32_t b_hi, uint32_t b_lo, uint32_t b_sbo,
+                                          uint32_t b_kstep, int ksteps, uint32_t idesc)
+{
+    const uint64_t dah = umma::desc(a_hi, a_lbo, a_sbo), dal = umma::desc(a_lo, a_lbo, a_sbo);
+    const uint64_t dbh = umma::desc(b_hi, 128, b_sbo), dbl = umma::desc(b_lo, 128, b_sbo);
+    const uint64_t sa = a_kstep >> 4, sb = b_kstep >> 4;
+    for (int ks = 0; ks < ksteps; ++ks) umma::mma_bf16(d, dah + ks * sa, dbh + ks * sb, idesc, ks != 0);
+    for (int ks = 0; ks < ksteps; ++ks) umma::mma_bf16(d, dah + ks * sa, dbl + ks * sb, idesc, 1u);
+    for (int ks = 0; ks < ksteps; ++ks) umma::mma_bf16(d, dal + ks * sa, dbh + ks * sb, idesc, 1u);
+}
+
+// Split product in two instruction groups: D[:, 0:2N] = A_hi [B_hi | B_lo], then
+// D[:, 0:N] += A_lo B_hi, so D[:, 0:N] + D[:, N:2N] = A B to ~16 bits.  Needs B_lo
+// to follow B_hi directly along N in shared memory (b_hilo is the start of
+// both).  Two thirds of the instructions of mma_split for the same tensor work.
+__device__ __forceinline__ void mma_split2(uint32_t d, uint32_t a_hi, uint32_t a_lo, uint32_t a_lbo, uint32_t a_sbo,
+                                           uint32_t a_kstep, uint32_t b_hilo, uint32_t b_sbo, uint32_t b_kstep,
+                                           int ksteps, int N, bool a_mn, bool b_mn)
+{
+    const uint64_t dah = umma::desc(a_hi, a_lbo, a_sbo), dal = umma::desc(a_lo, a_lbo, a_sbo);
+    const uint64_t db = umma::desc(b_hilo, 128, b_sbo);
+    const uint64_t sa = a_kstep >> 4, sb = b_kstep >> 4;
+    const uint32_t wide = umma::idesc_bf16(128, 2 * N, a_mn, b_mn), narrow = umma::idesc_bf16(128, N, a_mn, b_mn);
+    for (int ks = 0; ks < ksteps; ++ks) umma::mma_bf16(d, dah + ks * sa, db + ks * sb, wide, ks != 0);
+    for (int ks = 0; ks < ksteps; ++ks) umma::mma_bf16(d, dal + ks * sa, db + ks * sb, narrow, 1u);
+}
+
+// Chunk slots: sequence s owns slots [base(s), base(s) + ceil(len_s / 64)) with
+// base(s) = floor(cu[s] / 64) + s, which never overlap and need no prefix sum;
+// floor(T / 64) + n_seq slots cover every batch.
+__device__ __forceinline__ int slot_base(const ScanParams& p, int s) { return cu_at(p.cu_seqlens, s, p.T) / kChunk + s; }
+
+__host__ __device__ inline size_t n_slots(int T, int n_seq) { return (size_t)(T / kChunk) + (size_t)n_seq; }
+
+__device__ __forceinline__ unsigned char* am_image(const ScanParams& p, size_t slot, int h)
+{
+    return static_cast<unsigned char*>(p.workspace) + kWsHeader + (slot * p.hv + h) * kAmBytes;
+}
+
+__device__ __forceinline__ unsigned char* kq_image(const ScanParams& p, size_t slot, int j)
+{
+    return static_cast<unsigned char*>(p.workspace) + kWsHeader + n_slots(p.T, p.n_seq) * p.hv * kAmBytes +
+           (slot * p.hk + j) * kKqBytes;
+}
+
+// running log-decay of one chunk from warp 0: lam[q] for tokens lane + 32 q in,
+// inclusive sums out; returns the chunk total
+__device__ __forceinline__ float warp_chunk_cumsum(float (&lam)[2], int lane)
+{
+#pragma unroll
+    for (int q = 0; q < 2; ++q)
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+            const float y = __shfl_up_sync(0xffffffffu, lam[q], off);
+            if (lane >= off) lam[q] += y;
+        }
+    lam[1] += __shfl_sync(0xffffffffu, lam[0], 31);
+    return __shfl_sync(0xffffffffu, lam[1], 31);
+}
+
+// =======================================================================================
+// prep: one CTA per (chunk slot, value head)
+// =======================================================================================
+constexpr int kPrepThreads = 128;
+
+struct __align__(1024) PrepSmem {
     union {
-        uint16_t bt[2][64 * 64];  // T (MN-major B, 64 x 64)
-        float W[3 * 256];         // off-diagonal block sums of the solve
-    } u2;
-    uint16_t bs[2][128 * DVS];   // S slice (MN-major B, dk x DVS)
-    uint16_t bx[2][64 * DVS];    // X, then U (MN-major B, 64 x DVS)
-    float v[64 * DVS];           // V tile of the slice
-    float G[64], eG[64], beta[64], kdec[64];
-    float gL;
+        uint16_t akq[2][128 * 128];                                   // split [K; Q] (K-major)
+        struct { float A[64 * 68]; float T[64 * 68]; uint16_t bt[2][64 * 64]; } s;  // solve (rows padded), T as MN-major B
+    } u;
+    uint16_t am[2][128 * 64];  // [I; P] (K-major)
+    float W[3 * 256];          // off-diagonal block sums of the solve
+    float G[64], beta[64];
     uint32_t tmem_base;
     int abort_flag;
     uint64_t mbar;
 };
 
-// Three-pass split product D = A * B over `ksteps` 16-wide K steps.
-__device__ __forceinline__ void mma_split(uint32_t d, uint32_t a_hi, uint32_t a_lo, uint32_t a_sbo, uint32_t b_hi,
-                                          uint32_t b_lo, uint32_t b_sbo, int ksteps, uint32_t idesc)
-{
-    const uint32_t as[3] = {a_hi, a_hi, a_lo};
-    const uint32_t bs[3] = {b_hi, b_lo, b_hi};
-#pragma unroll
-    for (int pass = 0; pass < 3; ++pass)
-        for (int ks = 0; ks < ksteps; ++ks) {
-            const uint64_t da = umma::desc(as[pass] + ks * 256, 128, a_sbo);
-            const uint64_t db = umma::desc(bs[pass] + ks * 256, 128, b_sbo);
-            umma::mma_bf16(d, da, db, idesc, (pass | ks) != 0);
-        }
-}
-
-template <int DVS>
-__global__ void __launch_bounds__(kThreads, 1) scan_tc_kernel(ScanParams p)
+__global__ void __launch_bounds__(kPrepThreads) scan_prep_kernel(ScanParams p)
 {
     extern __shared__ __align__(1024) unsigned char smem_raw[];
-    ScanSmem<DVS>& sm = *reinterpret_cast<ScanSmem<DVS>*>(smem_raw);
-    constexpr int SLICES = kHeadDim / DVS;
-    constexpr uint32_t kTmemCols = 256;
-    // TMEM columns: [0,64) K K^T|Q K^T, then (K S0 ; Q S0); [64,128) T|P T, then (U ; P U); [128, 128+DVS) dS
-    constexpr uint32_t cKQ = 0, cPT = 64, cD2 = 0, cD3 = 64, cD4 = 128;
-
+    PrepSmem& sm = *reinterpret_cast<PrepSmem*>(smem_raw);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int h = blockIdx.x / SLICES, slice = blockIdx.x % SLICES, s = blockIdx.y;
-    const int j = h / (p.hv / p.hk);
-    const int v0 = slice * DVS;
-    const int t0 = cu_at(p.cu_seqlens, s, p.T), t1 = max(cu_at(p.cu_seqlens, s + 1, p.T), t0);
-    const size_t sbase = ((size_t)s * p.hv + h) * kHeadDim * kHeadDim;
-    const float qscale = rsqrtf((float)kHeadDim);
+    const int slot = blockIdx.x, h = blockIdx.y;
+    const int group = p.hv / p.hk, j = h / group;
     uint32_t* err = reinterpret_cast<uint32_t*>(p.workspace);
 
-    if (warp == 0) umma::tmem_alloc(&sm.tmem_base, kTmemCols);
+    // slot -> (sequence, chunk); last s with base(s) <= slot
+    int lo = 0, hi = p.n_seq - 1;
+    while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (slot_base(p, mid) <= slot) lo = mid; else hi = mid - 1;
+    }
+    const int s = lo;
+    const int start = cu_at(p.cu_seqlens, s, p.T), end = max(cu_at(p.cu_seqlens, s + 1, p.T), start);
+    const int c0 = start + (slot - slot_base(p, s)) * kChunk;
+    if (slot < slot_base(p, s) || c0 >= end) return;  // unused slot (whole CTA)
+    const int n = min(kChunk, end - c0);
+    const bool write_kq = (h % group) == 0;
+    const float qscale = rsqrtf((float)kHeadDim);
+
+    if (warp == 0) umma::tmem_alloc(&sm.tmem_base, 128);
     if (tid == 0) {
         umma::mbar_init(&sm.mbar, 1);
         sm.abort_flag = 0;
     }
-
-    // state slice: thread i holds row i (key index) of S[:, v0:v0+DVS]
-    float S[DVS];
+    // [K; Q] -> split tile (and the image for the chain when this CTA owns it).
+    // Unit u = (matrix, token group, column group, row in group), row fastest so
+    // that 8 consecutive lanes fill one 128-byte core matrix.  All 16 units'
+    // loads (and the gates') are in flight together.
+    {
+        float raw_lam[2] = {0.f, 0.f}, raw_beta[2] = {0.f, 0.f};
+        if (warp == 0) {
 #pragma unroll
-    for (int c = 0; c < DVS; c += 4) {
-        const float4 x = *reinterpret_cast<const float4*>(p.S_in + sbase + (size_t)tid * kHeadDim + v0 + c);
-        S[c] = x.x; S[c + 1] = x.y; S[c + 2] = x.z; S[c + 3] = x.w;
+            for (int q = 0; q < 2; ++q) {
+                const int t = lane + 32 * q;
+                if (t < n) {
+                    raw_lam[q] = __ldg(p.glog + (size_t)(c0 + t) * p.hv + h);
+                    raw_beta[q] = __ldg(p.beta + (size_t)(c0 + t) * p.hv + h);
+                }
+            }
+        }
+        float4 ld[32];
+#pragma unroll
+        for (int q = 0; q < 16; ++q) {
+            const int u = tid + kPrepThreads * q;
+            const int mat = u >> 10, tg = (u >> 7) & 7, g = (u >> 3) & 15, t = tg * 8 + (u & 7);
+            if (t < n) {
+                const float4* src = reinterpret_cast<const float4*>(
+                    (mat ? p.qn : p.kn) + ((size_t)(c0 + t) * p.hk + j) * kHeadDim + g * 8);
+                ld[2 * q] = __ldg(src);
+                ld[2 * q + 1] = __ldg(src + 1);
+            } else {
+                ld[2 * q] = ld[2 * q + 1] = make_float4(0.f, 0.f, 0.f, 0.f);
+            }
+        }
+        if (warp == 0) {  // gates of the chunk
+            float lam[2];
+#pragma unroll
+            for (int q = 0; q < 2; ++q) {
+                const int t = lane + 32 * q;
+                lam[q] = t < n ? fmaxf(raw_lam[q], kLamFloor) : 0.0f;
+                sm.beta[t] = raw_beta[q];
+            }
+            warp_chunk_cumsum(lam, lane);
+            sm.G[lane] = lam[0];
+            sm.G[lane + 32] = lam[1];
+        }
+        unsigned char* img = kq_image(p, slot, j);
+#pragma unroll
+        for (int q = 0; q < 16; ++q) {
+            const int u = tid + kPrepThreads * q;
+            const int mat = u >> 10, tg = (u >> 7) & 7, g = (u >> 3) & 15, t = tg * 8 + (u & 7);
+            const float x[8] = {ld[2 * q].x, ld[2 * q].y, ld[2 * q].z, ld[2 * q].w,
+                                ld[2 * q + 1].x, ld[2 * q + 1].y, ld[2 * q + 1].z, ld[2 * q + 1].w};
+            uint4 vh, vl;
+            split8(x, vh, vl);
+            const int off = kmaj(mat * 64 + t, g * 8, 128);
+            *reinterpret_cast<uint4*>(&sm.u.akq[0][off]) = vh;
+            *reinterpret_cast<uint4*>(&sm.u.akq[1][off]) = vl;
+            if (write_kq) {
+                *reinterpret_cast<uint4*>(img + off * 2) = vh;
+                *reinterpret_cast<uint4*>(img + kKqBytes / 2 + off * 2) = vl;
+            }
+        }
     }
-#pragma unroll
-    for (int c = 0; c < DVS; c += 8) store_split8(&sm.bs[0][mnmaj(c, tid, 128)], &sm.bs[1][mnmaj(c, tid, 128)], S + c);
-
     umma::fence_proxy_async();
     umma::fence_before_sync();
     __syncthreads();
     umma::fence_after_sync();
     const uint32_t tmem = sm.tmem_base;
     const uint32_t lane_off = (uint32_t)(warp * 32) << 16;
+    const uint32_t a_kq[2] = {umma::smem_u32(sm.u.akq[0]), umma::smem_u32(sm.u.akq[1])};
+    const uint32_t a_m[2] = {umma::smem_u32(sm.am[0]), umma::smem_u32(sm.am[1])};
+    const uint32_t b_t[2] = {umma::smem_u32(sm.u.s.bt[0]), umma::smem_u32(sm.u.s.bt[1])};
     uint32_t phase = 0;
 
-    const uint32_t a_kq[2] = {umma::smem_u32(sm.akq[0]), umma::smem_u32(sm.akq[1])};
-    const uint32_t a_kt[2] = {umma::smem_u32(sm.akt[0]), umma::smem_u32(sm.akt[1])};
-    const uint32_t a_m[2] = {umma::smem_u32(sm.am[0]), umma::smem_u32(sm.am[1])};
-    const uint32_t b_t[2] = {umma::smem_u32(sm.u2.bt[0]), umma::smem_u32(sm.u2.bt[1])};
+    // (K K^T ; Q K^T) = [K; Q] K^T  (B = the K rows of the same tile)
+    if (tid == 0) {
+        mma_split(tmem, a_kq[0], a_kq[1], 128, 2048, 256, a_kq[0], a_kq[1], 2048, 256, 8,
+                  umma::idesc_bf16(128, 64, false, false));
+        umma::commit(&sm.mbar);
+    }
+    if (!umma::mbar_wait(&sm.mbar, phase)) { sm.abort_flag = 1; atomicOr(err, kErrTimeout); }
+    phase ^= 1u;
+    __syncthreads();
+    if (sm.abort_flag) goto done;
+    umma::fence_after_sync();
+
+    // A (fp32, from K K^T rows) and [I; P] (split; P from Q K^T rows)
+    {
+        const int i = tid & 63;
+        const float Gi = sm.G[i];
+        float d[64];
+        {
+            float d0[32], d1[32];
+            umma::tmem_ld32(tmem + lane_off, d0);
+            umma::tmem_ld32(tmem + lane_off + 32, d1);
+            umma::tmem_wait_ld();
+#pragma unroll
+            for (int e = 0; e < 32; ++e) { d[e] = d0[e]; d[32 + e] = d1[e]; }
+        }
+        const float4* G4 = reinterpret_cast<const float4*>(sm.G);
+        if (tid < 64) {
+            const float bi = sm.beta[i];
+#pragma unroll
+            for (int q = 0; q < 16; ++q) {
+                const float4 g = G4[q];
+                const float gg[4] = {g.x, g.y, g.z, g.w};
+                float a[4];
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const int jj = 4 * q + e;
+                    a[e] = jj < i ? bi * __expf(Gi - gg[e]) * d[jj] : 0.0f;
+                }
+                *reinterpret_cast<float4*>(&sm.u.s.A[i * 68 + 4 * q]) = make_float4(a[0], a[1], a[2], a[3]);
+            }
+#pragma unroll
+            for (int c = 0; c < 64; c += 8) {
+                float idr[8];
+#pragma unroll
+                for (int e = 0; e < 8; ++e) idr[e] = (c + e == i) ? 1.0f : 0.0f;
+                store_split8(&sm.am[0][kmaj(i, c, 64)], &sm.am[1][kmaj(i, c, 64)], idr);
+            }
+        } else {
+#pragma unroll
+            for (int q = 0; q < 8; ++q) {
+                const float4 ga = G4[2 * q], gb = G4[2 * q + 1];
+                const float gg[8] = {ga.x, ga.y, ga.z, ga.w, gb.x, gb.y, gb.z, gb.w};
+                float pr[8];
+#pragma unroll
+                for (int e = 0; e < 8; ++e) {
+                    const int jj = 8 * q + e;
+                    pr[e] = jj <= i ? __expf(Gi - gg[e]) * d[jj] * qscale : 0.0f;
+                }
+                store_split8(&sm.am[0][kmaj(64 + i, 8 * q, 64)], &sm.am[1][kmaj(64 + i, 8 * q, 64)], pr);
+            }
+        }
+    }
+    __syncthreads();
+
+    // T = (I + A)^-1 (A strictly lower, fp32, row stride 68).
+    // (1) 16x16 diagonal blocks: thread (b, c) forms column c of inv(I + A_bb) by
+    //     forward substitution, col[r] = [r == c] - sum_{m<r} A[r][m] col[m]; the
+    //     entries above c come out zero by themselves, so the loop has no
+    //     data-dependent branch and reads each A row as broadcast float4s.
+    // (2) off-diagonal blocks by distance: W = sum_m A_(bi,m) T_(m,bj), then
+    //     T_(bi,bj) = -T_(bi,bi) W, each thread a 2 x 4 register tile.
+    {
+        float* A = sm.u.s.A;
+        float* Tm = sm.u.s.T;
+        constexpr int ST = 68;
+        for (int e = tid; e < 64 * ST; e += kPrepThreads) Tm[e] = 0.0f;
+        __syncthreads();
+        if (tid < 64) {
+            const int b = tid >> 4, c = tid & 15, o = 16 * b;
+            float col[16];
+#pragma unroll
+            for (int r = 0; r < 16; ++r) {
+                float acc = (r == c) ? 1.0f : 0.0f;
+#pragma unroll
+                for (int m4 = 0; m4 < r; m4 += 4) {
+                    const float4 a4 = *reinterpret_cast<const float4*>(&A[(o + r) * ST + o + m4]);
+                    if (m4 + 0 < r) acc = fmaf(-a4.x, col[m4 + 0], acc);
+                    if (m4 + 1 < r) acc = fmaf(-a4.y, col[m4 + 1], acc);
+                    if (m4 + 2 < r) acc = fmaf(-a4.z, col[m4 + 2], acc);
+                    if (m4 + 3 < r) acc = fmaf(-a4.w, col[m4 + 3], acc);
+                }
+                col[r] = acc;
+            }
+#pragma unroll
+            for (int r = 0; r < 16; ++r) Tm[(o + r) * ST + o + c] = col[r];
+        }
+        __syncthreads();
+        float* W = sm.W;  // [pair][16][16]
+        const int pr = tid >> 5, q = tid & 31, r0 = 2 * (q >> 2), c0 = 4 * (q & 3);
+        for (int dist = 1; dist < 4; ++dist) {
+            const int bj = pr, bi = pr + dist;
+            const bool active = pr < 4 - dist;
+            if (active) {
+                float acc[2][4] = {};
+                for (int m4 = 16 * bj; m4 < 16 * bi; m4 += 4) {
+                    const float4 a0 = *reinterpret_cast<const float4*>(&A[(16 * bi + r0) * ST + m4]);
+                    const float4 a1 = *reinterpret_cast<const float4*>(&A[(16 * bi + r0 + 1) * ST + m4]);
+                    const float av0[4] = {a0.x, a0.y, a0.z, a0.w}, av1[4] = {a1.x, a1.y, a1.z, a1.w};
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const float4 t4 = *reinterpret_cast<const float4*>(&Tm[(m4 + e) * ST + 16 * bj + c0]);
+                        acc[0][0] = fmaf(av0[e], t4.x, acc[0][0]); acc[0][1] = fmaf(av0[e], t4.y, acc[0][1]);
+                        acc[0][2] = fmaf(av0[e], t4.z, acc[0][2]); acc[0][3] = fmaf(av0[e], t4.w, acc[0][3]);
+                        acc[1][0] = fmaf(av1[e], t4.x, acc[1][0]); acc[1][1] = fmaf(av1[e], t4.y, acc[1][1]);
+                        acc[1][2] = fmaf(av1[e], t4.z, acc[1][2]); acc[1][3] = fmaf(av1[e], t4.w, acc[1][3]);
+                    }
+                }
+                *reinterpret_cast<float4*>(&W[pr * 256 + r0 * 16 + c0]) = make_float4(acc[0][0], acc[0][1], acc[0][2], acc[0][3]);
+                *reinterpret_cast<float4*>(&W[pr * 256 + (r0 + 1) * 16 + c0]) = make_float4(acc[1][0], acc[1][1], acc[1][2], acc[1][3]);
+            }
+            __syncthreads();
+            if (active) {
+                float acc[2][4] = {};
+#pragma unroll
+                for (int m4 = 0; m4 < 16; m4 += 4) {
+                    const float4 a0 = *reinterpret_cast<const float4*>(&Tm[(16 * bi + r0) * ST + 16 * bi + m4]);
+                    const float4 a1 = *reinterpret_cast<const float4*>(&Tm[(16 * bi + r0 + 1) * ST + 16 * bi + m4]);
+                    const float av0[4] = {a0.x, a0.y, a0.z, a0.w}, av1[4] = {a1.x, a1.y, a1.z, a1.w};
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const float4 w4 = *reinterpret_cast<const float4*>(&W[pr * 256 + (m4 + e) * 16 + c0]);
+                        acc[0][0] = fmaf(av0[e], w4.x, acc[0][0]); acc[0][1] = fmaf(av0[e], w4.y, acc[0][1]);
+                        acc[0][2] = fmaf(av0[e], w4.z, acc[0][2]); acc[0][3] = fmaf(av0[e], w4.w, acc[0][3]);
+                        acc[1][0] = fmaf(av1[e], w4.x, acc[1][0]); acc[1][1] = fmaf(av1[e], w4.y, acc[1][1]);
+                        acc[1][2] = fmaf(av1[e], w4.z, acc[1][2]); acc[1][3] = fmaf(av1[e], w4.w, acc[1][3]);
+                    }
+                }
+                *reinterpret_cast<float4*>(&Tm[(16 * bi + r0) * ST + 16 * bj + c0]) =
+                    make_float4(-acc[0][0], -acc[0][1], -acc[0][2], -acc[0][3]);
+                *reinterpret_cast<float4*>(&Tm[(16 * bi + r0 + 1) * ST + 16 * bj + c0]) =
+                    make_float4(-acc[1][0], -acc[1][1], -acc[1][2], -acc[1][3]);
+            }
+            __syncthreads();
+        }
+        // T -> MN-major B tile (element (n = column, k = row)); row fastest across lanes
+        for (int u = tid; u < 64 * 8; u += kPrepThreads) {
+            const int m = u & 63, g = u >> 6;
+            const float4 x0 = *reinterpret_cast<const float4*>(&Tm[m * ST + g * 8]);
+            const float4 x1 = *reinterpret_cast<const float4*>(&Tm[m * ST + g * 8 + 4]);
+            const float tr[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
+            store_split8(&sm.u.s.bt[0][mnmaj(g * 8, m, 64)], &sm.u.s.bt[1][mnmaj(g * 8, m, 64)], tr);
+        }
+    }
+    umma::fence_proxy_async();
+    umma::fence_before_sync();
+    __syncthreads();
+    umma::fence_after_sync();
+
+    // (T ; P T) = [I; P] T
+    if (tid == 0) {
+        mma_split(tmem + 64, a_m[0], a_m[1], 128, 1024, 256, b_t[0], b_t[1], 1024, 256, 4,
+                  umma::idesc_bf16(128, 64, false, true));
+        umma::commit(&sm.mbar);
+    }
+    if (!umma::mbar_wait(&sm.mbar, phase)) { sm.abort_flag = 1; atomicOr(err, kErrTimeout); }
+    phase ^= 1u;
+    __syncthreads();
+    if (sm.abort_flag) goto done;
+    umma::fence_after_sync();
+
+    // [T; P T] -> image (K-major, split), row `tid` per thread
+    {
+        unsigned char* img = am_image(p, slot, h);
+#pragma unroll 1
+        for (int c = 0; c < 64; c += 16) {
+            float d[16];
+            umma::tmem_ld16(tmem + lane_off + 64 + c, d);
+            umma::tmem_wait_ld();
+#pragma unroll
+            for (int q = 0; q < 2; ++q) {
+                uint4 vh, vl;
+                split8(d + 8 * q, vh, vl);
+                const int off = kmaj(tid, c + 8 * q, 64);
+                *reinterpret_cast<uint4*>(img + off * 2) = vh;
+                *reinterpret_cast<uint4*>(img + kAmBytes / 2 + off * 2) = vl;
+            }
+        }
+    }
+
+done:
+    umma::fence_before_sync();
+    __syncthreads();
+    if (warp == 0) umma::tmem_dealloc(sm.tmem_base, 128);
+}
+
+// =======================================================================================
+// chain: one CTA per (sequence, value head, kDVS-column slice)
+// =======================================================================================
+constexpr int kChainThreads = 256;  // two warpgroups: each covers all 128 TMEM lanes, half the columns
+
+template <int DVS>
+struct __align__(1024) ChainSmem {
+    uint16_t akq[2][2][128 * 128];  // [K; Q] image, double-buffered: [buffer][hi/lo]
+    uint16_t am[2][128 * 64];       // [T; P T] image
+    uint16_t bs[2][128 * DVS];      // S slice (MN-major B, dk x DVS)
+    uint16_t bx[2][64 * DVS];       // X, then e^{G_L-G} U (MN-major B, 64 x DVS)
+    float v[64 * (DVS + 4)];        // V tile of the slice, rows padded by 16 bytes (bank spread)
+    float eG[64], beta[64], kdec[64];
+    float gL;
+    uint32_t tmem_base;
+    int abort_flag;
+    uint64_t mbar_mma, mbar_kq[2], mbar_am;
+};
+
+template <int DVS>
+__global__ void __launch_bounds__(kChainThreads, 1) scan_chain_kernel(ScanParams p)
+{
+    extern __shared__ __align__(1024) unsigned char smem_raw[];
+    ChainSmem<DVS>& sm = *reinterpret_cast<ChainSmem<DVS>*>(smem_raw);
+    constexpr int SLICES = kHeadDim / DVS;
+    constexpr int HALF = DVS / 2;  // columns per warpgroup
+    constexpr uint32_t kTmemCols = 512;
+    // each product takes 2*DVS columns: [hi*hi + lo*hi | hi*lo]
+    constexpr uint32_t cD2 = 0, cD3 = 2 * DVS, cD4 = 4 * DVS;
+    static_assert(6 * DVS <= (int)kTmemCols, "TMEM columns");
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int L = tid & 127;            // TMEM lane of this thread
+    const int wg = tid >> 7;            // column half
+    const int h = blockIdx.x / SLICES, slice = blockIdx.x % SLICES, s = blockIdx.y;
+    const int j = h / (p.hv / p.hk);
+    const int v0 = slice * DVS;
+    const int t0 = cu_at(p.cu_seqlens, s, p.T), t1 = max(cu_at(p.cu_seqlens, s + 1, p.T), t0);
+    const int n_chunks = (t1 - t0 + kChunk - 1) / kChunk;
+    const size_t base = (size_t)slot_base(p, s);
+    const size_t sbase = ((size_t)s * p.hv + h) * kHeadDim * kHeadDim;
+    const float qscale = rsqrtf((float)kHeadDim);
+    uint32_t* err = reinterpret_cast<uint32_t*>(p.workspace);
+
+    if (warp == 0) umma::tmem_alloc(&sm.tmem_base, kTmemCols);
+    if (tid == 0) {
+        umma::mbar_init(&sm.mbar_mma, 1);
+        umma::mbar_init(&sm.mbar_kq[0], 1);
+        umma::mbar_init(&sm.mbar_kq[1], 1);
+        umma::mbar_init(&sm.mbar_am, 1);
+        sm.abort_flag = 0;
+    }
+
+    // state slice: thread (L, wg) holds row L (key index), columns v0 + wg*HALF + [0, HALF)
+    float S[HALF];
+    {
+        const float* src = p.S_in + sbase + (size_t)L * kHeadDim + v0 + wg * HALF;
+#pragma unroll
+        for (int c = 0; c < HALF; c += 4) {
+            const float4 x = *reinterpret_cast<const float4*>(src + c);
+            S[c] = x.x; S[c + 1] = x.y; S[c + 2] = x.z; S[c + 3] = x.w;
+        }
+#pragma unroll
+        for (int c = 0; c < HALF; c += 8)
+            store_split8(&sm.bs[0][mnmaj(wg * HALF + c, L, 128)], &sm.bs[1][mnmaj(wg * HALF + c, L, 128)], S + c);
+    }
+    umma::fence_proxy_async();
+    umma::fence_before_sync();
+    __syncthreads();
+    umma::fence_after_sync();
+
+    const uint32_t tmem = sm.tmem_base;
+    const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
     const uint32_t b_s[2] = {umma::smem_u32(sm.bs[0]), umma::smem_u32(sm.bs[1])};
     const uint32_t b_x[2] = {umma::smem_u32(sm.bx[0]), umma::smem_u32(sm.bx[1])};
+    const uint32_t a_m[2] = {umma::smem_u32(sm.am[0]), umma::smem_u32(sm.am[1])};
+    uint32_t ph_mma = 0;
+    // outstanding bulk copies (uniform across threads): issued but not yet waited
+    bool pend_kq[2] = {false, false}, pend_am = false;
 
-#define GDN_MMA_WAIT()                                                         \
+    // ---- bulk-copy issue helpers (thread 0) -----------------------------------------------
+    auto issue_kq = [&](int c) {  // [K; Q] image of chunk c into buffer c & 1
+        if (tid == 0) {
+            uint64_t* mb = &sm.mbar_kq[c & 1];
+            umma::mbar_arrive_expect_tx(mb, (uint32_t)kKqBytes);
+            const unsigned char* src = kq_image(p, base + c, j);
+            unsigned char* dst = reinterpret_cast<unsigned char*>(sm.akq[c & 1]);
+            umma::bulk_g2s(dst, src, (uint32_t)kKqBytes, mb);
+        }
+        pend_kq[c & 1] = true;
+    };
+    auto issue_am = [&](int c) {
+        if (tid == 0) {
+            umma::mbar_arrive_expect_tx(&sm.mbar_am, (uint32_t)kAmBytes);
+            const unsigned char* src = am_image(p, base + c, h);
+            unsigned char* dst = reinterpret_cast<unsigned char*>(sm.am);
+            umma::bulk_g2s(dst, src, (uint32_t)kAmBytes, &sm.mbar_am);
+        }
+        pend_am = true;
+    };
+    // V tile of a chunk: every thread loads 4 float4 into registers one chunk ahead
+    constexpr int kVq = 64 * DVS / 4 / kChainThreads;
+    float4 vpre[kVq];
+    auto load_v = [&](int c) {
+        const int cc0 = t0 + c * kChunk, nn = min(kChunk, t1 - cc0);
+#pragma unroll
+        for (int q = 0; q < kVq; ++q) {
+            const int u = tid + kChainThreads * q, t = u / (DVS / 4), c4 = (u % (DVS / 4)) * 4;
+            vpre[q] = t < nn ? __ldg(reinterpret_cast<const float4*>(p.vc + ((size_t)(cc0 + t) * p.hv + h) * kHeadDim + v0 + c4))
+                             : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+    };
+    auto store_v = [&]() {
+#pragma unroll
+        for (int q = 0; q < kVq; ++q) {
+            const int u = tid + kChainThreads * q, t = u / (DVS / 4), c4 = (u % (DVS / 4)) * 4;
+            *reinterpret_cast<float4*>(&sm.v[t * (DVS + 4) + c4]) = vpre[q];
+        }
+    };
+    // gates of one chunk, raw values prefetched into warp-0 registers one chunk ahead
+    float lam_nx[2] = {0.f, 0.f}, bet_nx[2] = {0.f, 0.f};
+    int n_nx = 0;
+    auto load_gates = [&](int c) {
+        const int cc0 = t0 + c * kChunk, nn = min(kChunk, t1 - cc0);
+        n_nx = nn;
+        if (warp == 0) {
+#pragma unroll
+            for (int q = 0; q < 2; ++q) {
+                const int t = lane + 32 * q;
+                lam_nx[q] = t < nn ? __ldg(p.glog + (size_t)(cc0 + t) * p.hv + h) : 0.0f;
+                bet_nx[q] = t < nn ? __ldg(p.beta + (size_t)(cc0 + t) * p.hv + h) : 0.0f;
+            }
+        }
+    };
+
+#define GDN_WAIT(mbar, parity)                                                 \
     do {                                                                       \
-        if (!umma::mbar_wait(&sm.mbar, phase)) {                               \
+        if (!umma::mbar_wait((mbar), (parity))) {                              \
             sm.abort_flag = 1;                                                 \
             atomicOr(err, kErrTimeout);                                        \
         }                                                                      \
-        phase ^= 1u;                                                           \
+    } while (0)
+#define GDN_SYNC_OR_ABORT()                                                    \
+    do {                                                                       \
         __syncthreads();                                                       \
         if (sm.abort_flag) goto done;                                          \
         umma::fence_after_sync();                                              \
     } while (0)
-
 #define GDN_PUBLISH()                                                          \
     do {                                                                       \
         umma::fence_proxy_async();                                             \
@@ -164,336 +614,201 @@ __global__ void __launch_bounds__(kThreads, 1) scan_tc_kernel(ScanParams p)
         umma::fence_after_sync();                                              \
     } while (0)
 
-    for (int c0 = t0; c0 < t1; c0 += kChunk) {
-        const int n = min(kChunk, t1 - c0);
+    if (n_chunks > 0) {
+        issue_kq(0);
+        issue_am(0);
+        load_gates(0);
+        load_v(0);
+        store_v();
+    }
 
-        // ---- 1-2. gates (warp 0), [K; Q] -> akq, Kd^T -> akt, V tile --------------------------
-        // Each thread owns 16 (matrix, token, 8-column group) units; their global loads are
-        // issued in two batches of 8 so that only two load latencies sit on this path.
-        {
-            float4 ld[16];
-            float4 vv[DVS / 8];
-            auto unit_src = [&](int u) -> const float* {
-                const int mat = u >> 10, t = (u >> 4) & 63, g = u & 15;
-                return (mat ? p.qn : p.kn) + ((size_t)(c0 + t) * p.hk + j) * kHeadDim + g * 8;
-            };
-            auto issue = [&](int batch) {
-#pragma unroll
-                for (int q = 0; q < 8; ++q) {
-                    const int u = tid + kThreads * (8 * batch + q);
-                    const int t = (u >> 4) & 63;
-                    if (t < n) {
-                        ld[2 * q] = __ldg(reinterpret_cast<const float4*>(unit_src(u)));
-                        ld[2 * q + 1] = __ldg(reinterpret_cast<const float4*>(unit_src(u)) + 1);
-                    } else {
-                        ld[2 * q] = ld[2 * q + 1] = make_float4(0.f, 0.f, 0.f, 0.f);
-                    }
-                }
-            };
-            issue(0);
-#pragma unroll
-            for (int q = 0; q < DVS / 8; ++q) {
-                const int u = tid + kThreads * q;
-                const int t = u / (DVS / 4), c = (u % (DVS / 4)) * 4;
-                vv[q] = t < n ? __ldg(reinterpret_cast<const float4*>(p.vc + ((size_t)(c0 + t) * p.hv + h) * kHeadDim + v0 + c))
-                              : make_float4(0.f, 0.f, 0.f, 0.f);
-            }
-            if (warp == 0) {
-                float lam[2], bb[2];
-#pragma unroll
-                for (int q = 0; q < 2; ++q) {
-                    const int t = lane + 32 * q;
-                    lam[q] = t < n ? fmaxf(__ldg(p.glog + (size_t)(c0 + t) * p.hv + h), kLamFloor) : 0.0f;
-                    bb[q] = t < n ? __ldg(p.beta + (size_t)(c0 + t) * p.hv + h) : 0.0f;
-                }
-#pragma unroll
-                for (int q = 0; q < 2; ++q)
-#pragma unroll
-                    for (int off = 1; off < 32; off <<= 1) {
-                        const float y = __shfl_up_sync(0xffffffffu, lam[q], off);
-                        if (lane >= off) lam[q] += y;
-                    }
-                lam[1] += __shfl_sync(0xffffffffu, lam[0], 31);
-                const float GL = __shfl_sync(0xffffffffu, lam[1], 31);
-#pragma unroll
-                for (int q = 0; q < 2; ++q) {
-                    const int t = lane + 32 * q;
-                    sm.G[t] = lam[q];
-                    sm.eG[t] = expf(lam[q]);
-                    sm.beta[t] = bb[q];
-                    sm.kdec[t] = expf(GL - lam[q]);
-                }
-                if (lane == 0) sm.gL = expf(GL);
-            }
-#pragma unroll
-            for (int q = 0; q < DVS / 8; ++q) {
-                const int u = tid + kThreads * q;
-                const int t = u / (DVS / 4), c = (u % (DVS / 4)) * 4;
-                *reinterpret_cast<float4*>(&sm.v[t * DVS + c]) = vv[q];
-            }
-            __syncthreads();  // G, kdec visible
-#pragma unroll
-            for (int batch = 0; batch < 2; ++batch) {
-                if (batch == 1) issue(1);
-#pragma unroll
-                for (int q = 0; q < 8; ++q) {
-                    const int u = tid + kThreads * (8 * batch + q);
-                    const int mat = u >> 10, t = (u >> 4) & 63, g = u & 15;
-                    float x[8] = {ld[2 * q].x, ld[2 * q].y, ld[2 * q].z, ld[2 * q].w,
-                                  ld[2 * q + 1].x, ld[2 * q + 1].y, ld[2 * q + 1].z, ld[2 * q + 1].w};
-                    const int r = mat * 64 + t;
-                    store_split8(&sm.akq[0][kmaj(r, g * 8, 128)], &sm.akq[1][kmaj(r, g * 8, 128)], x);
-                    if (mat == 0) {
-                        const float kd = sm.kdec[t];
-#pragma unroll
-                        for (int e = 0; e < 8; ++e) x[e] *= kd;
-                        // element (m = key index, k = token) of the MN-major A tile
-                        store_split8(&sm.akt[0][mnmaj(g * 8, t, 64)], &sm.akt[1][mnmaj(g * 8, t, 64)], x);
-                    }
-                }
-            }
-        }
-        GDN_PUBLISH();
+    for (int c = 0; c < n_chunks; ++c) {
+        const int c0 = t0 + c * kChunk, n = min(kChunk, t1 - c0);
+        const bool more = c + 1 < n_chunks;
+        if (more) issue_kq(c + 1);  // its buffer was last read by chunk c-1's state update
 
-        // ---- 3. (K K^T ; Q K^T) = [K; Q] K^T ------------------------------------------------
+        // ---- (K S0 ; Q S0) = [K; Q] S0 ------------------------------------------------------------
+        GDN_WAIT(&sm.mbar_kq[c & 1], (c >> 1) & 1);
+        pend_kq[c & 1] = false;
+        GDN_SYNC_OR_ABORT();
+        const uint32_t a_kq_hi = umma::smem_u32(sm.akq[c & 1][0]), a_kq_lo = umma::smem_u32(sm.akq[c & 1][1]);
         if (tid == 0) {
-            mma_split(tmem + cKQ, a_kq[0], a_kq[1], 2048, a_kq[0], a_kq[1], 2048, 8,
-                      umma::idesc_bf16(128, 64, false, false));
-            umma::commit(&sm.mbar);
+            mma_split2(tmem + cD2, a_kq_hi, a_kq_lo, 128, 2048, 256, b_s[0], 2048, 256, 8, DVS, false, true);
+            umma::commit(&sm.mbar_mma);
         }
-        GDN_MMA_WAIT();
+        // ---- meanwhile: gates e^G, beta, e^{G_L - G}, e^{G_L}; next chunk's gates and V ---------
+        if (warp == 0) {
+            float lam[2];
+#pragma unroll
+            for (int q = 0; q < 2; ++q) lam[q] = (lane + 32 * q) < n_nx ? fmaxf(lam_nx[q], kLamFloor) : 0.0f;
+            const float b0 = bet_nx[0], b1 = bet_nx[1];
+            if (more) load_gates(c + 1);
+            const float GL = warp_chunk_cumsum(lam, lane);
+            sm.eG[lane] = __expf(lam[0]);
+            sm.eG[lane + 32] = __expf(lam[1]);
+            sm.kdec[lane] = __expf(GL - lam[0]);
+            sm.kdec[lane + 32] = __expf(GL - lam[1]);
+            sm.beta[lane] = b0;
+            sm.beta[lane + 32] = b1;
+            if (lane == 0) sm.gL = __expf(GL);
+        }
+        if (more) load_v(c + 1);
+        GDN_WAIT(&sm.mbar_mma, ph_mma);
+        ph_mma ^= 1u;
+        GDN_SYNC_OR_ABORT();
 
-        // ---- 4. A (fp32, rows 0-63) and [I; P] (split, rows 64-127 P, rows 0-63 I) ----------
+        // ---- X = beta (V - e^G K S0) -> bx;  keep e^G Q S0 / sqrt(dk) --------------------------------
+        float qs[HALF];
         {
-            const int i = tid & 63;
-            const float Gi = sm.G[i];
-#pragma unroll 1
-            for (int c = 0; c < 64; c += 16) {
-                float d[16];
-                umma::tmem_ld16(tmem + lane_off + cKQ + c, d);
-                umma::tmem_wait_ld();
-                if (tid < 64) {
-                    const float bi = sm.beta[i];
-#pragma unroll
-                    for (int e = 0; e < 16; ++e) {
-                        const int jj = c + e;
-                        sm.f.A[i * 64 + jj] = jj < i ? bi * expf(Gi - sm.G[jj]) * d[e] : 0.0f;
-                    }
-                } else {
-                    float pr[16];
-#pragma unroll
-                    for (int e = 0; e < 16; ++e) {
-                        const int jj = c + e;
-                        pr[e] = jj <= i ? expf(Gi - sm.G[jj]) * d[e] * qscale : 0.0f;
-                    }
-                    store_split8(&sm.am[0][kmaj(64 + i, c, 64)], &sm.am[1][kmaj(64 + i, c, 64)], pr);
-                    store_split8(&sm.am[0][kmaj(64 + i, c + 8, 64)], &sm.am[1][kmaj(64 + i, c + 8, 64)], pr + 8);
-                }
-            }
-            if (tid < 64) {
-#pragma unroll
-                for (int c = 0; c < 64; c += 8) {
-                    float idr[8];
-#pragma unroll
-                    for (int e = 0; e < 8; ++e) idr[e] = (c + e == i) ? 1.0f : 0.0f;
-                    store_split8(&sm.am[0][kmaj(i, c, 64)], &sm.am[1][kmaj(i, c, 64)], idr);
-                }
-            }
-        }
-        __syncthreads();
-
-        // ---- 5. T = (I + A)^-1 -----------------------------------------------------------------
-        {
-            float* A = sm.f.A;
-            float* Tm = sm.f.T;
-            for (int e = tid; e < 64 * 64; e += kThreads) Tm[e] = 0.0f;
-            __syncthreads();
-            if (tid < 64) {  // diagonal 16x16 blocks: column c of block b by forward substitution
-                const int b = tid >> 4, c = tid & 15, o = 16 * b;
-                float col[16];
-#pragma unroll
-                for (int r = 0; r < 16; ++r) {
-                    float acc = (r == c) ? 1.0f : 0.0f;
-                    if (r > c) {
-#pragma unroll
-                        for (int m = 0; m < 16; ++m)
-                            if (m >= c && m < r) acc -= A[(o + r) * 64 + o + m] * col[m];
-                    }
-                    col[r] = r >= c ? acc : 0.0f;
-                }
-#pragma unroll
-                for (int r = 0; r < 16; ++r) Tm[(o + r) * 64 + o + c] = col[r];
-            }
-            __syncthreads();
-            float* W = sm.u2.W;
-            for (int dist = 1; dist < 4; ++dist) {
-                const int pairs = 4 - dist;
-                // W_(bi,bj) = sum_{m=bj}^{bi-1} A_(bi,m) T_(m,bj)
-                for (int e = tid; e < pairs * 256; e += kThreads) {
-                    const int pr = e >> 8, r = (e >> 4) & 15, c = e & 15;
-                    const int bj = pr, bi = pr + dist;
-                    float acc = 0.0f;
-                    for (int m = 16 * bj; m < 16 * bi; ++m) acc += A[(16 * bi + r) * 64 + m] * Tm[m * 64 + 16 * bj + c];
-                    W[e] = acc;
-                }
-                __syncthreads();
-                // T_(bi,bj) = -T_(bi,bi) W
-                for (int e = tid; e < pairs * 256; e += kThreads) {
-                    const int pr = e >> 8, r = (e >> 4) & 15, c = e & 15;
-                    const int bj = pr, bi = pr + dist;
-                    float acc = 0.0f;
-#pragma unroll
-                    for (int m = 0; m < 16; ++m) acc += Tm[(16 * bi + r) * 64 + 16 * bi + m] * W[(pr << 8) + m * 16 + c];
-                    Tm[(16 * bi + r) * 64 + 16 * bj + c] = -acc;
-                }
-                __syncthreads();
-            }
-            // T -> bt (MN-major B: element (n = column, k = row))
-            for (int u = tid; u < 64 * 8; u += kThreads) {
-                const int m = u >> 3, g = u & 7;
-                store_split8(&sm.u2.bt[0][mnmaj(g * 8, m, 64)], &sm.u2.bt[1][mnmaj(g * 8, m, 64)], &Tm[m * 64 + g * 8]);
-            }
-        }
-        GDN_PUBLISH();
-
-        // ---- 6. (T ; P T) = [I; P] T ---------------------------------------------------------
-        if (tid == 0) {
-            mma_split(tmem + cPT, a_m[0], a_m[1], 1024, b_t[0], b_t[1], 1024, 4,
-                      umma::idesc_bf16(128, 64, false, true));
-            umma::commit(&sm.mbar);
-        }
-        GDN_MMA_WAIT();
-
-        // ---- 7. [T; P T] -> am (split) -----------------------------------------------------------
-#pragma unroll 1
-        for (int c = 0; c < 64; c += 16) {
-            float d[16];
-            umma::tmem_ld16(tmem + lane_off + cPT + c, d);
+            const int t = L & 63;
+            float d[HALF], d2[HALF];
+            umma::tmem_ld32(tmem + lane_off + cD2 + wg * HALF, d);
+            umma::tmem_ld32(tmem + lane_off + cD2 + DVS + wg * HALF, d2);
             umma::tmem_wait_ld();
-            store_split8(&sm.am[0][kmaj(tid, c, 64)], &sm.am[1][kmaj(tid, c, 64)], d);
-            store_split8(&sm.am[0][kmaj(tid, c + 8, 64)], &sm.am[1][kmaj(tid, c + 8, 64)], d + 8);
-        }
-        GDN_PUBLISH();
-
-        // ---- 8. (K S0 ; Q S0) = [K; Q] S0 ------------------------------------------------------
-        if (tid == 0) {
-            mma_split(tmem + cD2, a_kq[0], a_kq[1], 2048, b_s[0], b_s[1], 2048, 8,
-                      umma::idesc_bf16(128, DVS, false, true));
-            umma::commit(&sm.mbar);
-        }
-        GDN_MMA_WAIT();
-
-        // ---- 9. X = beta (V - e^G K S0) -> bx;  keep e^G Q S0 / sqrt(dk) ----------------------
-        float qs[DVS];
-        {
-            const int t = tid & 63;
 #pragma unroll
-            for (int c = 0; c < DVS; c += 16) {
-                float d[16];
-                umma::tmem_ld16(tmem + lane_off + cD2 + c, d);
-                umma::tmem_wait_ld();
-                if (tid < 64) {
-                    const float bt = sm.beta[t], eg = sm.eG[t];
-                    float x[16];
+            for (int e = 0; e < HALF; ++e) d[e] += d2[e];
+            if (L < 64) {
+                const float bt = sm.beta[t], eg = sm.eG[t];
+                const float4* vr = reinterpret_cast<const float4*>(&sm.v[t * (DVS + 4) + wg * HALF]);
 #pragma unroll
-                    for (int e = 0; e < 16; ++e) x[e] = bt * (sm.v[t * DVS + c + e] - eg * d[e]);
-                    store_split8(&sm.bx[0][mnmaj(c, t, 64)], &sm.bx[1][mnmaj(c, t, 64)], x);
-                    store_split8(&sm.bx[0][mnmaj(c + 8, t, 64)], &sm.bx[1][mnmaj(c + 8, t, 64)], x + 8);
-                } else {
-                    const float f = sm.eG[t] * qscale;
+                for (int cc = 0; cc < HALF; cc += 8) {
+                    const float4 va = vr[cc / 4], vb = vr[cc / 4 + 1];
+                    const float vv[8] = {va.x, va.y, va.z, va.w, vb.x, vb.y, vb.z, vb.w};
+                    float x[8];
 #pragma unroll
-                    for (int e = 0; e < 16; ++e) qs[c + e] = f * d[e];
+                    for (int e = 0; e < 8; ++e) x[e] = bt * (vv[e] - eg * d[cc + e]);
+                    store_split8(&sm.bx[0][mnmaj(wg * HALF + cc, t, 64)], &sm.bx[1][mnmaj(wg * HALF + cc, t, 64)], x);
                 }
+            } else {
+                const float f = sm.eG[t] * qscale;
+#pragma unroll
+                for (int e = 0; e < HALF; ++e) qs[e] = f * d[e];
             }
         }
         GDN_PUBLISH();
 
-        // ---- 10. (U ; P U) = [T; P T] X ------------------------------------------------------------
+        // ---- (U ; P U) = [T; P T] X --------------------------------------------------------------------
+        GDN_WAIT(&sm.mbar_am, c & 1);
+        pend_am = false;
+        GDN_SYNC_OR_ABORT();
         if (tid == 0) {
-            mma_split(tmem + cD3, a_m[0], a_m[1], 1024, b_x[0], b_x[1], 1024, 4,
-                      umma::idesc_bf16(128, DVS, false, true));
-            umma::commit(&sm.mbar);
+            mma_split2(tmem + cD3, a_m[0], a_m[1], 128, 1024, 256, b_x[0], 1024, 256, 4, DVS, false, true);
+            umma::commit(&sm.mbar_mma);
         }
-        GDN_MMA_WAIT();
+        GDN_WAIT(&sm.mbar_mma, ph_mma);
+        ph_mma ^= 1u;
+        GDN_SYNC_OR_ABORT();
+        if (more) issue_am(c + 1);  // [T; P T] image consumed
 
-        // ---- 11. U -> bx;  O = e^G Q S0 / sqrt(dk) + P U -> o ----------------------------------------
+        // ---- e^{G_L-G} U -> bx;  O = e^G Q S0 / sqrt(dk) + P U -> o ------------------------------------
         {
-            const int t = tid & 63;
+            const int t = L & 63;
+            float d[HALF], d2[HALF];
+            umma::tmem_ld32(tmem + lane_off + cD3 + wg * HALF, d);
+            umma::tmem_ld32(tmem + lane_off + cD3 + DVS + wg * HALF, d2);
+            umma::tmem_wait_ld();
 #pragma unroll
-            for (int c = 0; c < DVS; c += 16) {
-                float d[16];
-                umma::tmem_ld16(tmem + lane_off + cD3 + c, d);
-                umma::tmem_wait_ld();
-                if (tid < 64) {
-                    store_split8(&sm.bx[0][mnmaj(c, t, 64)], &sm.bx[1][mnmaj(c, t, 64)], d);
-                    store_split8(&sm.bx[0][mnmaj(c + 8, t, 64)], &sm.bx[1][mnmaj(c + 8, t, 64)], d + 8);
-                } else if (t < n) {
-                    float* dst = p.o + ((size_t)(c0 + t) * p.hv + h) * kHeadDim + v0 + c;
+            for (int e = 0; e < HALF; ++e) d[e] += d2[e];
+            if (L < 64) {
+                const float kd = sm.kdec[t];
 #pragma unroll
-                    for (int e = 0; e < 16; e += 4)
-                        *reinterpret_cast<float4*>(dst + e) =
-                            make_float4(qs[c + e] + d[e], qs[c + e + 1] + d[e + 1], qs[c + e + 2] + d[e + 2],
-                                        qs[c + e + 3] + d[e + 3]);
-                }
+                for (int e = 0; e < HALF; ++e) d[e] *= kd;
+#pragma unroll
+                for (int cc = 0; cc < HALF; cc += 8)
+                    store_split8(&sm.bx[0][mnmaj(wg * HALF + cc, t, 64)], &sm.bx[1][mnmaj(wg * HALF + cc, t, 64)], d + cc);
+            } else {  // O row t -> the (consumed) V tile, written out coalesced below
+                float* dst = &sm.v[t * (DVS + 4) + wg * HALF];
+#pragma unroll
+                for (int e = 0; e < HALF; e += 4)
+                    *reinterpret_cast<float4*>(dst + e) =
+                        make_float4(qs[e] + d[e], qs[e + 1] + d[e + 1], qs[e + 2] + d[e + 2], qs[e + 3] + d[e + 3]);
             }
         }
         GDN_PUBLISH();
 
-        // ---- 12. dS = Kd^T U ---------------------------------------------------------------------------
+        // ---- dS = K^T (e^{G_L-G} U): K^T is the K half of the [K; Q] image, MN-major ------------------
         if (tid == 0) {
-            mma_split(tmem + cD4, a_kt[0], a_kt[1], 1024, b_x[0], b_x[1], 1024, 4,
-                      umma::idesc_bf16(128, DVS, true, true));
-            umma::commit(&sm.mbar);
+            mma_split2(tmem + cD4, a_kq_hi, a_kq_lo, 2048, 128, 4096, b_x[0], 1024, 256, 4, DVS, true, true);
+            umma::commit(&sm.mbar_mma);
         }
-        GDN_MMA_WAIT();
+        // O tile -> global while the state update runs: 16 lanes per 256-byte row
+#pragma unroll
+        for (int q = 0; q < kVq; ++q) {
+            const int u = tid + kChainThreads * q, t = u / (DVS / 4), c4 = (u % (DVS / 4)) * 4;
+            if (t < n)
+                __stcs(reinterpret_cast<float4*>(p.o + ((size_t)(c0 + t) * p.hv + h) * kHeadDim + v0 + c4),
+                       *reinterpret_cast<const float4*>(&sm.v[t * (DVS + 4) + c4]));
+        }
+        GDN_WAIT(&sm.mbar_mma, ph_mma);
+        ph_mma ^= 1u;
+        GDN_SYNC_OR_ABORT();
+        if (more) store_v();  // O tile written out: the next chunk's V goes in
 
-        // ---- 13. S = e^{G_L} S + dS -> registers and bs -------------------------------------------------
+        // ---- S = e^{G_L} S + dS -> registers and bs ----------------------------------------------------
         {
             const float gl = sm.gL;
+            float d[HALF], d2[HALF];
+            umma::tmem_ld32(tmem + lane_off + cD4 + wg * HALF, d);
+            umma::tmem_ld32(tmem + lane_off + cD4 + DVS + wg * HALF, d2);
+            umma::tmem_wait_ld();
 #pragma unroll
-            for (int c = 0; c < DVS; c += 16) {
-                float d[16];
-                umma::tmem_ld16(tmem + lane_off + cD4 + c, d);
-                umma::tmem_wait_ld();
+            for (int e = 0; e < HALF; ++e) d[e] += d2[e];
 #pragma unroll
-                for (int e = 0; e < 16; ++e) S[c + e] = fmaf(gl, S[c + e], d[e]);
-            }
+            for (int e = 0; e < HALF; ++e) S[e] = fmaf(gl, S[e], d[e]);
 #pragma unroll
-            for (int c = 0; c < DVS; c += 8)
-                store_split8(&sm.bs[0][mnmaj(c, tid, 128)], &sm.bs[1][mnmaj(c, tid, 128)], S + c);
+            for (int cc = 0; cc < HALF; cc += 8)
+                store_split8(&sm.bs[0][mnmaj(wg * HALF + cc, L, 128)], &sm.bs[1][mnmaj(wg * HALF + cc, L, 128)], S + cc);
         }
         GDN_PUBLISH();
     }
 
+    {
+        float* dst = p.S_out + sbase + (size_t)L * kHeadDim + v0 + wg * HALF;
 #pragma unroll
-    for (int c = 0; c < DVS; c += 4)
-        *reinterpret_cast<float4*>(p.S_out + sbase + (size_t)tid * kHeadDim + v0 + c) =
-            make_float4(S[c], S[c + 1], S[c + 2], S[c + 3]);
+        for (int c = 0; c < HALF; c += 4)
+            *reinterpret_cast<float4*>(dst + c) = make_float4(S[c], S[c + 1], S[c + 2], S[c + 3]);
+    }
 
 done:
+    // drain any copy still in flight into this CTA's shared memory (bounded), free TMEM
+    if (tid == 0) {
+        for (int b = 0; b < 2; ++b)
+            if (pend_kq[b]) umma::mbar_wait(&sm.mbar_kq[b], 0, 1u << 16), umma::mbar_wait(&sm.mbar_kq[b], 1, 1u << 16);
+        if (pend_am) umma::mbar_wait(&sm.mbar_am, 0, 1u << 16), umma::mbar_wait(&sm.mbar_am, 1, 1u << 16);
+    }
     umma::fence_before_sync();
     __syncthreads();
-    if (warp == 0) umma::tmem_dealloc(tmem, kTmemCols);
-#undef GDN_MMA_WAIT
+    if (warp == 0) umma::tmem_dealloc(sm.tmem_base, kTmemCols);
+#undef GDN_WAIT
+#undef GDN_SYNC_OR_ABORT
 #undef GDN_PUBLISH
 }
 
-constexpr int kDVS = 32;
-
 }  // namespace
 
-size_t scan_workspace_bytes(int, int, int, int) { return 256; }  // error word
+size_t scan_workspace_bytes(int hk, int hv, int n_seq, int T)
+{
+    return kWsHeader + n_slots(T, n_seq) * ((size_t)hv * kAmBytes + (size_t)hk * kKqBytes);
+}
 
 cudaError_t launch_scan(const ScanParams& p, cudaStream_t stream)
 {
     if (p.n_seq == 0) return cudaSuccess;
-    const size_t smem = sizeof(ScanSmem<kDVS>);
-    cudaError_t e = cudaFuncSetAttribute(scan_tc_kernel<kDVS>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    const size_t prep_smem = sizeof(PrepSmem), chain_smem = sizeof(ChainSmem<kDVS>);
+    cudaError_t e = cudaFuncSetAttribute(scan_prep_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)prep_smem);
+    if (e != cudaSuccess) return e;
+    e = cudaFuncSetAttribute(scan_chain_kernel<kDVS>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)chain_smem);
     if (e != cudaSuccess) return e;
     e = cudaMemsetAsync(p.workspace, 0, 4, stream);
     if (e != cudaSuccess) return e;
-    dim3 grid((unsigned)(p.hv * (kHeadDim / kDVS)), (unsigned)p.n_seq);
-    scan_tc_kernel<kDVS><<<grid, kThreads, smem, stream>>>(p);
+    const size_t slots = n_slots(p.T, p.n_seq);
+    if (p.T > 0) {
+        scan_prep_kernel<<<dim3((unsigned)slots, (unsigned)p.hv), kPrepThreads, prep_smem, stream>>>(p);
+        e = cudaGetLastError();
+        if (e != cudaSuccess) return e;
+    }
+    scan_chain_kernel<kDVS><<<dim3((unsigned)(p.hv * (kHeadDim / kDVS)), (unsigned)p.n_seq), kChainThreads,
+                              chain_smem, stream>>>(p);
     return cudaGetLastError();
 }
 
