@@ -23,12 +23,13 @@
 // so (Q S0) and (P U) land in the same TMEM lanes and O needs no exchange.
 //
 // Two kernels:
-//  * scan_prep_kernel, one CTA per (chunk, value head), fully parallel: the
-//    state-independent part.  It splits [K; Q] into the tensor-core layout,
-//    forms K K^T and Q K^T, A and P, inverts I + A (blocked forward
-//    substitution on CUDA cores, 16x16 diagonal blocks), forms [T; P T] and
-//    writes two operand images to the workspace: [T; P T] per (chunk, value
-//    head) and [K; Q] per (chunk, key head).
+//  * scan_prep_kernel, one CTA per (chunk, key head), fully parallel: the
+//    state-independent part.  It splits [K; Q] into the tensor-core layout
+//    and forms K K^T and Q K^T once; then, for each value head reading that
+//    key head, A and P, the inverse of I + A (blocked forward substitution on
+//    CUDA cores, 16x16 diagonal blocks) and [T; P T].  It writes two operand
+//    images to the workspace: [K; Q] per (chunk, key head) and [T; P T] per
+//    (chunk, value head).
 //  * scan_chain_kernel, one CTA per (sequence, value head, 64-column slice):
 //    the state-dependent part, chunk after chunk, with the fp32 state slice
 //    in registers.  The images stream in with bulk asynchronous copies one
@@ -147,7 +148,7 @@ __device__ __forceinline__ float warp_chunk_cumsum(float (&lam)[2], int lane)
 }
 
 // =======================================================================================
-// prep: one CTA per (chunk slot, value head)
+// prep: one CTA per (chunk slot, key head); its value heads one after another
 // =======================================================================================
 constexpr int kPrepThreads = 128;
 
@@ -169,8 +170,8 @@ __global__ void __launch_bounds__(kPrepThreads) scan_prep_kernel(ScanParams p)
     extern __shared__ __align__(1024) unsigned char smem_raw[];
     PrepSmem& sm = *reinterpret_cast<PrepSmem*>(smem_raw);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int slot = blockIdx.x, h = blockIdx.y;
-    const int group = p.hv / p.hk, j = h / group;
+    const int slot = blockIdx.x, j = blockIdx.y;
+    const int group = p.hv / p.hk;
     uint32_t* err = reinterpret_cast<uint32_t*>(p.workspace);
 
     // slot -> (sequence, chunk); last s with base(s) <= slot
@@ -184,7 +185,6 @@ __global__ void __launch_bounds__(kPrepThreads) scan_prep_kernel(ScanParams p)
     const int c0 = start + (slot - slot_base(p, s)) * kChunk;
     if (slot < slot_base(p, s) || c0 >= end) return;  // unused slot (whole CTA)
     const int n = min(kChunk, end - c0);
-    const bool write_kq = (h % group) == 0;
     const float qscale = rsqrtf((float)kHeadDim);
 
     if (warp == 0) umma::tmem_alloc(&sm.tmem_base, 128);
@@ -192,22 +192,24 @@ __global__ void __launch_bounds__(kPrepThreads) scan_prep_kernel(ScanParams p)
         umma::mbar_init(&sm.mbar, 1);
         sm.abort_flag = 0;
     }
-    // [K; Q] -> split tile (and the image for the chain when this CTA owns it).
-    // Unit u = (matrix, token group, column group, row in group), row fastest so
-    // that 8 consecutive lanes fill one 128-byte core matrix.  All 16 units'
-    // loads (and the gates') are in flight together.
-    {
-        float raw_lam[2] = {0.f, 0.f}, raw_beta[2] = {0.f, 0.f};
+    // raw gates of the first value head, in flight with the K/Q loads
+    float raw_lam[2] = {0.f, 0.f}, raw_beta[2] = {0.f, 0.f};
+    auto load_gates = [&](int h) {
         if (warp == 0) {
 #pragma unroll
             for (int q = 0; q < 2; ++q) {
                 const int t = lane + 32 * q;
-                if (t < n) {
-                    raw_lam[q] = __ldg(p.glog + (size_t)(c0 + t) * p.hv + h);
-                    raw_beta[q] = __ldg(p.beta + (size_t)(c0 + t) * p.hv + h);
-                }
+                raw_lam[q] = t < n ? __ldg(p.glog + (size_t)(c0 + t) * p.hv + h) : 0.0f;
+                raw_beta[q] = t < n ? __ldg(p.beta + (size_t)(c0 + t) * p.hv + h) : 0.0f;
             }
         }
+    };
+    load_gates(j * group);
+    // [K; Q] -> split tile and the chain's image.  Unit u = (matrix, token
+    // group, column group, row in group), row fastest so that 8 consecutive
+    // lanes fill one 128-byte core matrix.  All 16 units' loads are in flight
+    // together.
+    {
         float4 ld[32];
 #pragma unroll
         for (int q = 0; q < 16; ++q) {
@@ -222,18 +224,6 @@ __global__ void __launch_bounds__(kPrepThreads) scan_prep_kernel(ScanParams p)
                 ld[2 * q] = ld[2 * q + 1] = make_float4(0.f, 0.f, 0.f, 0.f);
             }
         }
-        if (warp == 0) {  // gates of the chunk
-            float lam[2];
-#pragma unroll
-            for (int q = 0; q < 2; ++q) {
-                const int t = lane + 32 * q;
-                lam[q] = t < n ? fmaxf(raw_lam[q], kLamFloor) : 0.0f;
-                sm.beta[t] = raw_beta[q];
-            }
-            warp_chunk_cumsum(lam, lane);
-            sm.G[lane] = lam[0];
-            sm.G[lane + 32] = lam[1];
-        }
         unsigned char* img = kq_image(p, slot, j);
 #pragma unroll
         for (int q = 0; q < 16; ++q) {
@@ -246,10 +236,8 @@ __global__ void __launch_bounds__(kPrepThreads) scan_prep_kernel(ScanParams p)
             const int off = kmaj(mat * 64 + t, g * 8, 128);
             *reinterpret_cast<uint4*>(&sm.u.akq[0][off]) = vh;
             *reinterpret_cast<uint4*>(&sm.u.akq[1][off]) = vl;
-            if (write_kq) {
-                *reinterpret_cast<uint4*>(img + off * 2) = vh;
-                *reinterpret_cast<uint4*>(img + kKqBytes / 2 + off * 2) = vl;
-            }
+            *reinterpret_cast<uint4*>(img + off * 2) = vh;
+            *reinterpret_cast<uint4*>(img + kKqBytes / 2 + off * 2) = vl;
         }
     }
     umma::fence_proxy_async();
@@ -263,7 +251,7 @@ __global__ void __launch_bounds__(kPrepThreads) scan_prep_kernel(ScanParams p)
     const uint32_t b_t[2] = {umma::smem_u32(sm.u.s.bt[0]), umma::smem_u32(sm.u.s.bt[1])};
     uint32_t phase = 0;
 
-    // (K K^T ; Q K^T) = [K; Q] K^T  (B = the K rows of the same tile)
+    // (K K^T ; Q K^T) = [K; Q] K^T  (B = the K rows of the same tile), shared by the group
     if (tid == 0) {
         mma_split(tmem, a_kq[0], a_kq[1], 128, 2048, 256, a_kq[0], a_kq[1], 2048, 256, 8,
                   umma::idesc_bf16(128, 64, false, false));
@@ -275,181 +263,200 @@ __global__ void __launch_bounds__(kPrepThreads) scan_prep_kernel(ScanParams p)
     if (sm.abort_flag) goto done;
     umma::fence_after_sync();
 
-    // A (fp32, from K K^T rows) and [I; P] (split; P from Q K^T rows)
-    {
-        const int i = tid & 63;
-        const float Gi = sm.G[i];
-        float d[64];
-        {
-            float d0[32], d1[32];
-            umma::tmem_ld32(tmem + lane_off, d0);
-            umma::tmem_ld32(tmem + lane_off + 32, d1);
-            umma::tmem_wait_ld();
+    for (int hh = 0; hh < group; ++hh) {
+        const int h = j * group + hh;
+        // gates of value head h: running log-decay G and beta
+        if (warp == 0) {
+            float lam[2];
 #pragma unroll
-            for (int e = 0; e < 32; ++e) { d[e] = d0[e]; d[32 + e] = d1[e]; }
+            for (int q = 0; q < 2; ++q) lam[q] = (lane + 32 * q) < n ? fmaxf(raw_lam[q], kLamFloor) : 0.0f;
+            const float b0 = raw_beta[0], b1 = raw_beta[1];
+            if (hh + 1 < group) load_gates(h + 1);
+            warp_chunk_cumsum(lam, lane);
+            sm.G[lane] = lam[0];
+            sm.G[lane + 32] = lam[1];
+            sm.beta[lane] = b0;
+            sm.beta[lane + 32] = b1;
         }
-        const float4* G4 = reinterpret_cast<const float4*>(sm.G);
-        if (tid < 64) {
-            const float bi = sm.beta[i];
-#pragma unroll
-            for (int q = 0; q < 16; ++q) {
-                const float4 g = G4[q];
-                const float gg[4] = {g.x, g.y, g.z, g.w};
-                float a[4];
-#pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    const int jj = 4 * q + e;
-                    a[e] = jj < i ? bi * __expf(Gi - gg[e]) * d[jj] : 0.0f;
+        __syncthreads();
+
+        // A (fp32, from K K^T rows) and [I; P] (split; P from Q K^T rows)
+        {
+            const int i = tid & 63;
+            const float Gi = sm.G[i];
+            float d[64];
+            {
+                float d0[32], d1[32];
+                umma::tmem_ld32(tmem + lane_off, d0);
+                umma::tmem_ld32(tmem + lane_off + 32, d1);
+                umma::tmem_wait_ld();
+    #pragma unroll
+                for (int e = 0; e < 32; ++e) { d[e] = d0[e]; d[32 + e] = d1[e]; }
+            }
+            const float4* G4 = reinterpret_cast<const float4*>(sm.G);
+            if (tid < 64) {
+                const float bi = sm.beta[i];
+    #pragma unroll
+                for (int q = 0; q < 16; ++q) {
+                    const float4 g = G4[q];
+                    const float gg[4] = {g.x, g.y, g.z, g.w};
+                    float a[4];
+    #pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const int jj = 4 * q + e;
+                        a[e] = jj < i ? bi * __expf(Gi - gg[e]) * d[jj] : 0.0f;
+                    }
+                    *reinterpret_cast<float4*>(&sm.u.s.A[i * 68 + 4 * q]) = make_float4(a[0], a[1], a[2], a[3]);
                 }
-                *reinterpret_cast<float4*>(&sm.u.s.A[i * 68 + 4 * q]) = make_float4(a[0], a[1], a[2], a[3]);
+    #pragma unroll
+                for (int c = 0; c < 64; c += 8) {
+                    float idr[8];
+    #pragma unroll
+                    for (int e = 0; e < 8; ++e) idr[e] = (c + e == i) ? 1.0f : 0.0f;
+                    store_split8(&sm.am[0][kmaj(i, c, 64)], &sm.am[1][kmaj(i, c, 64)], idr);
+                }
+            } else {
+    #pragma unroll
+                for (int q = 0; q < 8; ++q) {
+                    const float4 ga = G4[2 * q], gb = G4[2 * q + 1];
+                    const float gg[8] = {ga.x, ga.y, ga.z, ga.w, gb.x, gb.y, gb.z, gb.w};
+                    float pr[8];
+    #pragma unroll
+                    for (int e = 0; e < 8; ++e) {
+                        const int jj = 8 * q + e;
+                        pr[e] = jj <= i ? __expf(Gi - gg[e]) * d[jj] * qscale : 0.0f;
+                    }
+                    store_split8(&sm.am[0][kmaj(64 + i, 8 * q, 64)], &sm.am[1][kmaj(64 + i, 8 * q, 64)], pr);
+                }
             }
-#pragma unroll
-            for (int c = 0; c < 64; c += 8) {
-                float idr[8];
-#pragma unroll
-                for (int e = 0; e < 8; ++e) idr[e] = (c + e == i) ? 1.0f : 0.0f;
-                store_split8(&sm.am[0][kmaj(i, c, 64)], &sm.am[1][kmaj(i, c, 64)], idr);
+        }
+        __syncthreads();
+
+        // T = (I + A)^-1 (A strictly lower, fp32, row stride 68).
+        // (1) 16x16 diagonal blocks: thread (b, c) forms column c of inv(I + A_bb) by
+        //     forward substitution, col[r] = [r == c] - sum_{m<r} A[r][m] col[m]; the
+        //     entries above c come out zero by themselves, so the loop has no
+        //     data-dependent branch and reads each A row as broadcast float4s.
+        // (2) off-diagonal blocks by distance: W = sum_m A_(bi,m) T_(m,bj), then
+        //     T_(bi,bj) = -T_(bi,bi) W, each thread a 2 x 4 register tile.
+        {
+            float* A = sm.u.s.A;
+            float* Tm = sm.u.s.T;
+            constexpr int ST = 68;
+            for (int e = tid; e < 64 * ST; e += kPrepThreads) Tm[e] = 0.0f;
+            __syncthreads();
+            if (tid < 64) {
+                const int b = tid >> 4, c = tid & 15, o = 16 * b;
+                float col[16];
+    #pragma unroll
+                for (int r = 0; r < 16; ++r) {
+                    float acc = (r == c) ? 1.0f : 0.0f;
+    #pragma unroll
+                    for (int m4 = 0; m4 < r; m4 += 4) {
+                        const float4 a4 = *reinterpret_cast<const float4*>(&A[(o + r) * ST + o + m4]);
+                        if (m4 + 0 < r) acc = fmaf(-a4.x, col[m4 + 0], acc);
+                        if (m4 + 1 < r) acc = fmaf(-a4.y, col[m4 + 1], acc);
+                        if (m4 + 2 < r) acc = fmaf(-a4.z, col[m4 + 2], acc);
+                        if (m4 + 3 < r) acc = fmaf(-a4.w, col[m4 + 3], acc);
+                    }
+                    col[r] = acc;
+                }
+    #pragma unroll
+                for (int r = 0; r < 16; ++r) Tm[(o + r) * ST + o + c] = col[r];
             }
-        } else {
+            __syncthreads();
+            float* W = sm.W;  // [pair][16][16]
+            const int pr = tid >> 5, q = tid & 31, r0 = 2 * (q >> 2), c0 = 4 * (q & 3);
+            for (int dist = 1; dist < 4; ++dist) {
+                const int bj = pr, bi = pr + dist;
+                const bool active = pr < 4 - dist;
+                if (active) {
+                    float acc[2][4] = {};
+                    for (int m4 = 16 * bj; m4 < 16 * bi; m4 += 4) {
+                        const float4 a0 = *reinterpret_cast<const float4*>(&A[(16 * bi + r0) * ST + m4]);
+                        const float4 a1 = *reinterpret_cast<const float4*>(&A[(16 * bi + r0 + 1) * ST + m4]);
+                        const float av0[4] = {a0.x, a0.y, a0.z, a0.w}, av1[4] = {a1.x, a1.y, a1.z, a1.w};
+    #pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            const float4 t4 = *reinterpret_cast<const float4*>(&Tm[(m4 + e) * ST + 16 * bj + c0]);
+                            acc[0][0] = fmaf(av0[e], t4.x, acc[0][0]); acc[0][1] = fmaf(av0[e], t4.y, acc[0][1]);
+                            acc[0][2] = fmaf(av0[e], t4.z, acc[0][2]); acc[0][3] = fmaf(av0[e], t4.w, acc[0][3]);
+                            acc[1][0] = fmaf(av1[e], t4.x, acc[1][0]); acc[1][1] = fmaf(av1[e], t4.y, acc[1][1]);
+                            acc[1][2] = fmaf(av1[e], t4.z, acc[1][2]); acc[1][3] = fmaf(av1[e], t4.w, acc[1][3]);
+                        }
+                    }
+                    *reinterpret_cast<float4*>(&W[pr * 256 + r0 * 16 + c0]) = make_float4(acc[0][0], acc[0][1], acc[0][2], acc[0][3]);
+                    *reinterpret_cast<float4*>(&W[pr * 256 + (r0 + 1) * 16 + c0]) = make_float4(acc[1][0], acc[1][1], acc[1][2], acc[1][3]);
+                }
+                __syncthreads();
+                if (active) {
+                    float acc[2][4] = {};
+    #pragma unroll
+                    for (int m4 = 0; m4 < 16; m4 += 4) {
+                        const float4 a0 = *reinterpret_cast<const float4*>(&Tm[(16 * bi + r0) * ST + 16 * bi + m4]);
+                        const float4 a1 = *reinterpret_cast<const float4*>(&Tm[(16 * bi + r0 + 1) * ST + 16 * bi + m4]);
+                        const float av0[4] = {a0.x, a0.y, a0.z, a0.w}, av1[4] = {a1.x, a1.y, a1.z, a1.w};
+    #pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            const float4 w4 = *reinterpret_cast<const float4*>(&W[pr * 256 + (m4 + e) * 16 + c0]);
+                            acc[0][0] = fmaf(av0[e], w4.x, acc[0][0]); acc[0][1] = fmaf(av0[e], w4.y, acc[0][1]);
+                            acc[0][2] = fmaf(av0[e], w4.z, acc[0][2]); acc[0][3] = fmaf(av0[e], w4.w, acc[0][3]);
+                            acc[1][0] = fmaf(av1[e], w4.x, acc[1][0]); acc[1][1] = fmaf(av1[e], w4.y, acc[1][1]);
+                            acc[1][2] = fmaf(av1[e], w4.z, acc[1][2]); acc[1][3] = fmaf(av1[e], w4.w, acc[1][3]);
+                        }
+                    }
+                    *reinterpret_cast<float4*>(&Tm[(16 * bi + r0) * ST + 16 * bj + c0]) =
+                        make_float4(-acc[0][0], -acc[0][1], -acc[0][2], -acc[0][3]);
+                    *reinterpret_cast<float4*>(&Tm[(16 * bi + r0 + 1) * ST + 16 * bj + c0]) =
+                        make_float4(-acc[1][0], -acc[1][1], -acc[1][2], -acc[1][3]);
+                }
+                __syncthreads();
+            }
+            // T -> MN-major B tile (element (n = column, k = row)); row fastest across lanes
+            for (int u = tid; u < 64 * 8; u += kPrepThreads) {
+                const int m = u & 63, g = u >> 6;
+                const float4 x0 = *reinterpret_cast<const float4*>(&Tm[m * ST + g * 8]);
+                const float4 x1 = *reinterpret_cast<const float4*>(&Tm[m * ST + g * 8 + 4]);
+                const float tr[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
+                store_split8(&sm.u.s.bt[0][mnmaj(g * 8, m, 64)], &sm.u.s.bt[1][mnmaj(g * 8, m, 64)], tr);
+            }
+        }
+        umma::fence_proxy_async();
+        umma::fence_before_sync();
+        __syncthreads();
+        umma::fence_after_sync();
+
+        // (T ; P T) = [I; P] T
+        if (tid == 0) {
+            mma_split(tmem + 64, a_m[0], a_m[1], 128, 1024, 256, b_t[0], b_t[1], 1024, 256, 4,
+                      umma::idesc_bf16(128, 64, false, true));
+            umma::commit(&sm.mbar);
+        }
+        if (!umma::mbar_wait(&sm.mbar, phase)) { sm.abort_flag = 1; atomicOr(err, kErrTimeout); }
+        phase ^= 1u;
+        __syncthreads();
+        if (sm.abort_flag) goto done;
+        umma::fence_after_sync();
+
+        // [T; P T] -> image (K-major, split), row `tid` per thread
+        {
+            unsigned char* img = am_image(p, slot, h);
+            float d0[32], d1[32];
+            umma::tmem_ld32(tmem + lane_off + 64, d0);
+            umma::tmem_ld32(tmem + lane_off + 96, d1);
+            umma::tmem_wait_ld();
 #pragma unroll
             for (int q = 0; q < 8; ++q) {
-                const float4 ga = G4[2 * q], gb = G4[2 * q + 1];
-                const float gg[8] = {ga.x, ga.y, ga.z, ga.w, gb.x, gb.y, gb.z, gb.w};
-                float pr[8];
-#pragma unroll
-                for (int e = 0; e < 8; ++e) {
-                    const int jj = 8 * q + e;
-                    pr[e] = jj <= i ? __expf(Gi - gg[e]) * d[jj] * qscale : 0.0f;
-                }
-                store_split8(&sm.am[0][kmaj(64 + i, 8 * q, 64)], &sm.am[1][kmaj(64 + i, 8 * q, 64)], pr);
-            }
-        }
-    }
-    __syncthreads();
-
-    // T = (I + A)^-1 (A strictly lower, fp32, row stride 68).
-    // (1) 16x16 diagonal blocks: thread (b, c) forms column c of inv(I + A_bb) by
-    //     forward substitution, col[r] = [r == c] - sum_{m<r} A[r][m] col[m]; the
-    //     entries above c come out zero by themselves, so the loop has no
-    //     data-dependent branch and reads each A row as broadcast float4s.
-    // (2) off-diagonal blocks by distance: W = sum_m A_(bi,m) T_(m,bj), then
-    //     T_(bi,bj) = -T_(bi,bi) W, each thread a 2 x 4 register tile.
-    {
-        float* A = sm.u.s.A;
-        float* Tm = sm.u.s.T;
-        constexpr int ST = 68;
-        for (int e = tid; e < 64 * ST; e += kPrepThreads) Tm[e] = 0.0f;
-        __syncthreads();
-        if (tid < 64) {
-            const int b = tid >> 4, c = tid & 15, o = 16 * b;
-            float col[16];
-#pragma unroll
-            for (int r = 0; r < 16; ++r) {
-                float acc = (r == c) ? 1.0f : 0.0f;
-#pragma unroll
-                for (int m4 = 0; m4 < r; m4 += 4) {
-                    const float4 a4 = *reinterpret_cast<const float4*>(&A[(o + r) * ST + o + m4]);
-                    if (m4 + 0 < r) acc = fmaf(-a4.x, col[m4 + 0], acc);
-                    if (m4 + 1 < r) acc = fmaf(-a4.y, col[m4 + 1], acc);
-                    if (m4 + 2 < r) acc = fmaf(-a4.z, col[m4 + 2], acc);
-                    if (m4 + 3 < r) acc = fmaf(-a4.w, col[m4 + 3], acc);
-                }
-                col[r] = acc;
-            }
-#pragma unroll
-            for (int r = 0; r < 16; ++r) Tm[(o + r) * ST + o + c] = col[r];
-        }
-        __syncthreads();
-        float* W = sm.W;  // [pair][16][16]
-        const int pr = tid >> 5, q = tid & 31, r0 = 2 * (q >> 2), c0 = 4 * (q & 3);
-        for (int dist = 1; dist < 4; ++dist) {
-            const int bj = pr, bi = pr + dist;
-            const bool active = pr < 4 - dist;
-            if (active) {
-                float acc[2][4] = {};
-                for (int m4 = 16 * bj; m4 < 16 * bi; m4 += 4) {
-                    const float4 a0 = *reinterpret_cast<const float4*>(&A[(16 * bi + r0) * ST + m4]);
-                    const float4 a1 = *reinterpret_cast<const float4*>(&A[(16 * bi + r0 + 1) * ST + m4]);
-                    const float av0[4] = {a0.x, a0.y, a0.z, a0.w}, av1[4] = {a1.x, a1.y, a1.z, a1.w};
-#pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        const float4 t4 = *reinterpret_cast<const float4*>(&Tm[(m4 + e) * ST + 16 * bj + c0]);
-                        acc[0][0] = fmaf(av0[e], t4.x, acc[0][0]); acc[0][1] = fmaf(av0[e], t4.y, acc[0][1]);
-                        acc[0][2] = fmaf(av0[e], t4.z, acc[0][2]); acc[0][3] = fmaf(av0[e], t4.w, acc[0][3]);
-                        acc[1][0] = fmaf(av1[e], t4.x, acc[1][0]); acc[1][1] = fmaf(av1[e], t4.y, acc[1][1]);
-                        acc[1][2] = fmaf(av1[e], t4.z, acc[1][2]); acc[1][3] = fmaf(av1[e], t4.w, acc[1][3]);
-                    }
-                }
-                *reinterpret_cast<float4*>(&W[pr * 256 + r0 * 16 + c0]) = make_float4(acc[0][0], acc[0][1], acc[0][2], acc[0][3]);
-                *reinterpret_cast<float4*>(&W[pr * 256 + (r0 + 1) * 16 + c0]) = make_float4(acc[1][0], acc[1][1], acc[1][2], acc[1][3]);
-            }
-            __syncthreads();
-            if (active) {
-                float acc[2][4] = {};
-#pragma unroll
-                for (int m4 = 0; m4 < 16; m4 += 4) {
-                    const float4 a0 = *reinterpret_cast<const float4*>(&Tm[(16 * bi + r0) * ST + 16 * bi + m4]);
-                    const float4 a1 = *reinterpret_cast<const float4*>(&Tm[(16 * bi + r0 + 1) * ST + 16 * bi + m4]);
-                    const float av0[4] = {a0.x, a0.y, a0.z, a0.w}, av1[4] = {a1.x, a1.y, a1.z, a1.w};
-#pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        const float4 w4 = *reinterpret_cast<const float4*>(&W[pr * 256 + (m4 + e) * 16 + c0]);
-                        acc[0][0] = fmaf(av0[e], w4.x, acc[0][0]); acc[0][1] = fmaf(av0[e], w4.y, acc[0][1]);
-                        acc[0][2] = fmaf(av0[e], w4.z, acc[0][2]); acc[0][3] = fmaf(av0[e], w4.w, acc[0][3]);
-                        acc[1][0] = fmaf(av1[e], w4.x, acc[1][0]); acc[1][1] = fmaf(av1[e], w4.y, acc[1][1]);
-                        acc[1][2] = fmaf(av1[e], w4.z, acc[1][2]); acc[1][3] = fmaf(av1[e], w4.w, acc[1][3]);
-                    }
-                }
-                *reinterpret_cast<float4*>(&Tm[(16 * bi + r0) * ST + 16 * bj + c0]) =
-                    make_float4(-acc[0][0], -acc[0][1], -acc[0][2], -acc[0][3]);
-                *reinterpret_cast<float4*>(&Tm[(16 * bi + r0 + 1) * ST + 16 * bj + c0]) =
-                    make_float4(-acc[1][0], -acc[1][1], -acc[1][2], -acc[1][3]);
-            }
-            __syncthreads();
-        }
-        // T -> MN-major B tile (element (n = column, k = row)); row fastest across lanes
-        for (int u = tid; u < 64 * 8; u += kPrepThreads) {
-            const int m = u & 63, g = u >> 6;
-            const float4 x0 = *reinterpret_cast<const float4*>(&Tm[m * ST + g * 8]);
-            const float4 x1 = *reinterpret_cast<const float4*>(&Tm[m * ST + g * 8 + 4]);
-            const float tr[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
-            store_split8(&sm.u.s.bt[0][mnmaj(g * 8, m, 64)], &sm.u.s.bt[1][mnmaj(g * 8, m, 64)], tr);
-        }
-    }
-    umma::fence_proxy_async();
-    umma::fence_before_sync();
-    __syncthreads();
-    umma::fence_after_sync();
-
-    // (T ; P T) = [I; P] T
-    if (tid == 0) {
-        mma_split(tmem + 64, a_m[0], a_m[1], 128, 1024, 256, b_t[0], b_t[1], 1024, 256, 4,
-                  umma::idesc_bf16(128, 64, false, true));
-        umma::commit(&sm.mbar);
-    }
-    if (!umma::mbar_wait(&sm.mbar, phase)) { sm.abort_flag = 1; atomicOr(err, kErrTimeout); }
-    phase ^= 1u;
-    __syncthreads();
-    if (sm.abort_flag) goto done;
-    umma::fence_after_sync();
-
-    // [T; P T] -> image (K-major, split), row `tid` per thread
-    {
-        unsigned char* img = am_image(p, slot, h);
-#pragma unroll 1
-        for (int c = 0; c < 64; c += 16) {
-            float d[16];
-            umma::tmem_ld16(tmem + lane_off + 64 + c, d);
-            umma::tmem_wait_ld();
-#pragma unroll
-            for (int q = 0; q < 2; ++q) {
                 uint4 vh, vl;
-                split8(d + 8 * q, vh, vl);
-                const int off = kmaj(tid, c + 8 * q, 64);
+                split8(q < 4 ? d0 + 8 * q : d1 + 8 * (q - 4), vh, vl);
+                const int off = kmaj(tid, 8 * q, 64);
                 *reinterpret_cast<uint4*>(img + off * 2) = vh;
                 *reinterpret_cast<uint4*>(img + kAmBytes / 2 + off * 2) = vl;
             }
         }
+        umma::fence_before_sync();
+        __syncthreads();
+        umma::fence_after_sync();
     }
 
 done:
@@ -803,7 +810,7 @@ cudaError_t launch_scan(const ScanParams& p, cudaStream_t stream)
     if (e != cudaSuccess) return e;
     const size_t slots = n_slots(p.T, p.n_seq);
     if (p.T > 0) {
-        scan_prep_kernel<<<dim3((unsigned)slots, (unsigned)p.hv), kPrepThreads, prep_smem, stream>>>(p);
+        scan_prep_kernel<<<dim3((unsigned)slots, (unsigned)p.hk), kPrepThreads, prep_smem, stream>>>(p);
         e = cudaGetLastError();
         if (e != cudaSuccess) return e;
     }
