@@ -55,7 +55,7 @@ PRE_BYTES_SEQ = C * 16 + 2 * C * 3 * 2 + 2 * HV * 4   # conv_w, hist in+out, A_l
 def parse():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--steps", type=int, default=100)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -108,7 +108,7 @@ class ClockSampler:
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
-                 "-lms", "200"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
             self.reader = threading.Thread(target=self._read, daemon=True)
             self.reader.start()
         except (OSError, FileNotFoundError):
@@ -147,6 +147,32 @@ class ClockSampler:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0}
         return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
                 "samples": len(sm)}
+
+
+STAGE_SOURCES = {"pre": ["gdn_pre.cu"], "scan": ["gdn_scan.cu", "umma.cuh"], "post": ["gdn_post.cu"]}
+
+
+def source_digest(stage: str) -> str:
+    import hashlib
+    h = hashlib.sha256()
+    for name in STAGE_SOURCES[stage] + ["gdn_internal.cuh"]:
+        with open(os.path.join(ROOT, "gated_deltanet_linear_pre_gb300", "csrc", name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()
+
+
+def stage_traffic(stage: str):
+    """DRAM bytes (read + write) per launch of a stage from the committed ncu
+    capture in profiles/traffic.json; None when the stage's kernels changed
+    since the capture."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(path):
+        return None
+    with open(path) as f:
+        rec = json.load(f).get(stage)
+    if not rec or rec.get("source_sha256") != source_digest(stage):
+        return None
+    return rec.get("dram_bytes_per_launch")
 
 
 def load_peaks():
@@ -350,11 +376,7 @@ def main():
         stages[k] = {"ms_per_launch": per_launch_ms[k], "alg_bytes_per_launch": stage_bytes[k],
                      "achieved_gbs": gbs, "frac_of_hbm": gbs / hbm_peak}
     dom = max(per_launch_ms, key=per_launch_ms.get)
-    traffic = None
-    prof_path = os.path.join(ROOT, "profiles", "traffic.json")
-    if os.path.exists(prof_path):
-        with open(prof_path) as f:
-            traffic = json.load(f).get(dom)
+    traffic = stage_traffic(dom)
     roofline = {"bound": "hbm", "kernel": f"gdn_{dom}", "achieved": stages[dom]["achieved_gbs"], "peak": hbm_peak,
                 "unit": "GB/s", "frac": stages[dom]["frac_of_hbm"], "traffic": traffic,
                 "peak_source": f"{peak_src} (MEASURED_PEAKS.json hbm_gbs)" if peak_src == "measured" else "fallback"}

@@ -150,7 +150,7 @@ __device__ __forceinline__ float warp_chunk_cumsum(float (&lam)[2], int lane)
 // =======================================================================================
 // prep: one CTA per (chunk slot, key head); its value heads one after another
 // =======================================================================================
-constexpr int kPrepThreads = 128;
+constexpr int kPrepThreads = 256;  // two warpgroups: each covers all 128 TMEM lanes, half the columns
 
 struct __align__(1024) PrepSmem {
     union {
@@ -170,9 +170,11 @@ __global__ void __launch_bounds__(kPrepThreads) scan_prep_kernel(ScanParams p)
     extern __shared__ __align__(1024) unsigned char smem_raw[];
     PrepSmem& sm = *reinterpret_cast<PrepSmem*>(smem_raw);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int L = tid & 127, wg = tid >> 7;  // TMEM lane, column half
     const int slot = blockIdx.x, j = blockIdx.y;
     const int group = p.hv / p.hk;
     uint32_t* err = reinterpret_cast<uint32_t*>(p.workspace);
+    constexpr int ST = 68;  // fp32 row stride of A and T
 
     // slot -> (sequence, chunk); last s with base(s) <= slot
     int lo = 0, hi = p.n_seq - 1;
@@ -192,7 +194,7 @@ __global__ void __launch_bounds__(kPrepThreads) scan_prep_kernel(ScanParams p)
         umma::mbar_init(&sm.mbar, 1);
         sm.abort_flag = 0;
     }
-    // raw gates of the first value head, in flight with the K/Q loads
+    // raw gates of a value head, loaded by warp 0 one head ahead
     float raw_lam[2] = {0.f, 0.f}, raw_beta[2] = {0.f, 0.f};
     auto load_gates = [&](int h) {
         if (warp == 0) {
@@ -207,12 +209,12 @@ __global__ void __launch_bounds__(kPrepThreads) scan_prep_kernel(ScanParams p)
     load_gates(j * group);
     // [K; Q] -> split tile and the chain's image.  Unit u = (matrix, token
     // group, column group, row in group), row fastest so that 8 consecutive
-    // lanes fill one 128-byte core matrix.  All 16 units' loads are in flight
-    // together.
+    // lanes fill one 128-byte core matrix; all loads in flight together.
     {
-        float4 ld[32];
+        constexpr int kU = 2 * 64 * 16 / kPrepThreads;
+        float4 ld[2 * kU];
 #pragma unroll
-        for (int q = 0; q < 16; ++q) {
+        for (int q = 0; q < kU; ++q) {
             const int u = tid + kPrepThreads * q;
             const int mat = u >> 10, tg = (u >> 7) & 7, g = (u >> 3) & 15, t = tg * 8 + (u & 7);
             if (t < n) {
@@ -226,7 +228,7 @@ __global__ void __launch_bounds__(kPrepThreads) scan_prep_kernel(ScanParams p)
         }
         unsigned char* img = kq_image(p, slot, j);
 #pragma unroll
-        for (int q = 0; q < 16; ++q) {
+        for (int q = 0; q < kU; ++q) {
             const int u = tid + kPrepThreads * q;
             const int mat = u >> 10, tg = (u >> 7) & 7, g = (u >> 3) & 15, t = tg * 8 + (u & 7);
             const float x[8] = {ld[2 * q].x, ld[2 * q].y, ld[2 * q].z, ld[2 * q].w,
@@ -245,7 +247,7 @@ __global__ void __launch_bounds__(kPrepThreads) scan_prep_kernel(ScanParams p)
     __syncthreads();
     umma::fence_after_sync();
     const uint32_t tmem = sm.tmem_base;
-    const uint32_t lane_off = (uint32_t)(warp * 32) << 16;
+    const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
     const uint32_t a_kq[2] = {umma::smem_u32(sm.u.akq[0]), umma::smem_u32(sm.u.akq[1])};
     const uint32_t a_m[2] = {umma::smem_u32(sm.am[0]), umma::smem_u32(sm.am[1])};
     const uint32_t b_t[2] = {umma::smem_u32(sm.u.s.bt[0]), umma::smem_u32(sm.u.s.bt[1])};
@@ -280,78 +282,71 @@ __global__ void __launch_bounds__(kPrepThreads) scan_prep_kernel(ScanParams p)
         }
         __syncthreads();
 
-        // A (fp32, from K K^T rows) and [I; P] (split; P from Q K^T rows)
+        // A (fp32, from the K K^T rows) and [I; P] (split; P from the Q K^T rows);
+        // thread (L, wg) does columns [32 wg, 32 wg + 32) of row L & 63
         {
-            const int i = tid & 63;
+            const int i = L & 63, cb = 32 * wg;
             const float Gi = sm.G[i];
-            float d[64];
-            {
-                float d0[32], d1[32];
-                umma::tmem_ld32(tmem + lane_off, d0);
-                umma::tmem_ld32(tmem + lane_off + 32, d1);
-                umma::tmem_wait_ld();
-    #pragma unroll
-                for (int e = 0; e < 32; ++e) { d[e] = d0[e]; d[32 + e] = d1[e]; }
-            }
-            const float4* G4 = reinterpret_cast<const float4*>(sm.G);
-            if (tid < 64) {
+            float d[32];
+            umma::tmem_ld32(tmem + lane_off + cb, d);
+            umma::tmem_wait_ld();
+            const float4* G4 = reinterpret_cast<const float4*>(sm.G + cb);
+            if (L < 64) {
                 const float bi = sm.beta[i];
-    #pragma unroll
-                for (int q = 0; q < 16; ++q) {
+#pragma unroll
+                for (int q = 0; q < 8; ++q) {
                     const float4 g = G4[q];
                     const float gg[4] = {g.x, g.y, g.z, g.w};
                     float a[4];
-    #pragma unroll
+#pragma unroll
                     for (int e = 0; e < 4; ++e) {
-                        const int jj = 4 * q + e;
-                        a[e] = jj < i ? bi * __expf(Gi - gg[e]) * d[jj] : 0.0f;
+                        const int jj = cb + 4 * q + e;
+                        a[e] = jj < i ? bi * __expf(Gi - gg[e]) * d[4 * q + e] : 0.0f;
                     }
-                    *reinterpret_cast<float4*>(&sm.u.s.A[i * 68 + 4 * q]) = make_float4(a[0], a[1], a[2], a[3]);
+                    *reinterpret_cast<float4*>(&sm.u.s.A[i * ST + cb + 4 * q]) = make_float4(a[0], a[1], a[2], a[3]);
                 }
-    #pragma unroll
-                for (int c = 0; c < 64; c += 8) {
+#pragma unroll
+                for (int c = 0; c < 32; c += 8) {
                     float idr[8];
-    #pragma unroll
-                    for (int e = 0; e < 8; ++e) idr[e] = (c + e == i) ? 1.0f : 0.0f;
-                    store_split8(&sm.am[0][kmaj(i, c, 64)], &sm.am[1][kmaj(i, c, 64)], idr);
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) idr[e] = (cb + c + e == i) ? 1.0f : 0.0f;
+                    store_split8(&sm.am[0][kmaj(i, cb + c, 64)], &sm.am[1][kmaj(i, cb + c, 64)], idr);
                 }
             } else {
-    #pragma unroll
-                for (int q = 0; q < 8; ++q) {
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
                     const float4 ga = G4[2 * q], gb = G4[2 * q + 1];
                     const float gg[8] = {ga.x, ga.y, ga.z, ga.w, gb.x, gb.y, gb.z, gb.w};
                     float pr[8];
-    #pragma unroll
+#pragma unroll
                     for (int e = 0; e < 8; ++e) {
-                        const int jj = 8 * q + e;
-                        pr[e] = jj <= i ? __expf(Gi - gg[e]) * d[jj] * qscale : 0.0f;
+                        const int jj = cb + 8 * q + e;
+                        pr[e] = jj <= i ? __expf(Gi - gg[e]) * d[8 * q + e] * qscale : 0.0f;
                     }
-                    store_split8(&sm.am[0][kmaj(64 + i, 8 * q, 64)], &sm.am[1][kmaj(64 + i, 8 * q, 64)], pr);
+                    store_split8(&sm.am[0][kmaj(64 + i, cb + 8 * q, 64)], &sm.am[1][kmaj(64 + i, cb + 8 * q, 64)], pr);
                 }
             }
         }
         __syncthreads();
 
-        // T = (I + A)^-1 (A strictly lower, fp32, row stride 68).
-        // (1) 16x16 diagonal blocks: thread (b, c) forms column c of inv(I + A_bb) by
-        //     forward substitution, col[r] = [r == c] - sum_{m<r} A[r][m] col[m]; the
+        // T = (I + A)^-1 (A strictly lower).  Only the block lower triangle of T
+        // is ever written or read.
+        // (1) 16x16 diagonal blocks: thread (b, c) forms column c of inv(I + A_bb)
+        //     by forward substitution, col[r] = [r == c] - sum_{m<r} A[r][m] col[m];
         //     entries above c come out zero by themselves, so the loop has no
         //     data-dependent branch and reads each A row as broadcast float4s.
         // (2) off-diagonal blocks by distance: W = sum_m A_(bi,m) T_(m,bj), then
-        //     T_(bi,bj) = -T_(bi,bi) W, each thread a 2 x 4 register tile.
+        //     T_(bi,bj) = -T_(bi,bi) W, one 1 x 4 register tile per thread.
         {
             float* A = sm.u.s.A;
             float* Tm = sm.u.s.T;
-            constexpr int ST = 68;
-            for (int e = tid; e < 64 * ST; e += kPrepThreads) Tm[e] = 0.0f;
-            __syncthreads();
             if (tid < 64) {
                 const int b = tid >> 4, c = tid & 15, o = 16 * b;
                 float col[16];
-    #pragma unroll
+#pragma unroll
                 for (int r = 0; r < 16; ++r) {
                     float acc = (r == c) ? 1.0f : 0.0f;
-    #pragma unroll
+#pragma unroll
                     for (int m4 = 0; m4 < r; m4 += 4) {
                         const float4 a4 = *reinterpret_cast<const float4*>(&A[(o + r) * ST + o + m4]);
                         if (m4 + 0 < r) acc = fmaf(-a4.x, col[m4 + 0], acc);
@@ -361,63 +356,62 @@ __global__ void __launch_bounds__(kPrepThreads) scan_prep_kernel(ScanParams p)
                     }
                     col[r] = acc;
                 }
-    #pragma unroll
+#pragma unroll
                 for (int r = 0; r < 16; ++r) Tm[(o + r) * ST + o + c] = col[r];
             }
             __syncthreads();
             float* W = sm.W;  // [pair][16][16]
-            const int pr = tid >> 5, q = tid & 31, r0 = 2 * (q >> 2), c0 = 4 * (q & 3);
+            const int pr = tid >> 6, q = tid & 63, r = q >> 2, c4 = 4 * (q & 3);
             for (int dist = 1; dist < 4; ++dist) {
                 const int bj = pr, bi = pr + dist;
                 const bool active = pr < 4 - dist;
                 if (active) {
-                    float acc[2][4] = {};
+                    float acc[4] = {0.f, 0.f, 0.f, 0.f};
                     for (int m4 = 16 * bj; m4 < 16 * bi; m4 += 4) {
-                        const float4 a0 = *reinterpret_cast<const float4*>(&A[(16 * bi + r0) * ST + m4]);
-                        const float4 a1 = *reinterpret_cast<const float4*>(&A[(16 * bi + r0 + 1) * ST + m4]);
-                        const float av0[4] = {a0.x, a0.y, a0.z, a0.w}, av1[4] = {a1.x, a1.y, a1.z, a1.w};
-    #pragma unroll
+                        const float4 a4 = *reinterpret_cast<const float4*>(&A[(16 * bi + r) * ST + m4]);
+                        const float av[4] = {a4.x, a4.y, a4.z, a4.w};
+#pragma unroll
                         for (int e = 0; e < 4; ++e) {
-                            const float4 t4 = *reinterpret_cast<const float4*>(&Tm[(m4 + e) * ST + 16 * bj + c0]);
-                            acc[0][0] = fmaf(av0[e], t4.x, acc[0][0]); acc[0][1] = fmaf(av0[e], t4.y, acc[0][1]);
-                            acc[0][2] = fmaf(av0[e], t4.z, acc[0][2]); acc[0][3] = fmaf(av0[e], t4.w, acc[0][3]);
-                            acc[1][0] = fmaf(av1[e], t4.x, acc[1][0]); acc[1][1] = fmaf(av1[e], t4.y, acc[1][1]);
-                            acc[1][2] = fmaf(av1[e], t4.z, acc[1][2]); acc[1][3] = fmaf(av1[e], t4.w, acc[1][3]);
+                            const float4 t4 = *reinterpret_cast<const float4*>(&Tm[(m4 + e) * ST + 16 * bj + c4]);
+                            acc[0] = fmaf(av[e], t4.x, acc[0]); acc[1] = fmaf(av[e], t4.y, acc[1]);
+                            acc[2] = fmaf(av[e], t4.z, acc[2]); acc[3] = fmaf(av[e], t4.w, acc[3]);
                         }
                     }
-                    *reinterpret_cast<float4*>(&W[pr * 256 + r0 * 16 + c0]) = make_float4(acc[0][0], acc[0][1], acc[0][2], acc[0][3]);
-                    *reinterpret_cast<float4*>(&W[pr * 256 + (r0 + 1) * 16 + c0]) = make_float4(acc[1][0], acc[1][1], acc[1][2], acc[1][3]);
+                    *reinterpret_cast<float4*>(&W[pr * 256 + r * 16 + c4]) = make_float4(acc[0], acc[1], acc[2], acc[3]);
                 }
                 __syncthreads();
                 if (active) {
-                    float acc[2][4] = {};
-    #pragma unroll
+                    float acc[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
                     for (int m4 = 0; m4 < 16; m4 += 4) {
-                        const float4 a0 = *reinterpret_cast<const float4*>(&Tm[(16 * bi + r0) * ST + 16 * bi + m4]);
-                        const float4 a1 = *reinterpret_cast<const float4*>(&Tm[(16 * bi + r0 + 1) * ST + 16 * bi + m4]);
-                        const float av0[4] = {a0.x, a0.y, a0.z, a0.w}, av1[4] = {a1.x, a1.y, a1.z, a1.w};
-    #pragma unroll
+                        const float4 a4 = *reinterpret_cast<const float4*>(&Tm[(16 * bi + r) * ST + 16 * bi + m4]);
+                        const float av[4] = {a4.x, a4.y, a4.z, a4.w};
+#pragma unroll
                         for (int e = 0; e < 4; ++e) {
-                            const float4 w4 = *reinterpret_cast<const float4*>(&W[pr * 256 + (m4 + e) * 16 + c0]);
-                            acc[0][0] = fmaf(av0[e], w4.x, acc[0][0]); acc[0][1] = fmaf(av0[e], w4.y, acc[0][1]);
-                            acc[0][2] = fmaf(av0[e], w4.z, acc[0][2]); acc[0][3] = fmaf(av0[e], w4.w, acc[0][3]);
-                            acc[1][0] = fmaf(av1[e], w4.x, acc[1][0]); acc[1][1] = fmaf(av1[e], w4.y, acc[1][1]);
-                            acc[1][2] = fmaf(av1[e], w4.z, acc[1][2]); acc[1][3] = fmaf(av1[e], w4.w, acc[1][3]);
+                            const float4 w4 = *reinterpret_cast<const float4*>(&W[pr * 256 + (m4 + e) * 16 + c4]);
+                            acc[0] = fmaf(av[e], w4.x, acc[0]); acc[1] = fmaf(av[e], w4.y, acc[1]);
+                            acc[2] = fmaf(av[e], w4.z, acc[2]); acc[3] = fmaf(av[e], w4.w, acc[3]);
                         }
                     }
-                    *reinterpret_cast<float4*>(&Tm[(16 * bi + r0) * ST + 16 * bj + c0]) =
-                        make_float4(-acc[0][0], -acc[0][1], -acc[0][2], -acc[0][3]);
-                    *reinterpret_cast<float4*>(&Tm[(16 * bi + r0 + 1) * ST + 16 * bj + c0]) =
-                        make_float4(-acc[1][0], -acc[1][1], -acc[1][2], -acc[1][3]);
+                    *reinterpret_cast<float4*>(&Tm[(16 * bi + r) * ST + 16 * bj + c4]) =
+                        make_float4(-acc[0], -acc[1], -acc[2], -acc[3]);
                 }
                 __syncthreads();
             }
-            // T -> MN-major B tile (element (n = column, k = row)); row fastest across lanes
+            // T -> MN-major B tile (element (n = column, k = row)); row fastest across
+            // lanes; column groups right of the row's diagonal block are zero
             for (int u = tid; u < 64 * 8; u += kPrepThreads) {
                 const int m = u & 63, g = u >> 6;
-                const float4 x0 = *reinterpret_cast<const float4*>(&Tm[m * ST + g * 8]);
-                const float4 x1 = *reinterpret_cast<const float4*>(&Tm[m * ST + g * 8 + 4]);
-                const float tr[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
+                float tr[8];
+                if ((g >> 1) <= (m >> 4)) {
+                    const float4 x0 = *reinterpret_cast<const float4*>(&Tm[m * ST + g * 8]);
+                    const float4 x1 = *reinterpret_cast<const float4*>(&Tm[m * ST + g * 8 + 4]);
+                    tr[0] = x0.x; tr[1] = x0.y; tr[2] = x0.z; tr[3] = x0.w;
+                    tr[4] = x1.x; tr[5] = x1.y; tr[6] = x1.z; tr[7] = x1.w;
+                } else {
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) tr[e] = 0.0f;
+                }
                 store_split8(&sm.u.s.bt[0][mnmaj(g * 8, m, 64)], &sm.u.s.bt[1][mnmaj(g * 8, m, 64)], tr);
             }
         }
@@ -438,18 +432,17 @@ __global__ void __launch_bounds__(kPrepThreads) scan_prep_kernel(ScanParams p)
         if (sm.abort_flag) goto done;
         umma::fence_after_sync();
 
-        // [T; P T] -> image (K-major, split), row `tid` per thread
+        // [T; P T] -> image (K-major, split): thread (L, wg) writes row L, columns of wg
         {
             unsigned char* img = am_image(p, slot, h);
-            float d0[32], d1[32];
-            umma::tmem_ld32(tmem + lane_off + 64, d0);
-            umma::tmem_ld32(tmem + lane_off + 96, d1);
+            float d[32];
+            umma::tmem_ld32(tmem + lane_off + 64 + 32 * wg, d);
             umma::tmem_wait_ld();
 #pragma unroll
-            for (int q = 0; q < 8; ++q) {
+            for (int q = 0; q < 4; ++q) {
                 uint4 vh, vl;
-                split8(q < 4 ? d0 + 8 * q : d1 + 8 * (q - 4), vh, vl);
-                const int off = kmaj(tid, 8 * q, 64);
+                split8(d + 8 * q, vh, vl);
+                const int off = kmaj(L, 32 * wg + 8 * q, 64);
                 *reinterpret_cast<uint4*>(img + off * 2) = vh;
                 *reinterpret_cast<uint4*>(img + kAmBytes / 2 + off * 2) = vl;
             }
