@@ -69,6 +69,8 @@ def lib():
             L.gdn_scan_workspace_bytes.argtypes = [D, _i32, _i32]
             L.gdn_scan.restype = ctypes.c_int
             L.gdn_scan.argtypes = [D, _i32, _i32] + [_p] * 10 + [_sz, _p]
+            L.gdn_scan_noalloc.restype = ctypes.c_int
+            L.gdn_scan_noalloc.argtypes = [D, _i32, _i32] + [_p] * 9 + [_p]
             L.gdn_post.restype = ctypes.c_int
             L.gdn_post.argtypes = [D, _i32, _p, _p, _p, _i32, _p, _p]
             L.gdn_layer_workspace_bytes.restype = _sz
@@ -153,6 +155,21 @@ def gdn_scan(d: gdn_dims, cu_seqlens, total_tokens, qn, kn, vc, glog, beta, S_in
                         _ptr(S_out, "S_out", f32, (n_seq, hv, dk, dv)), _ptr(o, "o", f32, (T, hv, dv)),
                         ws_ptr, ws_bytes, _stream(stream))
     _check("gdn_scan", st)
+
+
+def gdn_scan_noalloc(d: gdn_dims, cu_seqlens, total_tokens, qn, kn, vc, glog, beta, S_in, S_out, o, stream=None):
+    """gdn_scan with the library's own fixed scratch instead of a workspace, for
+    callers that cannot allocate device memory (see include/gdn.h)."""
+    n_seq, T = _batch(cu_seqlens, total_tokens)
+    hk, hv, dk, dv = d.hk, d.hv, d.dk, d.dv
+    f32 = torch.float32
+    st = lib().gdn_scan_noalloc(ctypes.byref(d), n_seq, T, _ptr(cu_seqlens, "cu_seqlens", torch.int32),
+                                _ptr(qn, "qn", f32, (T, hk, dk)), _ptr(kn, "kn", f32, (T, hk, dk)),
+                                _ptr(vc, "vc", f32, (T, hv, dv)), _ptr(glog, "glog", f32, (T, hv)),
+                                _ptr(beta, "beta", f32, (T, hv)), _ptr(S_in, "S_in", f32, (n_seq, hv, dk, dv)),
+                                _ptr(S_out, "S_out", f32, (n_seq, hv, dk, dv)), _ptr(o, "o", f32, (T, hv, dv)),
+                                _stream(stream))
+    _check("gdn_scan_noalloc", st)
 
 
 def gdn_post(d: gdn_dims, total_tokens, o, z, gamma, out_f32: bool, y, stream=None):

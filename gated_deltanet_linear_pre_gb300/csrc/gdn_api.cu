@@ -100,6 +100,10 @@ int channels(const gdn_dims* d) { return 2 * d->hk * d->dk + d->hv * d->dv; }
 
 }  // namespace
 
+namespace gdn {
+void set_last_error(const char* msg) { g_last_error = msg; }
+}  // namespace gdn
+
 extern "C" {
 
 const char* gdn_status_string(gdn_status s)

@@ -60,6 +60,9 @@ size_t scan_workspace_bytes(int hk, int hv, int n_seq, int T);
 cudaError_t launch_scan(const ScanParams& p, cudaStream_t stream);
 cudaError_t launch_post(const PostParams& p, cudaStream_t stream);
 
+// record the detail string returned by gdn_last_error_string on this thread
+void set_last_error(const char* msg);
+
 // ---- small device helpers ---------------------------------------------------
 __device__ __forceinline__ float warp_sum(float v)
 {

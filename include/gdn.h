@@ -160,6 +160,37 @@ GDN_API gdn_status gdn_post(const gdn_dims* dims, int32_t total_tokens, const fl
                     const uint16_t* z, const float* gamma, int32_t out_f32, void* y,
                     struct CUstream_st* stream);
 
+/*
+ * gdn_scan_noalloc -- gdn_scan for callers that cannot allocate device
+ * memory.  The paper has no counterpart to this entry point.
+ *
+ * Some callers have no device allocator to hand to the library: a host
+ * program that links this C ABI directly and has no workspace buffer to
+ * give, or a service that forbids device allocations after start-up.  For
+ * them this entry point runs the same scan with its scratch in a
+ * fixed-size array that the library owns (GDN_SCAN_NOALLOC_MAX_BYTES, held
+ * on every device that loads the library until the process exits).  The
+ * caller still passes every input and output, exactly as for gdn_scan.
+ *
+ * - Allocates nothing: no cudaMalloc, cudaFree or allocating library call.
+ * - The first call on each device looks up that device's copy of the array
+ *   (with the device current) and caches it; make that first call before
+ *   any stream capture.
+ * - Batches whose scan scratch (gdn_scan_workspace_bytes) exceeds
+ *   GDN_SCAN_NOALLOC_MAX_BYTES are rejected with GDN_ERR_UNSUPPORTED and a
+ *   message naming the limit; nothing is enqueued.
+ * - All calls on a device share the one array and it keeps the last call's
+ *   contents (the part that must start at zero is cleared by every call):
+ *   calls whose work overlaps on the GPU -- different streams, or several
+ *   host threads -- race on it.  Serialise them, e.g. on one stream.
+ */
+#define GDN_SCAN_NOALLOC_MAX_BYTES ((size_t)64 << 20)
+GDN_API gdn_status gdn_scan_noalloc(const gdn_dims* dims, int32_t n_seq, int32_t total_tokens,
+                                    const int32_t* cu_seqlens, const float* qn, const float* kn,
+                                    const float* vc, const float* glog, const float* beta,
+                                    const float* S_in, float* S_out, float* o,
+                                    struct CUstream_st* stream);
+
 /* Workspace bytes gdn_layer needs: the stage tensors qn, kn, vc, glog, beta,
  * o plus the scan's own workspace, each 256-byte aligned. */
 GDN_API size_t gdn_layer_workspace_bytes(const gdn_dims* dims, int32_t n_seq, int32_t total_tokens);
