@@ -82,4 +82,8 @@ __device__ __forceinline__ float sigmoidf_(float x) { return 1.0f / (1.0f + expf
 
 __device__ __forceinline__ float siluf_(float x) { return x / (1.0f + expf(-x)); }
 
+// SiLU with the fast exponential and reciprocal intrinsics (a few ulp; for
+// x -> -inf the reciprocal of inf is 0, so the result goes to -0 cleanly)
+__device__ __forceinline__ float silu_fast(float x) { return x * __fdividef(1.0f, 1.0f + __expf(-x)); }
+
 }  // namespace gdn

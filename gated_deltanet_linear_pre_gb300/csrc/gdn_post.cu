@@ -49,12 +49,12 @@ __global__ void __launch_bounds__(kThreads) post_kernel(PostParams p, long long 
             const float2 z01 = __half22float2(*reinterpret_cast<__half2*>(&zv[i].x));
             const float2 z23 = __half22float2(*reinterpret_cast<__half2*>(&zv[i].y));
             // gate and gamma first, then the reduction
-            const float g0 = gm.x * siluf_(z01.x), g1 = gm.y * siluf_(z01.y);
-            const float g2 = gm.z * siluf_(z23.x), g3 = gm.w * siluf_(z23.y);
+            const float g0 = gm.x * silu_fast(z01.x), g1 = gm.y * silu_fast(z01.y);
+            const float g2 = gm.z * silu_fast(z23.x), g3 = gm.w * silu_fast(z23.y);
             const float4 o = ov[i];
             float ss = o.x * o.x + o.y * o.y + o.z * o.z + o.w * o.w;
             ss = warp_sum(ss);
-            const float inv = 1.0f / sqrtf(ss * inv_dv + p.eps);
+            const float inv = rsqrtf(ss * inv_dv + p.eps);
             const float y0 = o.x * inv * g0, y1 = o.y * inv * g1;
             const float y2 = o.z * inv * g2, y3 = o.w * inv * g3;
             if (r < n_rows) {

@@ -152,10 +152,10 @@ pre_kernel(PreParams p, int n_slots, int head_groups, int n_conv_blocks)
             win2 = tap4(p, seq, seq_start, -1, c);
         }
         const F4 x = unpack_half4(cur[i]);
-        float y0 = siluf_(conv4(w0.x, w0.y, w0.z, w0.w, win0.x, win1.x, win2.x, x.x));
-        float y1 = siluf_(conv4(w1.x, w1.y, w1.z, w1.w, win0.y, win1.y, win2.y, x.y));
-        float y2 = siluf_(conv4(w2.x, w2.y, w2.z, w2.w, win0.z, win1.z, win2.z, x.z));
-        float y3 = siluf_(conv4(w3.x, w3.y, w3.z, w3.w, win0.w, win1.w, win2.w, x.w));
+        float y0 = silu_fast(conv4(w0.x, w0.y, w0.z, w0.w, win0.x, win1.x, win2.x, x.x));
+        float y1 = silu_fast(conv4(w1.x, w1.y, w1.z, w1.w, win0.y, win1.y, win2.y, x.y));
+        float y2 = silu_fast(conv4(w2.x, w2.y, w2.z, w2.w, win0.z, win1.z, win2.z, x.z));
+        float y3 = silu_fast(conv4(w3.x, w3.y, w3.z, w3.w, win0.w, win1.w, win2.w, x.w));
         win0 = win1;
         win1 = win2;
         win2 = x;
@@ -165,7 +165,7 @@ pre_kernel(PreParams p, int n_slots, int head_groups, int n_conv_blocks)
         } else {
             float ss = y0 * y0 + y1 * y1 + y2 * y2 + y3 * y3;
             ss = warp_sum(ss);
-            const float inv = 1.0f / sqrtf(ss + p.eps);
+            const float inv = rsqrtf(ss + p.eps);
             y0 *= inv; y1 *= inv; y2 *= inv; y3 *= inv;
             const int j = is_q ? slot : slot - hk;
             dst = (is_k ? p.kn : p.qn) + ((size_t)t * hk + j) * kHeadDim + lane * 4;
