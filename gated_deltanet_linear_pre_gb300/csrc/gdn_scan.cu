@@ -461,7 +461,8 @@ done:
 // =======================================================================================
 // chain: one CTA per (sequence, value head, kDVS-column slice)
 // =======================================================================================
-constexpr int kChainThreads = 256;  // two warpgroups: each covers all 128 TMEM lanes, half the columns
+constexpr int kChainWG = 4;                   // warpgroups; each covers all 128 TMEM lanes
+constexpr int kChainThreads = 128 * kChainWG;  // and kDVS / kChainWG of the columns
 
 template <int DVS>
 struct __align__(1024) ChainSmem {
@@ -469,7 +470,7 @@ struct __align__(1024) ChainSmem {
     uint16_t am[2][128 * 64];       // [T; P T] image
     uint16_t bs[2][128 * DVS];      // S slice (MN-major B, dk x DVS)
     uint16_t bx[2][64 * DVS];       // X, then e^{G_L-G} U (MN-major B, 64 x DVS)
-    float v[64 * (DVS + 4)];        // V tile of the slice, rows padded by 16 bytes (bank spread)
+    float v[64 * (DVS + 4)];        // V tile of the slice (rows padded by 16 bytes), later the O tile
     float eG[64], beta[64], kdec[64];
     float gL;
     uint32_t tmem_base;
@@ -477,21 +478,32 @@ struct __align__(1024) ChainSmem {
     uint64_t mbar_mma, mbar_kq[2], mbar_am;
 };
 
+template <int COLS>
+__device__ __forceinline__ void tmem_ld_cols(uint32_t taddr, float (&d)[COLS])
+{
+    static_assert(COLS == 16 || COLS == 32, "column count");
+    if constexpr (COLS == 16) umma::tmem_ld16(taddr, d);
+    else umma::tmem_ld32(taddr, d);
+}
+
 template <int DVS>
 __global__ void __launch_bounds__(kChainThreads, 1) scan_chain_kernel(ScanParams p)
 {
     extern __shared__ __align__(1024) unsigned char smem_raw[];
     ChainSmem<DVS>& sm = *reinterpret_cast<ChainSmem<DVS>*>(smem_raw);
     constexpr int SLICES = kHeadDim / DVS;
-    constexpr int HALF = DVS / 2;  // columns per warpgroup
+    constexpr int COLS = DVS / kChainWG;  // columns per thread
     constexpr uint32_t kTmemCols = 512;
     // each product takes 2*DVS columns: [hi*hi + lo*hi | hi*lo]
     constexpr uint32_t cD2 = 0, cD3 = 2 * DVS, cD4 = 4 * DVS;
     static_assert(6 * DVS <= (int)kTmemCols, "TMEM columns");
+    constexpr int kGateWarp = 3;   // computes the gates while thread 0 issues MMAs
+    constexpr int kCopyThread = 64;  // issues the bulk copies
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int L = tid & 127;            // TMEM lane of this thread
-    const int wg = tid >> 7;            // column half
+    const int wg = tid >> 7;            // column group
+    const int cb = wg * COLS;           // first column of this thread within the slice
     const int h = blockIdx.x / SLICES, slice = blockIdx.x % SLICES, s = blockIdx.y;
     const int j = h / (p.hv / p.hk);
     const int v0 = slice * DVS;
@@ -511,18 +523,18 @@ __global__ void __launch_bounds__(kChainThreads, 1) scan_chain_kernel(ScanParams
         sm.abort_flag = 0;
     }
 
-    // state slice: thread (L, wg) holds row L (key index), columns v0 + wg*HALF + [0, HALF)
-    float S[HALF];
+    // state slice: thread (L, wg) holds row L (key index), columns v0 + cb + [0, COLS)
+    float S[COLS];
     {
-        const float* src = p.S_in + sbase + (size_t)L * kHeadDim + v0 + wg * HALF;
+        const float* src = p.S_in + sbase + (size_t)L * kHeadDim + v0 + cb;
 #pragma unroll
-        for (int c = 0; c < HALF; c += 4) {
+        for (int c = 0; c < COLS; c += 4) {
             const float4 x = *reinterpret_cast<const float4*>(src + c);
             S[c] = x.x; S[c + 1] = x.y; S[c + 2] = x.z; S[c + 3] = x.w;
         }
 #pragma unroll
-        for (int c = 0; c < HALF; c += 8)
-            store_split8(&sm.bs[0][mnmaj(wg * HALF + c, L, 128)], &sm.bs[1][mnmaj(wg * HALF + c, L, 128)], S + c);
+        for (int c = 0; c < COLS; c += 8)
+            store_split8(&sm.bs[0][mnmaj(cb + c, L, 128)], &sm.bs[1][mnmaj(cb + c, L, 128)], S + c);
     }
     umma::fence_proxy_async();
     umma::fence_before_sync();
@@ -531,34 +543,30 @@ __global__ void __launch_bounds__(kChainThreads, 1) scan_chain_kernel(ScanParams
 
     const uint32_t tmem = sm.tmem_base;
     const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
-    const uint32_t b_s[2] = {umma::smem_u32(sm.bs[0]), umma::smem_u32(sm.bs[1])};
-    const uint32_t b_x[2] = {umma::smem_u32(sm.bx[0]), umma::smem_u32(sm.bx[1])};
+    const uint32_t b_s = umma::smem_u32(sm.bs[0]);
+    const uint32_t b_x = umma::smem_u32(sm.bx[0]);
     const uint32_t a_m[2] = {umma::smem_u32(sm.am[0]), umma::smem_u32(sm.am[1])};
     uint32_t ph_mma = 0;
     // outstanding bulk copies (uniform across threads): issued but not yet waited
     bool pend_kq[2] = {false, false}, pend_am = false;
 
-    // ---- bulk-copy issue helpers (thread 0) -----------------------------------------------
+    // ---- bulk-copy issue helpers -----------------------------------------------------------
     auto issue_kq = [&](int c) {  // [K; Q] image of chunk c into buffer c & 1
-        if (tid == 0) {
+        if (tid == kCopyThread) {
             uint64_t* mb = &sm.mbar_kq[c & 1];
             umma::mbar_arrive_expect_tx(mb, (uint32_t)kKqBytes);
-            const unsigned char* src = kq_image(p, base + c, j);
-            unsigned char* dst = reinterpret_cast<unsigned char*>(sm.akq[c & 1]);
-            umma::bulk_g2s(dst, src, (uint32_t)kKqBytes, mb);
+            umma::bulk_g2s(sm.akq[c & 1], kq_image(p, base + c, j), (uint32_t)kKqBytes, mb);
         }
         pend_kq[c & 1] = true;
     };
     auto issue_am = [&](int c) {
-        if (tid == 0) {
+        if (tid == kCopyThread) {
             umma::mbar_arrive_expect_tx(&sm.mbar_am, (uint32_t)kAmBytes);
-            const unsigned char* src = am_image(p, base + c, h);
-            unsigned char* dst = reinterpret_cast<unsigned char*>(sm.am);
-            umma::bulk_g2s(dst, src, (uint32_t)kAmBytes, &sm.mbar_am);
+            umma::bulk_g2s(sm.am, am_image(p, base + c, h), (uint32_t)kAmBytes, &sm.mbar_am);
         }
         pend_am = true;
     };
-    // V tile of a chunk: every thread loads 4 float4 into registers one chunk ahead
+    // V tile of a chunk: every thread loads its float4s into registers one chunk ahead
     constexpr int kVq = 64 * DVS / 4 / kChainThreads;
     float4 vpre[kVq];
     auto load_v = [&](int c) {
@@ -577,13 +585,13 @@ __global__ void __launch_bounds__(kChainThreads, 1) scan_chain_kernel(ScanParams
             *reinterpret_cast<float4*>(&sm.v[t * (DVS + 4) + c4]) = vpre[q];
         }
     };
-    // gates of one chunk, raw values prefetched into warp-0 registers one chunk ahead
+    // gates of one chunk, raw values prefetched into the gate warp's registers one chunk ahead
     float lam_nx[2] = {0.f, 0.f}, bet_nx[2] = {0.f, 0.f};
     int n_nx = 0;
     auto load_gates = [&](int c) {
         const int cc0 = t0 + c * kChunk, nn = min(kChunk, t1 - cc0);
         n_nx = nn;
-        if (warp == 0) {
+        if (warp == kGateWarp) {
 #pragma unroll
             for (int q = 0; q < 2; ++q) {
                 const int t = lane + 32 * q;
@@ -633,11 +641,11 @@ __global__ void __launch_bounds__(kChainThreads, 1) scan_chain_kernel(ScanParams
         GDN_SYNC_OR_ABORT();
         const uint32_t a_kq_hi = umma::smem_u32(sm.akq[c & 1][0]), a_kq_lo = umma::smem_u32(sm.akq[c & 1][1]);
         if (tid == 0) {
-            mma_split2(tmem + cD2, a_kq_hi, a_kq_lo, 128, 2048, 256, b_s[0], 2048, 256, 8, DVS, false, true);
+            mma_split2(tmem + cD2, a_kq_hi, a_kq_lo, 128, 2048, 256, b_s, 2048, 256, 8, DVS, false, true);
             umma::commit(&sm.mbar_mma);
         }
         // ---- meanwhile: gates e^G, beta, e^{G_L - G}, e^{G_L}; next chunk's gates and V ---------
-        if (warp == 0) {
+        if (warp == kGateWarp) {
             float lam[2];
 #pragma unroll
             for (int q = 0; q < 2; ++q) lam[q] = (lane + 32 * q) < n_nx ? fmaxf(lam_nx[q], kLamFloor) : 0.0f;
@@ -651,6 +659,8 @@ __global__ void __launch_bounds__(kChainThreads, 1) scan_chain_kernel(ScanParams
             sm.beta[lane] = b0;
             sm.beta[lane + 32] = b1;
             if (lane == 0) sm.gL = __expf(GL);
+        } else if (more) {
+            n_nx = min(kChunk, t1 - (c0 + kChunk));
         }
         if (more) load_v(c + 1);
         GDN_WAIT(&sm.mbar_mma, ph_mma);
@@ -658,31 +668,31 @@ __global__ void __launch_bounds__(kChainThreads, 1) scan_chain_kernel(ScanParams
         GDN_SYNC_OR_ABORT();
 
         // ---- X = beta (V - e^G K S0) -> bx;  keep e^G Q S0 / sqrt(dk) --------------------------------
-        float qs[HALF];
+        float qs[COLS];
         {
             const int t = L & 63;
-            float d[HALF], d2[HALF];
-            umma::tmem_ld32(tmem + lane_off + cD2 + wg * HALF, d);
-            umma::tmem_ld32(tmem + lane_off + cD2 + DVS + wg * HALF, d2);
+            float d[COLS], d2[COLS];
+            tmem_ld_cols<COLS>(tmem + lane_off + cD2 + cb, d);
+            tmem_ld_cols<COLS>(tmem + lane_off + cD2 + DVS + cb, d2);
             umma::tmem_wait_ld();
 #pragma unroll
-            for (int e = 0; e < HALF; ++e) d[e] += d2[e];
+            for (int e = 0; e < COLS; ++e) d[e] += d2[e];
             if (L < 64) {
                 const float bt = sm.beta[t], eg = sm.eG[t];
-                const float4* vr = reinterpret_cast<const float4*>(&sm.v[t * (DVS + 4) + wg * HALF]);
+                const float4* vr = reinterpret_cast<const float4*>(&sm.v[t * (DVS + 4) + cb]);
 #pragma unroll
-                for (int cc = 0; cc < HALF; cc += 8) {
+                for (int cc = 0; cc < COLS; cc += 8) {
                     const float4 va = vr[cc / 4], vb = vr[cc / 4 + 1];
                     const float vv[8] = {va.x, va.y, va.z, va.w, vb.x, vb.y, vb.z, vb.w};
                     float x[8];
 #pragma unroll
                     for (int e = 0; e < 8; ++e) x[e] = bt * (vv[e] - eg * d[cc + e]);
-                    store_split8(&sm.bx[0][mnmaj(wg * HALF + cc, t, 64)], &sm.bx[1][mnmaj(wg * HALF + cc, t, 64)], x);
+                    store_split8(&sm.bx[0][mnmaj(cb + cc, t, 64)], &sm.bx[1][mnmaj(cb + cc, t, 64)], x);
                 }
             } else {
                 const float f = sm.eG[t] * qscale;
 #pragma unroll
-                for (int e = 0; e < HALF; ++e) qs[e] = f * d[e];
+                for (int e = 0; e < COLS; ++e) qs[e] = f * d[e];
             }
         }
         GDN_PUBLISH();
@@ -692,7 +702,7 @@ __global__ void __launch_bounds__(kChainThreads, 1) scan_chain_kernel(ScanParams
         pend_am = false;
         GDN_SYNC_OR_ABORT();
         if (tid == 0) {
-            mma_split2(tmem + cD3, a_m[0], a_m[1], 128, 1024, 256, b_x[0], 1024, 256, 4, DVS, false, true);
+            mma_split2(tmem + cD3, a_m[0], a_m[1], 128, 1024, 256, b_x, 1024, 256, 4, DVS, false, true);
             umma::commit(&sm.mbar_mma);
         }
         GDN_WAIT(&sm.mbar_mma, ph_mma);
@@ -700,26 +710,26 @@ __global__ void __launch_bounds__(kChainThreads, 1) scan_chain_kernel(ScanParams
         GDN_SYNC_OR_ABORT();
         if (more) issue_am(c + 1);  // [T; P T] image consumed
 
-        // ---- e^{G_L-G} U -> bx;  O = e^G Q S0 / sqrt(dk) + P U -> o ------------------------------------
+        // ---- e^{G_L-G} U -> bx;  O = e^G Q S0 / sqrt(dk) + P U -> the V tile ----------------------------
         {
             const int t = L & 63;
-            float d[HALF], d2[HALF];
-            umma::tmem_ld32(tmem + lane_off + cD3 + wg * HALF, d);
-            umma::tmem_ld32(tmem + lane_off + cD3 + DVS + wg * HALF, d2);
+            float d[COLS], d2[COLS];
+            tmem_ld_cols<COLS>(tmem + lane_off + cD3 + cb, d);
+            tmem_ld_cols<COLS>(tmem + lane_off + cD3 + DVS + cb, d2);
             umma::tmem_wait_ld();
 #pragma unroll
-            for (int e = 0; e < HALF; ++e) d[e] += d2[e];
+            for (int e = 0; e < COLS; ++e) d[e] += d2[e];
             if (L < 64) {
                 const float kd = sm.kdec[t];
 #pragma unroll
-                for (int e = 0; e < HALF; ++e) d[e] *= kd;
+                for (int e = 0; e < COLS; ++e) d[e] *= kd;
 #pragma unroll
-                for (int cc = 0; cc < HALF; cc += 8)
-                    store_split8(&sm.bx[0][mnmaj(wg * HALF + cc, t, 64)], &sm.bx[1][mnmaj(wg * HALF + cc, t, 64)], d + cc);
+                for (int cc = 0; cc < COLS; cc += 8)
+                    store_split8(&sm.bx[0][mnmaj(cb + cc, t, 64)], &sm.bx[1][mnmaj(cb + cc, t, 64)], d + cc);
             } else {  // O row t -> the (consumed) V tile, written out coalesced below
-                float* dst = &sm.v[t * (DVS + 4) + wg * HALF];
+                float* dst = &sm.v[t * (DVS + 4) + cb];
 #pragma unroll
-                for (int e = 0; e < HALF; e += 4)
+                for (int e = 0; e < COLS; e += 4)
                     *reinterpret_cast<float4*>(dst + e) =
                         make_float4(qs[e] + d[e], qs[e + 1] + d[e + 1], qs[e + 2] + d[e + 2], qs[e + 3] + d[e + 3]);
             }
@@ -728,10 +738,10 @@ __global__ void __launch_bounds__(kChainThreads, 1) scan_chain_kernel(ScanParams
 
         // ---- dS = K^T (e^{G_L-G} U): K^T is the K half of the [K; Q] image, MN-major ------------------
         if (tid == 0) {
-            mma_split2(tmem + cD4, a_kq_hi, a_kq_lo, 2048, 128, 4096, b_x[0], 1024, 256, 4, DVS, true, true);
+            mma_split2(tmem + cD4, a_kq_hi, a_kq_lo, 2048, 128, 4096, b_x, 1024, 256, 4, DVS, true, true);
             umma::commit(&sm.mbar_mma);
         }
-        // O tile -> global while the state update runs: 16 lanes per 256-byte row
+        // O tile -> global while the state update runs: DVS/4 threads per row
 #pragma unroll
         for (int q = 0; q < kVq; ++q) {
             const int u = tid + kChainThreads * q, t = u / (DVS / 4), c4 = (u % (DVS / 4)) * 4;
@@ -747,31 +757,29 @@ __global__ void __launch_bounds__(kChainThreads, 1) scan_chain_kernel(ScanParams
         // ---- S = e^{G_L} S + dS -> registers and bs ----------------------------------------------------
         {
             const float gl = sm.gL;
-            float d[HALF], d2[HALF];
-            umma::tmem_ld32(tmem + lane_off + cD4 + wg * HALF, d);
-            umma::tmem_ld32(tmem + lane_off + cD4 + DVS + wg * HALF, d2);
+            float d[COLS], d2[COLS];
+            tmem_ld_cols<COLS>(tmem + lane_off + cD4 + cb, d);
+            tmem_ld_cols<COLS>(tmem + lane_off + cD4 + DVS + cb, d2);
             umma::tmem_wait_ld();
 #pragma unroll
-            for (int e = 0; e < HALF; ++e) d[e] += d2[e];
+            for (int e = 0; e < COLS; ++e) S[e] = fmaf(gl, S[e], d[e] + d2[e]);
 #pragma unroll
-            for (int e = 0; e < HALF; ++e) S[e] = fmaf(gl, S[e], d[e]);
-#pragma unroll
-            for (int cc = 0; cc < HALF; cc += 8)
-                store_split8(&sm.bs[0][mnmaj(wg * HALF + cc, L, 128)], &sm.bs[1][mnmaj(wg * HALF + cc, L, 128)], S + cc);
+            for (int cc = 0; cc < COLS; cc += 8)
+                store_split8(&sm.bs[0][mnmaj(cb + cc, L, 128)], &sm.bs[1][mnmaj(cb + cc, L, 128)], S + cc);
         }
         GDN_PUBLISH();
     }
 
     {
-        float* dst = p.S_out + sbase + (size_t)L * kHeadDim + v0 + wg * HALF;
+        float* dst = p.S_out + sbase + (size_t)L * kHeadDim + v0 + cb;
 #pragma unroll
-        for (int c = 0; c < HALF; c += 4)
+        for (int c = 0; c < COLS; c += 4)
             *reinterpret_cast<float4*>(dst + c) = make_float4(S[c], S[c + 1], S[c + 2], S[c + 3]);
     }
 
 done:
     // drain any copy still in flight into this CTA's shared memory (bounded), free TMEM
-    if (tid == 0) {
+    if (tid == kCopyThread) {
         for (int b = 0; b < 2; ++b)
             if (pend_kq[b]) umma::mbar_wait(&sm.mbar_kq[b], 0, 1u << 16), umma::mbar_wait(&sm.mbar_kq[b], 1, 1u << 16);
         if (pend_am) umma::mbar_wait(&sm.mbar_am, 0, 1u << 16), umma::mbar_wait(&sm.mbar_am, 1, 1u << 16);
