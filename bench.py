@@ -333,6 +333,9 @@ def main():
     value = world * T * args.steps / (total_ms / 1e3)
 
     # ---- end to end through gdn_layer with pinned host buffers -------------------------
+    # Three streams: host->device copies of layer l+1 and device->host copies of
+    # layer l-1 overlap the compute of layer l.  Per-layer events keep every
+    # buffer's writer behind its previous reader across steps.
     e2e = None
     if not args.no_e2e:
         y_host = [torch.empty((T, HV, DV), dtype=torch.float16).pin_memory() for _ in range(LAYERS)]
@@ -341,17 +344,34 @@ def main():
         acts = ("qkv", "a", "b", "z", "hist", "S0")
         h2d = sum(host[l][k].numel() * host[l][k].element_size() for l in range(LAYERS) for k in acts)
         d2h = sum(t.numel() * t.element_size() for ts in (y_host, S_host, hist_host) for t in ts)
+        s_in, s_out = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+        ev_in = [torch.cuda.Event() for _ in range(LAYERS)]
+        ev_comp = [torch.cuda.Event() for _ in range(LAYERS)]
+        ev_out = [torch.cuda.Event() for _ in range(LAYERS)]
+        for l in range(LAYERS):  # a recorded starting point for every event
+            ev_comp[l].record(stream)
+            ev_out[l].record(stream)
 
         def e2e_step():
             for l in range(LAYERS):
                 x = devl[l]
-                for k in acts:
-                    x[k].copy_(host[l][k], non_blocking=True)
+                with torch.cuda.stream(s_in):
+                    s_in.wait_event(ev_comp[l])  # the previous step's compute has read these inputs
+                    for k in acts:
+                        x[k].copy_(host[l][k], non_blocking=True)
+                    ev_in[l].record(s_in)
+                stream.wait_event(ev_in[l])
+                stream.wait_event(ev_out[l])  # the previous step's read-back of y/S/hist is done
                 gdn.gdn_layer(d, cu, T, x["qkv"], x["conv_w"], x["hist"], hist_out[l], x["a"], x["b"], x["z"],
-                              x["A_log"], x["dt_bias"], x["gamma"], x["S0"], S_out[l], False, y[l], layer_ws)
-                y_host[l].copy_(y[l], non_blocking=True)
-                S_host[l].copy_(S_out[l], non_blocking=True)
-                hist_host[l].copy_(hist_out[l], non_blocking=True)
+                              x["A_log"], x["dt_bias"], x["gamma"], x["S0"], S_out[l], False, y[l], layer_ws,
+                              stream=stream)
+                ev_comp[l].record(stream)
+                with torch.cuda.stream(s_out):
+                    s_out.wait_event(ev_comp[l])
+                    y_host[l].copy_(y[l], non_blocking=True)
+                    S_host[l].copy_(S_out[l], non_blocking=True)
+                    hist_host[l].copy_(hist_out[l], non_blocking=True)
+                    ev_out[l].record(s_out)
 
         for _ in range(max(1, args.warmup)):
             e2e_step()
@@ -359,8 +379,12 @@ def main():
         barrier(world)
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e0.record(stream)
+        s_in.wait_stream(stream)
+        s_out.wait_stream(stream)
         for _ in range(args.steps):
             e2e_step()
+        stream.wait_stream(s_in)
+        stream.wait_stream(s_out)
         e1.record(stream)
         torch.cuda.synchronize()
         e2e_ms = max_over_ranks(e0.elapsed_time(e1), world)
