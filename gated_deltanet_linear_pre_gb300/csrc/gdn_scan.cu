@@ -18,17 +18,18 @@
 // x = hi + lo (hi = bf16(x), lo = bf16(x - hi)) and three MMAs hi*hi + hi*lo
 // + lo*hi accumulated in fp32 in TMEM (about 16 significant bits per operand).
 // Products are stacked to fill the 128 rows of one MMA:
-//   [K; Q] K^T -> (K K^T ; Q K^T)          [I; P] T -> (T ; P T)
+//   [K; Q] K^T -> (K K^T ; Q K^T)          P T (rows 0-63 of an M=128 MMA)
 //   [K; Q] S0  -> (K S0 ; Q S0)            [T; P T] X -> (U ; P U)
 // so (Q S0) and (P U) land in the same TMEM lanes and O needs no exchange.
 //
-// Two kernels:
-//  * scan_prep_kernel, one CTA per (chunk, key head), fully parallel: the
-//    state-independent part.  It splits [K; Q] into the tensor-core layout
-//    and forms K K^T and Q K^T once; then, for each value head reading that
-//    key head, A and P, the inverse of I + A (blocked forward substitution on
-//    CUDA cores, 16x16 diagonal blocks) and [T; P T].  It writes two operand
-//    images to the workspace: [K; Q] per (chunk, key head) and [T; P T] per
+// Three kernels:
+//  * scan_gram_kernel, one CTA per (chunk, key head), fully parallel: splits
+//    [K; Q] into the tensor-core layout (the chain's [K; Q] image) and forms
+//    (K K^T ; Q K^T) in fp32.
+//  * scan_prep_kernel, one CTA per (chunk, key head), fully parallel: for each
+//    value head reading that key head, A and P, the inverse of I + A
+//    (recursive halving with 16x16 diagonal blocks by forward substitution,
+//    on CUDA cores) and P T on the tensor core; writes the [T; P T] image per
 //    (chunk, value head).
 //  * scan_chain_kernel, one CTA per (sequence, value head, 64-column slice):
 //    the state-dependent part, chunk after chunk, with the fp32 state slice
@@ -51,6 +52,7 @@ constexpr float kLamFloor = -110.0f;  // e^-110 is below the smallest fp32 denor
 constexpr uint32_t kErrTimeout = 1u;
 constexpr size_t kAmBytes = 128 * 64 * 2 * 2;     // [T; P T] image, bf16 hi + lo
 constexpr size_t kKqBytes = 128 * 128 * 2 * 2;    // [K; Q] image, bf16 hi + lo
+constexpr size_t kGramBytes = 128 * 64 * 4;       // (K K^T ; Q K^T), fp32 rows
 constexpr size_t kWsHeader = 4096;                // error words
 constexpr int kDVS = 64;                          // value columns per chain CTA
 
@@ -132,6 +134,27 @@ __device__ __forceinline__ unsigned char* kq_image(const ScanParams& p, size_t s
            (slot * p.hk + j) * kKqBytes;
 }
 
+__device__ __forceinline__ float* gram_rows(const ScanParams& p, size_t slot, int j)
+{
+    return reinterpret_cast<float*>(static_cast<unsigned char*>(p.workspace) + kWsHeader +
+                                    n_slots(p.T, p.n_seq) * ((size_t)p.hv * kAmBytes + (size_t)p.hk * kKqBytes) +
+                                    (slot * p.hk + j) * kGramBytes);
+}
+
+// slot -> (sequence, first token, token count); false for a slot no sequence uses
+__device__ __forceinline__ bool slot_chunk(const ScanParams& p, int slot, int& c0, int& n)
+{
+    int lo = 0, hi = p.n_seq - 1;
+    while (lo < hi) {  // last s with base(s) <= slot
+        const int mid = (lo + hi + 1) >> 1;
+        if (slot_base(p, mid) <= slot) lo = mid; else hi = mid - 1;
+    }
+    const int start = cu_at(p.cu_seqlens, lo, p.T), end = max(cu_at(p.cu_seqlens, lo + 1, p.T), start);
+    c0 = start + (slot - slot_base(p, lo)) * kChunk;
+    n = min(kChunk, end - c0);
+    return slot >= slot_base(p, lo) && c0 < end;
+}
+
 // running log-decay of one chunk from warp 0: lam[q] for tokens lane + 32 q in,
 // inclusive sums out; returns the chunk total
 __device__ __forceinline__ float warp_chunk_cumsum(float (&lam)[2], int lane)
@@ -148,24 +171,113 @@ __device__ __forceinline__ float warp_chunk_cumsum(float (&lam)[2], int lane)
 }
 
 // =======================================================================================
+// gram: one CTA per (chunk slot, key head): split [K; Q] (the chain's operand
+// image) and (K K^T ; Q K^T) in fp32 for the prep kernel
+// =======================================================================================
+constexpr int kGramThreads = 256;
+
+struct __align__(1024) GramSmem {
+    uint16_t akq[2][128 * 128];  // split [K; Q] (K-major)
+    uint32_t tmem_base;
+    int abort_flag;
+    uint64_t mbar;
+};
+
+__global__ void __launch_bounds__(kGramThreads) scan_gram_kernel(ScanParams p)
+{
+    extern __shared__ __align__(1024) unsigned char smem_raw[];
+    GramSmem& sm = *reinterpret_cast<GramSmem*>(smem_raw);
+    const int tid = threadIdx.x, warp = tid >> 5;
+    const int L = tid & 127, wg = tid >> 7;
+    const int slot = blockIdx.x, j = blockIdx.y;
+    uint32_t* err = reinterpret_cast<uint32_t*>(p.workspace);
+    int c0, n;
+    if (!slot_chunk(p, slot, c0, n)) return;  // unused slot (whole CTA)
+
+    if (warp == 0) umma::tmem_alloc(&sm.tmem_base, 64);
+    if (tid == 0) {
+        umma::mbar_init(&sm.mbar, 1);
+        sm.abort_flag = 0;
+    }
+    // Unit u = (matrix, token group, column group, row in group), row fastest so
+    // that 8 consecutive lanes fill one 128-byte core matrix; all loads in flight together.
+    {
+        constexpr int kU = 2 * 64 * 16 / kGramThreads;
+        float4 ld[2 * kU];
+#pragma unroll
+        for (int q = 0; q < kU; ++q) {
+            const int u = tid + kGramThreads * q;
+            const int mat = u >> 10, tg = (u >> 7) & 7, g = (u >> 3) & 15, t = tg * 8 + (u & 7);
+            if (t < n) {
+                const float4* src = reinterpret_cast<const float4*>(
+                    (mat ? p.qn : p.kn) + ((size_t)(c0 + t) * p.hk + j) * kHeadDim + g * 8);
+                ld[2 * q] = __ldg(src);
+                ld[2 * q + 1] = __ldg(src + 1);
+            } else {
+                ld[2 * q] = ld[2 * q + 1] = make_float4(0.f, 0.f, 0.f, 0.f);
+            }
+        }
+        unsigned char* img = kq_image(p, slot, j);
+#pragma unroll
+        for (int q = 0; q < kU; ++q) {
+            const int u = tid + kGramThreads * q;
+            const int mat = u >> 10, tg = (u >> 7) & 7, g = (u >> 3) & 15, t = tg * 8 + (u & 7);
+            const float x[8] = {ld[2 * q].x, ld[2 * q].y, ld[2 * q].z, ld[2 * q].w,
+                                ld[2 * q + 1].x, ld[2 * q + 1].y, ld[2 * q + 1].z, ld[2 * q + 1].w};
+            uint4 vh, vl;
+            split8(x, vh, vl);
+            const int off = kmaj(mat * 64 + t, g * 8, 128);
+            *reinterpret_cast<uint4*>(&sm.akq[0][off]) = vh;
+            *reinterpret_cast<uint4*>(&sm.akq[1][off]) = vl;
+            *reinterpret_cast<uint4*>(img + off * 2) = vh;
+            *reinterpret_cast<uint4*>(img + kKqBytes / 2 + off * 2) = vl;
+        }
+    }
+    umma::fence_proxy_async();
+    umma::fence_before_sync();
+    __syncthreads();
+    umma::fence_after_sync();
+    const uint32_t tmem = sm.tmem_base;
+    // (K K^T ; Q K^T) = [K; Q] K^T  (B = the K rows of the same tile)
+    if (tid == 0) {
+        const uint32_t a_hi = umma::smem_u32(sm.akq[0]), a_lo = umma::smem_u32(sm.akq[1]);
+        mma_split(tmem, a_hi, a_lo, 128, 2048, 256, a_hi, a_lo, 2048, 256, 8, umma::idesc_bf16(128, 64, false, false));
+        umma::commit(&sm.mbar);
+    }
+    if (!umma::mbar_wait(&sm.mbar, 0)) { sm.abort_flag = 1; atomicOr(err, kErrTimeout); }
+    __syncthreads();
+    if (!sm.abort_flag) {
+        umma::fence_after_sync();
+        float d[32];
+        umma::tmem_ld32(tmem + ((uint32_t)((warp & 3) * 32) << 16) + 32 * wg, d);
+        umma::tmem_wait_ld();
+        float4* dst = reinterpret_cast<float4*>(gram_rows(p, slot, j) + L * 64 + 32 * wg);
+#pragma unroll
+        for (int q = 0; q < 8; ++q) dst[q] = make_float4(d[4 * q], d[4 * q + 1], d[4 * q + 2], d[4 * q + 3]);
+    }
+    umma::fence_before_sync();
+    __syncthreads();
+    if (warp == 0) umma::tmem_dealloc(sm.tmem_base, 64);
+}
+
+// =======================================================================================
 // prep: one CTA per (chunk slot, key head); its value heads one after another
 // =======================================================================================
 constexpr int kPrepThreads = 256;  // two warpgroups: each covers all 128 TMEM lanes, half the columns
 
 struct __align__(1024) PrepSmem {
-    union {
-        uint16_t akq[2][128 * 128];                                   // split [K; Q] (K-major)
-        struct { float A[64 * 68]; float T[64 * 68]; uint16_t bt[2][64 * 64]; } s;  // solve (rows padded), T as MN-major B
-    } u;
-    uint16_t am[2][128 * 64];  // [I; P] (K-major)
-    float W[3 * 256];          // off-diagonal block sums of the solve
+    uint16_t ap[2][64 * 64];   // P (K-major, 64 rows); an M = 128 descriptor reads its rows 64-127 from
+    uint16_t bt[2][64 * 64];   //   the next 16 KB (here), whose products are never read
+    float A[64 * 68];          // fp32 A and T (rows padded to 68 floats)
+    float T[64 * 68];
+    float W[32 * 32];          // off-diagonal block products of the solve
     float G[64], beta[64];
     uint32_t tmem_base;
     int abort_flag;
     uint64_t mbar;
 };
 
-__global__ void __launch_bounds__(kPrepThreads) scan_prep_kernel(ScanParams p)
+__global__ void __launch_bounds__(kPrepThreads, 3) scan_prep_kernel(ScanParams p)
 {
     extern __shared__ __align__(1024) unsigned char smem_raw[];
     PrepSmem& sm = *reinterpret_cast<PrepSmem*>(smem_raw);
@@ -175,21 +287,11 @@ __global__ void __launch_bounds__(kPrepThreads) scan_prep_kernel(ScanParams p)
     const int group = p.hv / p.hk;
     uint32_t* err = reinterpret_cast<uint32_t*>(p.workspace);
     constexpr int ST = 68;  // fp32 row stride of A and T
-
-    // slot -> (sequence, chunk); last s with base(s) <= slot
-    int lo = 0, hi = p.n_seq - 1;
-    while (lo < hi) {
-        const int mid = (lo + hi + 1) >> 1;
-        if (slot_base(p, mid) <= slot) lo = mid; else hi = mid - 1;
-    }
-    const int s = lo;
-    const int start = cu_at(p.cu_seqlens, s, p.T), end = max(cu_at(p.cu_seqlens, s + 1, p.T), start);
-    const int c0 = start + (slot - slot_base(p, s)) * kChunk;
-    if (slot < slot_base(p, s) || c0 >= end) return;  // unused slot (whole CTA)
-    const int n = min(kChunk, end - c0);
+    int c0, n;
+    if (!slot_chunk(p, slot, c0, n)) return;  // unused slot (whole CTA)
     const float qscale = rsqrtf((float)kHeadDim);
 
-    if (warp == 0) umma::tmem_alloc(&sm.tmem_base, 128);
+    if (warp == 0) umma::tmem_alloc(&sm.tmem_base, 64);
     if (tid == 0) {
         umma::mbar_init(&sm.mbar, 1);
         sm.abort_flag = 0;
@@ -207,63 +309,26 @@ __global__ void __launch_bounds__(kPrepThreads) scan_prep_kernel(ScanParams p)
         }
     };
     load_gates(j * group);
-    // [K; Q] -> split tile and the chain's image.  Unit u = (matrix, token
-    // group, column group, row in group), row fastest so that 8 consecutive
-    // lanes fill one 128-byte core matrix; all loads in flight together.
+    // this thread's 32 entries of the gram rows: row L (K K^T for L < 64, Q K^T
+    // for L >= 64), columns [32 wg, 32 wg + 32); shared by all value heads
+    float d[32];
     {
-        constexpr int kU = 2 * 64 * 16 / kPrepThreads;
-        float4 ld[2 * kU];
+        const float4* src = reinterpret_cast<const float4*>(gram_rows(p, slot, j) + L * 64 + 32 * wg);
 #pragma unroll
-        for (int q = 0; q < kU; ++q) {
-            const int u = tid + kPrepThreads * q;
-            const int mat = u >> 10, tg = (u >> 7) & 7, g = (u >> 3) & 15, t = tg * 8 + (u & 7);
-            if (t < n) {
-                const float4* src = reinterpret_cast<const float4*>(
-                    (mat ? p.qn : p.kn) + ((size_t)(c0 + t) * p.hk + j) * kHeadDim + g * 8);
-                ld[2 * q] = __ldg(src);
-                ld[2 * q + 1] = __ldg(src + 1);
-            } else {
-                ld[2 * q] = ld[2 * q + 1] = make_float4(0.f, 0.f, 0.f, 0.f);
-            }
-        }
-        unsigned char* img = kq_image(p, slot, j);
-#pragma unroll
-        for (int q = 0; q < kU; ++q) {
-            const int u = tid + kPrepThreads * q;
-            const int mat = u >> 10, tg = (u >> 7) & 7, g = (u >> 3) & 15, t = tg * 8 + (u & 7);
-            const float x[8] = {ld[2 * q].x, ld[2 * q].y, ld[2 * q].z, ld[2 * q].w,
-                                ld[2 * q + 1].x, ld[2 * q + 1].y, ld[2 * q + 1].z, ld[2 * q + 1].w};
-            uint4 vh, vl;
-            split8(x, vh, vl);
-            const int off = kmaj(mat * 64 + t, g * 8, 128);
-            *reinterpret_cast<uint4*>(&sm.u.akq[0][off]) = vh;
-            *reinterpret_cast<uint4*>(&sm.u.akq[1][off]) = vl;
-            *reinterpret_cast<uint4*>(img + off * 2) = vh;
-            *reinterpret_cast<uint4*>(img + kKqBytes / 2 + off * 2) = vl;
+        for (int q = 0; q < 8; ++q) {
+            const float4 x = __ldg(src + q);
+            d[4 * q] = x.x; d[4 * q + 1] = x.y; d[4 * q + 2] = x.z; d[4 * q + 3] = x.w;
         }
     }
-    umma::fence_proxy_async();
-    umma::fence_before_sync();
     __syncthreads();
     umma::fence_after_sync();
     const uint32_t tmem = sm.tmem_base;
     const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
-    const uint32_t a_kq[2] = {umma::smem_u32(sm.u.akq[0]), umma::smem_u32(sm.u.akq[1])};
-    const uint32_t a_m[2] = {umma::smem_u32(sm.am[0]), umma::smem_u32(sm.am[1])};
-    const uint32_t b_t[2] = {umma::smem_u32(sm.u.s.bt[0]), umma::smem_u32(sm.u.s.bt[1])};
+    const uint32_t a_p[2] = {umma::smem_u32(sm.ap[0]), umma::smem_u32(sm.ap[1])};
+    const uint32_t b_t[2] = {umma::smem_u32(sm.bt[0]), umma::smem_u32(sm.bt[1])};
     uint32_t phase = 0;
-
-    // (K K^T ; Q K^T) = [K; Q] K^T  (B = the K rows of the same tile), shared by the group
-    if (tid == 0) {
-        mma_split(tmem, a_kq[0], a_kq[1], 128, 2048, 256, a_kq[0], a_kq[1], 2048, 256, 8,
-                  umma::idesc_bf16(128, 64, false, false));
-        umma::commit(&sm.mbar);
-    }
-    if (!umma::mbar_wait(&sm.mbar, phase)) { sm.abort_flag = 1; atomicOr(err, kErrTimeout); }
-    phase ^= 1u;
-    __syncthreads();
-    if (sm.abort_flag) goto done;
-    umma::fence_after_sync();
+    float* A = sm.A;
+    float* Tm = sm.T;
 
     for (int hh = 0; hh < group; ++hh) {
         const int h = j * group + hh;
@@ -282,14 +347,10 @@ __global__ void __launch_bounds__(kPrepThreads) scan_prep_kernel(ScanParams p)
         }
         __syncthreads();
 
-        // A (fp32, from the K K^T rows) and [I; P] (split; P from the Q K^T rows);
-        // thread (L, wg) does columns [32 wg, 32 wg + 32) of row L & 63
+        // A (fp32, rows L < 64) and P (split, rows L - 64 for L >= 64), columns of wg
         {
             const int i = L & 63, cb = 32 * wg;
             const float Gi = sm.G[i];
-            float d[32];
-            umma::tmem_ld32(tmem + lane_off + cb, d);
-            umma::tmem_wait_ld();
             const float4* G4 = reinterpret_cast<const float4*>(sm.G + cb);
             if (L < 64) {
                 const float bi = sm.beta[i];
@@ -303,14 +364,7 @@ __global__ void __launch_bounds__(kPrepThreads) scan_prep_kernel(ScanParams p)
                         const int jj = cb + 4 * q + e;
                         a[e] = jj < i ? bi * __expf(Gi - gg[e]) * d[4 * q + e] : 0.0f;
                     }
-                    *reinterpret_cast<float4*>(&sm.u.s.A[i * ST + cb + 4 * q]) = make_float4(a[0], a[1], a[2], a[3]);
-                }
-#pragma unroll
-                for (int c = 0; c < 32; c += 8) {
-                    float idr[8];
-#pragma unroll
-                    for (int e = 0; e < 8; ++e) idr[e] = (cb + c + e == i) ? 1.0f : 0.0f;
-                    store_split8(&sm.am[0][kmaj(i, cb + c, 64)], &sm.am[1][kmaj(i, cb + c, 64)], idr);
+                    *reinterpret_cast<float4*>(&A[i * ST + cb + 4 * q]) = make_float4(a[0], a[1], a[2], a[3]);
                 }
             } else {
 #pragma unroll
@@ -323,23 +377,19 @@ __global__ void __launch_bounds__(kPrepThreads) scan_prep_kernel(ScanParams p)
                         const int jj = cb + 8 * q + e;
                         pr[e] = jj <= i ? __expf(Gi - gg[e]) * d[8 * q + e] * qscale : 0.0f;
                     }
-                    store_split8(&sm.am[0][kmaj(64 + i, cb + 8 * q, 64)], &sm.am[1][kmaj(64 + i, cb + 8 * q, 64)], pr);
+                    store_split8(&sm.ap[0][kmaj(i, cb + 8 * q, 64)], &sm.ap[1][kmaj(i, cb + 8 * q, 64)], pr);
                 }
             }
         }
         __syncthreads();
 
-        // T = (I + A)^-1 (A strictly lower).  Only the block lower triangle of T
-        // is ever written or read.
-        // (1) 16x16 diagonal blocks: thread (b, c) forms column c of inv(I + A_bb)
-        //     by forward substitution, col[r] = [r == c] - sum_{m<r} A[r][m] col[m];
-        //     entries above c come out zero by themselves, so the loop has no
-        //     data-dependent branch and reads each A row as broadcast float4s.
-        // (2) off-diagonal blocks by distance: W = sum_m A_(bi,m) T_(m,bj), then
-        //     T_(bi,bj) = -T_(bi,bi) W, one 1 x 4 register tile per thread.
+        // T = (I + A)^-1 (A strictly lower), recursively by halves: T = [[T1, 0], [-T2 A21 T1, T2]].
+        // (1) the four 16x16 diagonal blocks by forward substitution (thread (b, c): column c;
+        //     col[r] = [r == c] - sum_{m<r} A[r][m] col[m], the entries above c come out zero);
+        // (2) the two 32x32 halves: T_(b,b-1) = -T_(b,b) A_(b,b-1) T_(b-1,b-1) for b = 1, 3;
+        // (3) the 32x32 off-diagonal block: T21 = -T2 (A21 T1).
+        // Only the block lower triangle of T is written; readers treat the rest as zero.
         {
-            float* A = sm.u.s.A;
-            float* Tm = sm.u.s.T;
             if (tid < 64) {
                 const int b = tid >> 4, c = tid & 15, o = 16 * b;
                 float col[16];
@@ -360,44 +410,55 @@ __global__ void __launch_bounds__(kPrepThreads) scan_prep_kernel(ScanParams p)
                 for (int r = 0; r < 16; ++r) Tm[(o + r) * ST + o + c] = col[r];
             }
             __syncthreads();
-            float* W = sm.W;  // [pair][16][16]
-            const int pr = tid >> 6, q = tid & 63, r = q >> 2, c4 = 4 * (q & 3);
-            for (int dist = 1; dist < 4; ++dist) {
-                const int bj = pr, bi = pr + dist;
-                const bool active = pr < 4 - dist;
-                if (active) {
-                    float acc[4] = {0.f, 0.f, 0.f, 0.f};
-                    for (int m4 = 16 * bj; m4 < 16 * bi; m4 += 4) {
-                        const float4 a4 = *reinterpret_cast<const float4*>(&A[(16 * bi + r) * ST + m4]);
-                        const float av[4] = {a4.x, a4.y, a4.z, a4.w};
+            {   // (2) pairs b = 1 (rows 16-31 x cols 0-15) and b = 3 (rows 48-63 x cols 32-47)
+                const int pr = tid >> 7, r = (tid >> 3) & 15, c2 = 2 * (tid & 7);
+                const int ro = 32 * pr + 16, co = 32 * pr;  // block (b, b-1) origin
+                float w0 = 0.f, w1 = 0.f;
 #pragma unroll
-                        for (int e = 0; e < 4; ++e) {
-                            const float4 t4 = *reinterpret_cast<const float4*>(&Tm[(m4 + e) * ST + 16 * bj + c4]);
-                            acc[0] = fmaf(av[e], t4.x, acc[0]); acc[1] = fmaf(av[e], t4.y, acc[1]);
-                            acc[2] = fmaf(av[e], t4.z, acc[2]); acc[3] = fmaf(av[e], t4.w, acc[3]);
-                        }
-                    }
-                    *reinterpret_cast<float4*>(&W[pr * 256 + r * 16 + c4]) = make_float4(acc[0], acc[1], acc[2], acc[3]);
+                for (int m = 0; m < 16; ++m) {
+                    const float a = A[(ro + r) * ST + co + m];
+                    const float2 t2 = *reinterpret_cast<const float2*>(&Tm[(co + m) * ST + co + c2]);
+                    w0 = fmaf(a, t2.x, w0);
+                    w1 = fmaf(a, t2.y, w1);
                 }
+                *reinterpret_cast<float2*>(&sm.W[pr * 256 + r * 16 + c2]) = make_float2(w0, w1);
                 __syncthreads();
-                if (active) {
-                    float acc[4] = {0.f, 0.f, 0.f, 0.f};
+                float t0 = 0.f, t1 = 0.f;
 #pragma unroll
-                    for (int m4 = 0; m4 < 16; m4 += 4) {
-                        const float4 a4 = *reinterpret_cast<const float4*>(&Tm[(16 * bi + r) * ST + 16 * bi + m4]);
-                        const float av[4] = {a4.x, a4.y, a4.z, a4.w};
-#pragma unroll
-                        for (int e = 0; e < 4; ++e) {
-                            const float4 w4 = *reinterpret_cast<const float4*>(&W[pr * 256 + (m4 + e) * 16 + c4]);
-                            acc[0] = fmaf(av[e], w4.x, acc[0]); acc[1] = fmaf(av[e], w4.y, acc[1]);
-                            acc[2] = fmaf(av[e], w4.z, acc[2]); acc[3] = fmaf(av[e], w4.w, acc[3]);
-                        }
-                    }
-                    *reinterpret_cast<float4*>(&Tm[(16 * bi + r) * ST + 16 * bj + c4]) =
-                        make_float4(-acc[0], -acc[1], -acc[2], -acc[3]);
+                for (int m = 0; m < 16; ++m) {
+                    const float a = Tm[(ro + r) * ST + ro + m];
+                    const float2 w2 = *reinterpret_cast<const float2*>(&sm.W[pr * 256 + m * 16 + c2]);
+                    t0 = fmaf(a, w2.x, t0);
+                    t1 = fmaf(a, w2.y, t1);
                 }
-                __syncthreads();
+                *reinterpret_cast<float2*>(&Tm[(ro + r) * ST + co + c2]) = make_float2(-t0, -t1);
             }
+            __syncthreads();
+            {   // (3) rows 32-63 x cols 0-31; T1 and T2 are block lower triangular
+                const int r = tid >> 3, c4 = 4 * (tid & 7);
+                float acc[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll 8
+                for (int m = 0; m < 32; ++m) {
+                    if ((m >> 4) < (c4 >> 4)) continue;  // T1[m][c] = 0 above the block diagonal
+                    const float a = A[(32 + r) * ST + m];
+                    const float4 t4 = *reinterpret_cast<const float4*>(&Tm[m * ST + c4]);
+                    acc[0] = fmaf(a, t4.x, acc[0]); acc[1] = fmaf(a, t4.y, acc[1]);
+                    acc[2] = fmaf(a, t4.z, acc[2]); acc[3] = fmaf(a, t4.w, acc[3]);
+                }
+                *reinterpret_cast<float4*>(&sm.W[r * 32 + c4]) = make_float4(acc[0], acc[1], acc[2], acc[3]);
+                __syncthreads();
+                float t[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll 8
+                for (int m = 0; m < 32; ++m) {
+                    if ((m >> 4) > (r >> 4)) continue;  // T2[r][m] = 0 above the block diagonal
+                    const float a = Tm[(32 + r) * ST + 32 + m];
+                    const float4 w4 = *reinterpret_cast<const float4*>(&sm.W[m * 32 + c4]);
+                    t[0] = fmaf(a, w4.x, t[0]); t[1] = fmaf(a, w4.y, t[1]);
+                    t[2] = fmaf(a, w4.z, t[2]); t[3] = fmaf(a, w4.w, t[3]);
+                }
+                *reinterpret_cast<float4*>(&Tm[(32 + r) * ST + c4]) = make_float4(-t[0], -t[1], -t[2], -t[3]);
+            }
+            __syncthreads();
             // T -> MN-major B tile (element (n = column, k = row)); row fastest across
             // lanes; column groups right of the row's diagonal block are zero
             for (int u = tid; u < 64 * 8; u += kPrepThreads) {
@@ -412,7 +473,7 @@ __global__ void __launch_bounds__(kPrepThreads) scan_prep_kernel(ScanParams p)
 #pragma unroll
                     for (int e = 0; e < 8; ++e) tr[e] = 0.0f;
                 }
-                store_split8(&sm.u.s.bt[0][mnmaj(g * 8, m, 64)], &sm.u.s.bt[1][mnmaj(g * 8, m, 64)], tr);
+                store_split8(&sm.bt[0][mnmaj(g * 8, m, 64)], &sm.bt[1][mnmaj(g * 8, m, 64)], tr);
             }
         }
         umma::fence_proxy_async();
@@ -420,9 +481,9 @@ __global__ void __launch_bounds__(kPrepThreads) scan_prep_kernel(ScanParams p)
         __syncthreads();
         umma::fence_after_sync();
 
-        // (T ; P T) = [I; P] T
+        // P T  (M = 128 descriptor over the 64-row P tile; rows 64-127 of the product unused)
         if (tid == 0) {
-            mma_split(tmem + 64, a_m[0], a_m[1], 128, 1024, 256, b_t[0], b_t[1], 1024, 256, 4,
+            mma_split(tmem, a_p[0], a_p[1], 128, 1024, 256, b_t[0], b_t[1], 1024, 256, 4,
                       umma::idesc_bf16(128, 64, false, true));
             umma::commit(&sm.mbar);
         }
@@ -432,17 +493,33 @@ __global__ void __launch_bounds__(kPrepThreads) scan_prep_kernel(ScanParams p)
         if (sm.abort_flag) goto done;
         umma::fence_after_sync();
 
-        // [T; P T] -> image (K-major, split): thread (L, wg) writes row L, columns of wg
+        // [T; P T] image (K-major, split): threads L >= 64 write row L - 64 (T, from shared
+        // memory), threads L < 64 write row 64 + L (P T, from TMEM lane L); columns of wg
         {
             unsigned char* img = am_image(p, slot, h);
-            float d[32];
-            umma::tmem_ld32(tmem + lane_off + 64 + 32 * wg, d);
-            umma::tmem_wait_ld();
+            const int cb = 32 * wg;
+            float x[32];
+            int row;
+            if (L < 64) {
+                umma::tmem_ld32(tmem + lane_off + cb, x);
+                umma::tmem_wait_ld();
+                row = 64 + L;
+            } else {
+                const int m = L - 64;
+#pragma unroll
+                for (int q = 0; q < 8; ++q) {
+                    const int g = (cb + 4 * q) >> 3;
+                    float4 t4 = make_float4(0.f, 0.f, 0.f, 0.f);
+                    if ((g >> 1) <= (m >> 4)) t4 = *reinterpret_cast<const float4*>(&Tm[m * ST + cb + 4 * q]);
+                    x[4 * q] = t4.x; x[4 * q + 1] = t4.y; x[4 * q + 2] = t4.z; x[4 * q + 3] = t4.w;
+                }
+                row = m;
+            }
 #pragma unroll
             for (int q = 0; q < 4; ++q) {
                 uint4 vh, vl;
-                split8(d + 8 * q, vh, vl);
-                const int off = kmaj(L, 32 * wg + 8 * q, 64);
+                split8(x + 8 * q, vh, vl);
+                const int off = kmaj(row, cb + 8 * q, 64);
                 *reinterpret_cast<uint4*>(img + off * 2) = vh;
                 *reinterpret_cast<uint4*>(img + kAmBytes / 2 + off * 2) = vl;
             }
@@ -455,7 +532,7 @@ __global__ void __launch_bounds__(kPrepThreads) scan_prep_kernel(ScanParams p)
 done:
     umma::fence_before_sync();
     __syncthreads();
-    if (warp == 0) umma::tmem_dealloc(sm.tmem_base, 128);
+    if (warp == 0) umma::tmem_dealloc(sm.tmem_base, 64);
 }
 
 // =======================================================================================
@@ -796,14 +873,16 @@ done:
 
 size_t scan_workspace_bytes(int hk, int hv, int n_seq, int T)
 {
-    return kWsHeader + n_slots(T, n_seq) * ((size_t)hv * kAmBytes + (size_t)hk * kKqBytes);
+    return kWsHeader + n_slots(T, n_seq) * ((size_t)hv * kAmBytes + (size_t)hk * (kKqBytes + kGramBytes));
 }
 
 cudaError_t launch_scan(const ScanParams& p, cudaStream_t stream)
 {
     if (p.n_seq == 0) return cudaSuccess;
-    const size_t prep_smem = sizeof(PrepSmem), chain_smem = sizeof(ChainSmem<kDVS>);
-    cudaError_t e = cudaFuncSetAttribute(scan_prep_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)prep_smem);
+    const size_t gram_smem = sizeof(GramSmem), prep_smem = sizeof(PrepSmem), chain_smem = sizeof(ChainSmem<kDVS>);
+    cudaError_t e = cudaFuncSetAttribute(scan_gram_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)gram_smem);
+    if (e != cudaSuccess) return e;
+    e = cudaFuncSetAttribute(scan_prep_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)prep_smem);
     if (e != cudaSuccess) return e;
     e = cudaFuncSetAttribute(scan_chain_kernel<kDVS>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)chain_smem);
     if (e != cudaSuccess) return e;
@@ -811,6 +890,9 @@ cudaError_t launch_scan(const ScanParams& p, cudaStream_t stream)
     if (e != cudaSuccess) return e;
     const size_t slots = n_slots(p.T, p.n_seq);
     if (p.T > 0) {
+        scan_gram_kernel<<<dim3((unsigned)slots, (unsigned)p.hk), kGramThreads, gram_smem, stream>>>(p);
+        e = cudaGetLastError();
+        if (e != cudaSuccess) return e;
         scan_prep_kernel<<<dim3((unsigned)slots, (unsigned)p.hk), kPrepThreads, prep_smem, stream>>>(p);
         e = cudaGetLastError();
         if (e != cudaSuccess) return e;
