@@ -53,8 +53,16 @@ constexpr uint32_t kErrTimeout = 1u;
 constexpr size_t kAmBytes = 128 * 64 * 2 * 2;     // [T; P T] image, bf16 hi + lo
 constexpr size_t kKqBytes = 128 * 128 * 2 * 2;    // [K; Q] image, bf16 hi + lo
 constexpr size_t kGramBytes = 128 * 64 * 4;       // (K K^T ; Q K^T), fp32 rows
+constexpr size_t kMBytes = 128 * 64 * 2 * 2;      // [K; Q] of a chunk times K^T of the previous one, bf16 hi + lo
+constexpr size_t kGateBytes = 1024;               // per-chunk gate row of a value head (784 bytes used)
+constexpr size_t kAmBlock = kAmBytes + kGateBytes; // [T; P T] image followed by the gate row
 constexpr size_t kWsHeader = 4096;                // error words
 constexpr int kDVS = 64;                          // value columns per chain CTA
+
+// [K; Q] image of a chunk (bytes): 16 groups of 8 rows, each group its hi plane
+// (2 KB, 16 core matrices along K) then its lo plane, so that any run of row
+// groups, e.g. one 64-row half, is one contiguous block
+__device__ __forceinline__ int kq_off(int r, int k) { return (r >> 3) * 4096 + (k >> 3) * 128 + (r & 7) * 16 + (k & 7) * 2; }
 
 // element offsets inside no-swizzle core-matrix tiles (bf16, 64 elements per core matrix)
 __device__ __forceinline__ int kmaj(int r, int k, int Kd) { return ((r >> 3) * (Kd >> 3) + (k >> 3)) * 64 + (r & 7) * 8 + (k & 7); }
@@ -106,13 +114,13 @@ __device__ __forceinline__ void mma_split(uint32_t d, uint32_t a_hi, uint32_t a_
 // both).  Two thirds of the instructions of mma_split for the same tensor work.
 __device__ __forceinline__ void mma_split2(uint32_t d, uint32_t a_hi, uint32_t a_lo, uint32_t a_lbo, uint32_t a_sbo,
                                            uint32_t a_kstep, uint32_t b_hilo, uint32_t b_sbo, uint32_t b_kstep,
-                                           int ksteps, int N, bool a_mn, bool b_mn)
+                                           int ksteps, int N, bool a_mn, bool b_mn, bool acc = false)
 {
     const uint64_t dah = umma::desc(a_hi, a_lbo, a_sbo), dal = umma::desc(a_lo, a_lbo, a_sbo);
     const uint64_t db = umma::desc(b_hilo, 128, b_sbo);
     const uint64_t sa = a_kstep >> 4, sb = b_kstep >> 4;
     const uint32_t wide = umma::idesc_bf16(128, 2 * N, a_mn, b_mn), narrow = umma::idesc_bf16(128, N, a_mn, b_mn);
-    for (int ks = 0; ks < ksteps; ++ks) umma::mma_bf16(d, dah + ks * sa, db + ks * sb, wide, ks != 0);
+    for (int ks = 0; ks < ksteps; ++ks) umma::mma_bf16(d, dah + ks * sa, db + ks * sb, wide, acc || ks != 0);
     for (int ks = 0; ks < ksteps; ++ks) umma::mma_bf16(d, dal + ks * sa, db + ks * sb, narrow, 1u);
 }
 
@@ -125,24 +133,47 @@ __host__ __device__ inline size_t n_slots(int T, int n_seq) { return (size_t)(T 
 
 __device__ __forceinline__ unsigned char* am_image(const ScanParams& p, size_t slot, int h)
 {
-    return static_cast<unsigned char*>(p.workspace) + kWsHeader + (slot * p.hv + h) * kAmBytes;
+    return static_cast<unsigned char*>(p.workspace) + kWsHeader + (slot * p.hv + h) * kAmBlock;
 }
 
 __device__ __forceinline__ unsigned char* kq_image(const ScanParams& p, size_t slot, int j)
 {
-    return static_cast<unsigned char*>(p.workspace) + kWsHeader + n_slots(p.T, p.n_seq) * p.hv * kAmBytes +
+    return static_cast<unsigned char*>(p.workspace) + kWsHeader + n_slots(p.T, p.n_seq) * p.hv * kAmBlock +
            (slot * p.hk + j) * kKqBytes;
 }
 
 __device__ __forceinline__ float* gram_rows(const ScanParams& p, size_t slot, int j)
 {
     return reinterpret_cast<float*>(static_cast<unsigned char*>(p.workspace) + kWsHeader +
-                                    n_slots(p.T, p.n_seq) * ((size_t)p.hv * kAmBytes + (size_t)p.hk * kKqBytes) +
+                                    n_slots(p.T, p.n_seq) * ((size_t)p.hv * kAmBlock + (size_t)p.hk * kKqBytes) +
                                     (slot * p.hk + j) * kGramBytes);
 }
 
+__device__ __forceinline__ unsigned char* m_image(const ScanParams& p, size_t slot, int j)
+{
+    return static_cast<unsigned char*>(p.workspace) + kWsHeader +
+           n_slots(p.T, p.n_seq) * ((size_t)p.hv * kAmBlock + (size_t)p.hk * (kKqBytes + kGramBytes)) +
+           (slot * p.hk + j) * kMBytes;
+}
+
+// gates of one chunk of one value head as the chain consumes them: e^{G_t},
+// beta_t, e^{G_L - G_t} and e^{G_L} (rows past the chunk's end: lam = beta = 0)
+struct ChainGates {
+    float eG[64], beta[64], kdec[64];
+    float gL, pad[3];
+};
+static_assert(sizeof(ChainGates) % 16 == 0 && sizeof(ChainGates) <= kGateBytes, "gate row");
+
+__device__ __forceinline__ ChainGates* gate_row(const ScanParams& p, size_t slot, int h)
+{
+    return reinterpret_cast<ChainGates*>(am_image(p, slot, h) + kAmBytes);
+}
+
 // slot -> (sequence, first token, token count); false for a slot no sequence uses
-__device__ __forceinline__ bool slot_chunk(const ScanParams& p, int slot, int& c0, int& n)
+// (has_prev: the chunk has a predecessor in its sequence; odd: its index within the
+// sequence is odd, which fixes the row order of its M and [T; P T] images)
+__device__ __forceinline__ bool slot_chunk(const ScanParams& p, int slot, int& c0, int& n, bool* has_prev = nullptr,
+                                           bool* odd = nullptr)
 {
     int lo = 0, hi = p.n_seq - 1;
     while (lo < hi) {  // last s with base(s) <= slot
@@ -152,6 +183,8 @@ __device__ __forceinline__ bool slot_chunk(const ScanParams& p, int slot, int& c
     const int start = cu_at(p.cu_seqlens, lo, p.T), end = max(cu_at(p.cu_seqlens, lo + 1, p.T), start);
     c0 = start + (slot - slot_base(p, lo)) * kChunk;
     n = min(kChunk, end - c0);
+    if (has_prev) *has_prev = slot > slot_base(p, lo);
+    if (odd) *odd = ((slot - slot_base(p, lo)) & 1) != 0;
     return slot >= slot_base(p, lo) && c0 < end;
 }
 
@@ -172,16 +205,60 @@ __device__ __forceinline__ float warp_chunk_cumsum(float (&lam)[2], int lane)
 
 // =======================================================================================
 // gram: one CTA per (chunk slot, key head): split [K; Q] (the chain's operand
-// image) and (K K^T ; Q K^T) in fp32 for the prep kernel
+// image), (K K^T ; Q K^T) in fp32 for the prep kernel, and, for every chunk but
+// a sequence's first, M = [K; Q] K_prev^T against the previous chunk's keys
+// (the chain's look-ahead operand)
 // =======================================================================================
 constexpr int kGramThreads = 256;
 
 struct __align__(1024) GramSmem {
     uint16_t akq[2][128 * 128];  // split [K; Q] (K-major)
+    uint16_t bkp[2][64 * 128];   // split K of the previous chunk (K-major B, 64 rows)
     uint32_t tmem_base;
     int abort_flag;
     uint64_t mbar;
 };
+
+// split 64 token rows x 128 fp32 of one key head into a K-major bf16 tile
+// (rows `row0 + t`), optionally mirroring the bytes to rows `img_row0 + t` of a
+// [K; Q] image
+template <int kThreads>
+__device__ __forceinline__ void load_split_rows(const float* src_base, size_t row_stride, int n, uint16_t* hi,
+                                                uint16_t* lo, int row0, int tile_k, unsigned char* img,
+                                                int img_row0, int tid)
+{
+    constexpr int kU = 64 * 16 / kThreads;
+    float4 ld[2 * kU];
+#pragma unroll
+    for (int q = 0; q < kU; ++q) {
+        const int u = tid + kThreads * q;
+        const int tg = (u >> 7) & 7, g = (u >> 3) & 15, t = tg * 8 + (u & 7);
+        if (t < n) {
+            const float4* src = reinterpret_cast<const float4*>(src_base + (size_t)t * row_stride + g * 8);
+            ld[2 * q] = __ldg(src);
+            ld[2 * q + 1] = __ldg(src + 1);
+        } else {
+            ld[2 * q] = ld[2 * q + 1] = make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+    }
+#pragma unroll
+    for (int q = 0; q < kU; ++q) {
+        const int u = tid + kThreads * q;
+        const int tg = (u >> 7) & 7, g = (u >> 3) & 15, t = tg * 8 + (u & 7);
+        const float x[8] = {ld[2 * q].x, ld[2 * q].y, ld[2 * q].z, ld[2 * q].w,
+                            ld[2 * q + 1].x, ld[2 * q + 1].y, ld[2 * q + 1].z, ld[2 * q + 1].w};
+        uint4 vh, vl;
+        split8(x, vh, vl);
+        const int off = kmaj(row0 + t, g * 8, tile_k);
+        *reinterpret_cast<uint4*>(hi + off) = vh;
+        *reinterpret_cast<uint4*>(lo + off) = vl;
+        if (img) {
+            const int io = kq_off(img_row0 + t, g * 8);
+            *reinterpret_cast<uint4*>(img + io) = vh;
+            *reinterpret_cast<uint4*>(img + io + 2048) = vl;
+        }
+    }
+}
 
 __global__ void __launch_bounds__(kGramThreads) scan_gram_kernel(ScanParams p)
 {
@@ -192,72 +269,67 @@ __global__ void __launch_bounds__(kGramThreads) scan_gram_kernel(ScanParams p)
     const int slot = blockIdx.x, j = blockIdx.y;
     uint32_t* err = reinterpret_cast<uint32_t*>(p.workspace);
     int c0, n;
-    if (!slot_chunk(p, slot, c0, n)) return;  // unused slot (whole CTA)
+    bool has_prev, odd;
+    if (!slot_chunk(p, slot, c0, n, &has_prev, &odd)) return;  // unused slot (whole CTA)
 
-    if (warp == 0) umma::tmem_alloc(&sm.tmem_base, 64);
+    if (warp == 0) umma::tmem_alloc(&sm.tmem_base, 128);
     if (tid == 0) {
         umma::mbar_init(&sm.mbar, 1);
         sm.abort_flag = 0;
     }
-    // Unit u = (matrix, token group, column group, row in group), row fastest so
-    // that 8 consecutive lanes fill one 128-byte core matrix; all loads in flight together.
-    {
-        constexpr int kU = 2 * 64 * 16 / kGramThreads;
-        float4 ld[2 * kU];
-#pragma unroll
-        for (int q = 0; q < kU; ++q) {
-            const int u = tid + kGramThreads * q;
-            const int mat = u >> 10, tg = (u >> 7) & 7, g = (u >> 3) & 15, t = tg * 8 + (u & 7);
-            if (t < n) {
-                const float4* src = reinterpret_cast<const float4*>(
-                    (mat ? p.qn : p.kn) + ((size_t)(c0 + t) * p.hk + j) * kHeadDim + g * 8);
-                ld[2 * q] = __ldg(src);
-                ld[2 * q + 1] = __ldg(src + 1);
-            } else {
-                ld[2 * q] = ld[2 * q + 1] = make_float4(0.f, 0.f, 0.f, 0.f);
-            }
-        }
-        unsigned char* img = kq_image(p, slot, j);
-#pragma unroll
-        for (int q = 0; q < kU; ++q) {
-            const int u = tid + kGramThreads * q;
-            const int mat = u >> 10, tg = (u >> 7) & 7, g = (u >> 3) & 15, t = tg * 8 + (u & 7);
-            const float x[8] = {ld[2 * q].x, ld[2 * q].y, ld[2 * q].z, ld[2 * q].w,
-                                ld[2 * q + 1].x, ld[2 * q + 1].y, ld[2 * q + 1].z, ld[2 * q + 1].w};
-            uint4 vh, vl;
-            split8(x, vh, vl);
-            const int off = kmaj(mat * 64 + t, g * 8, 128);
-            *reinterpret_cast<uint4*>(&sm.akq[0][off]) = vh;
-            *reinterpret_cast<uint4*>(&sm.akq[1][off]) = vl;
-            *reinterpret_cast<uint4*>(img + off * 2) = vh;
-            *reinterpret_cast<uint4*>(img + kKqBytes / 2 + off * 2) = vl;
-        }
-    }
+    const size_t rs = (size_t)p.hk * kHeadDim;
+    unsigned char* img = kq_image(p, slot, j);
+    // image rows in the chunk's stacking order: [K; Q] for even chunks, [Q; K] for odd ones
+    load_split_rows<kGramThreads>(p.kn + (size_t)c0 * rs + (size_t)j * kHeadDim, rs, n, sm.akq[0], sm.akq[1], 0, 128,
+                                  img, odd ? 64 : 0, tid);
+    load_split_rows<kGramThreads>(p.qn + (size_t)c0 * rs + (size_t)j * kHeadDim, rs, n, sm.akq[0], sm.akq[1], 64, 128,
+                                  img, odd ? 0 : 64, tid);
+    if (has_prev)  // the previous chunk is always full
+        load_split_rows<kGramThreads>(p.kn + (size_t)(c0 - kChunk) * rs + (size_t)j * kHeadDim, rs, kChunk, sm.bkp[0],
+                                      sm.bkp[1], 0, 128, nullptr, 0, tid);
     umma::fence_proxy_async();
     umma::fence_before_sync();
     __syncthreads();
     umma::fence_after_sync();
     const uint32_t tmem = sm.tmem_base;
-    // (K K^T ; Q K^T) = [K; Q] K^T  (B = the K rows of the same tile)
+    // (K K^T ; Q K^T) = [K; Q] K^T  (B = the K rows of the same tile);  M = [K; Q] K_prev^T
     if (tid == 0) {
         const uint32_t a_hi = umma::smem_u32(sm.akq[0]), a_lo = umma::smem_u32(sm.akq[1]);
         mma_split(tmem, a_hi, a_lo, 128, 2048, 256, a_hi, a_lo, 2048, 256, 8, umma::idesc_bf16(128, 64, false, false));
+        if (has_prev)
+            mma_split(tmem + 64, a_hi, a_lo, 128, 2048, 256, umma::smem_u32(sm.bkp[0]), umma::smem_u32(sm.bkp[1]), 2048,
+                      256, 8, umma::idesc_bf16(128, 64, false, false));
         umma::commit(&sm.mbar);
     }
     if (!umma::mbar_wait(&sm.mbar, 0)) { sm.abort_flag = 1; atomicOr(err, kErrTimeout); }
     __syncthreads();
     if (!sm.abort_flag) {
         umma::fence_after_sync();
+        const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
         float d[32];
-        umma::tmem_ld32(tmem + ((uint32_t)((warp & 3) * 32) << 16) + 32 * wg, d);
+        umma::tmem_ld32(tmem + lane_off + 32 * wg, d);
         umma::tmem_wait_ld();
         float4* dst = reinterpret_cast<float4*>(gram_rows(p, slot, j) + L * 64 + 32 * wg);
 #pragma unroll
         for (int q = 0; q < 8; ++q) dst[q] = make_float4(d[4 * q], d[4 * q + 1], d[4 * q + 2], d[4 * q + 3]);
+        if (has_prev) {  // M rows -> split K-major image (K = 64 tokens of the previous chunk), Q rows first for odd chunks
+            const int mrow = odd ? (L ^ 64) : L;
+            umma::tmem_ld32(tmem + lane_off + 64 + 32 * wg, d);
+            umma::tmem_wait_ld();
+            unsigned char* mimg = m_image(p, slot, j);
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                uint4 vh, vl;
+                split8(d + 8 * q, vh, vl);
+                const int off = kmaj(mrow, 32 * wg + 8 * q, 64);
+                *reinterpret_cast<uint4*>(mimg + off * 2) = vh;
+                *reinterpret_cast<uint4*>(mimg + kMBytes / 2 + off * 2) = vl;
+            }
+        }
     }
     umma::fence_before_sync();
     __syncthreads();
-    if (warp == 0) umma::tmem_dealloc(sm.tmem_base, 64);
+    if (warp == 0) umma::tmem_dealloc(sm.tmem_base, 128);
 }
 
 // =======================================================================================
@@ -288,7 +360,8 @@ __global__ void __launch_bounds__(kPrepThreads, 3) scan_prep_kernel(ScanParams p
     uint32_t* err = reinterpret_cast<uint32_t*>(p.workspace);
     constexpr int ST = 68;  // fp32 row stride of A and T
     int c0, n;
-    if (!slot_chunk(p, slot, c0, n)) return;  // unused slot (whole CTA)
+    bool odd;
+    if (!slot_chunk(p, slot, c0, n, nullptr, &odd)) return;  // unused slot (whole CTA)
     const float qscale = rsqrtf((float)kHeadDim);
 
     if (warp == 0) umma::tmem_alloc(&sm.tmem_base, 64);
@@ -339,11 +412,19 @@ __global__ void __launch_bounds__(kPrepThreads, 3) scan_prep_kernel(ScanParams p
             for (int q = 0; q < 2; ++q) lam[q] = (lane + 32 * q) < n ? fmaxf(raw_lam[q], kLamFloor) : 0.0f;
             const float b0 = raw_beta[0], b1 = raw_beta[1];
             if (hh + 1 < group) load_gates(h + 1);
-            warp_chunk_cumsum(lam, lane);
+            const float GL = warp_chunk_cumsum(lam, lane);
             sm.G[lane] = lam[0];
             sm.G[lane + 32] = lam[1];
             sm.beta[lane] = b0;
             sm.beta[lane + 32] = b1;
+            ChainGates* gr = gate_row(p, slot, h);  // the chain's copy
+            gr->eG[lane] = __expf(lam[0]);
+            gr->eG[lane + 32] = __expf(lam[1]);
+            gr->kdec[lane] = __expf(GL - lam[0]);
+            gr->kdec[lane + 32] = __expf(GL - lam[1]);
+            gr->beta[lane] = b0;
+            gr->beta[lane + 32] = b1;
+            if (lane == 0) gr->gL = __expf(GL);
         }
         __syncthreads();
 
@@ -493,8 +574,8 @@ __global__ void __launch_bounds__(kPrepThreads, 3) scan_prep_kernel(ScanParams p
         if (sm.abort_flag) goto done;
         umma::fence_after_sync();
 
-        // [T; P T] image (K-major, split): threads L >= 64 write row L - 64 (T, from shared
-        // memory), threads L < 64 write row 64 + L (P T, from TMEM lane L); columns of wg
+        // [T; P T] image (K-major, split; [P T; T] for odd chunks): threads L >= 64 write T row
+        // L - 64 (from shared memory), threads L < 64 write P T row L (from TMEM lane L); columns of wg
         {
             unsigned char* img = am_image(p, slot, h);
             const int cb = 32 * wg;
@@ -519,7 +600,7 @@ __global__ void __launch_bounds__(kPrepThreads, 3) scan_prep_kernel(ScanParams p
             for (int q = 0; q < 4; ++q) {
                 uint4 vh, vl;
                 split8(x + 8 * q, vh, vl);
-                const int off = kmaj(row, cb + 8 * q, 64);
+                const int off = kmaj(odd ? (row ^ 64) : row, cb + 8 * q, 64);
                 *reinterpret_cast<uint4*>(img + off * 2) = vh;
                 *reinterpret_cast<uint4*>(img + kAmBytes / 2 + off * 2) = vl;
             }
@@ -537,23 +618,57 @@ done:
 
 // =======================================================================================
 // chain: one CTA per (sequence, value head, kDVS-column slice)
+//
+// Look-ahead form of the next chunk's (K S ; Q S): with S_{c+1} = g_c S_c + K_c^T U'_c
+// (U' = e^{G_L-G} U, g_c = e^{G_L} of chunk c),
+//     [K; Q]_{c+1} S_{c+1} = [K; Q]_{c+1} (g_c S_c) + M_{c+1} U'_c,   M_{c+1} = [K; Q]_{c+1} K_c^T,
+// so the first product is issued while chunk c is still being worked on and
+// only M U' (K = 64) waits for U'_c; the state update K_c^T U'_c and the fp32
+// state stay off the chunk-to-chunk path.
+//
+// Roles: warps 0-15 (compute; warpgroup w owns columns [16w, 16w+16) of the
+// slice for all 128 TMEM lanes) run three short phases per chunk (X, state,
+// U/O) and publish their operands on mbarriers; warp 16 issues every MMA;
+// warp 17 issues every bulk copy (operand images and gate rows) as soon as its
+// destination buffer is released, so a busy copy engine never delays an MMA.
+//
+// [K; Q] lives in three 64-row half slots R0 R1 R2: Q of every chunk in R1,
+// K of even chunks in R0 and of odd chunks in R2, so K_c stays resident for
+// its state update while both halves of chunk c+1 land.  Odd chunks thus
+// stack [Q; K]; the gram and prep kernels write the [K; Q], M and [T; P T]
+// images of every chunk with its two 64-row halves in that order, so each
+// lands with one bulk copy (an SM's bulk copies retire at roughly one per
+// 600 cycles whatever their size up to 64 KB, so a chunk takes three: [K; Q],
+// M, and [T; P T] with the gate row behind it).  In chunk c the thread in TMEM
+// lane L owns the K-side row L & 63 when (L >> 6) == (c & 1), else the Q-side row.
 // =======================================================================================
-constexpr int kChainWG = 4;                   // warpgroups; each covers all 128 TMEM lanes
-constexpr int kChainThreads = 128 * kChainWG;  // and kDVS / kChainWG of the columns
+constexpr int kChainWG = 4;                        // compute warpgroups
+constexpr int kChainCompute = 128 * kChainWG;
+constexpr int kMmaWarp = kChainCompute / 32;       // issues every MMA
+constexpr int kCopyWarp = kMmaWarp + 1;             // issues every bulk copy
+constexpr int kChainThreads = kChainCompute + 64;
+constexpr uint32_t kSlotBytes = 64 * 128 * 2 * 2;  // one 64-row half of a [K; Q] image, hi + lo
 
 template <int DVS>
 struct __align__(1024) ChainSmem {
-    uint16_t akq[2][2][128 * 128];  // [K; Q] image, double-buffered: [buffer][hi/lo]
-    uint16_t am[2][128 * 64];       // [T; P T] image
-    uint16_t bs[2][128 * DVS];      // S slice (MN-major B, dk x DVS)
-    uint16_t bx[2][64 * DVS];       // X, then e^{G_L-G} U (MN-major B, 64 x DVS)
-    float v[64 * (DVS + 4)];        // V tile of the slice (rows padded by 16 bytes), later the O tile
-    float eG[64], beta[64], kdec[64];
-    float gL;
+    unsigned char kh[3 * kSlotBytes];  // half slots R0 R1 R2 of the [K; Q] tiles, image layout
+    uint16_t mm[2][128 * 64];      // M image of the chunk, rows in its stacking order
+    uint16_t am[2][128 * 64];      // [T; P T] image, same order; the gate row lands right behind it
+    ChainGates gb;
+    uint16_t bs[2][128 * DVS];     // g_c S_c slice (MN-major B, dk x DVS), hi then lo
+    uint16_t bx[2][64 * DVS];      // X (MN-major B, 64 x DVS); between uses the fp32 V / O staging tile
+    uint16_t bu[2][64 * DVS];      // U' = e^{G_L-G} U
     uint32_t tmem_base;
     int abort_flag;
-    uint64_t mbar_mma, mbar_kq[2], mbar_am;
+    uint64_t mb_kq, mb_m, mb_am;          // bulk copies
+    uint64_t mb_f, mb_d3, mb_d4, mb_fin;  // MMA completions
+    uint64_t mb_x, mb_s, mb_u;            // compute -> producer (all compute threads arrive)
+    uint64_t mb_grp[2];                   // row groups of the compute threads (lanes 0-63 / 64-127)
 };
+
+// fp32 64 x 64 staging tile over bx: row r, 16-byte column chunk k at chunk
+// (k ^ (r & 15)) of the row, so that a warp's 32 rows hit distinct banks
+__device__ __forceinline__ int stage_off(int r, int k) { return r * 64 + ((k ^ (r & 15)) << 2); }
 
 template <int COLS>
 __device__ __forceinline__ void tmem_ld_cols(uint32_t taddr, float (&d)[COLS])
@@ -563,24 +678,35 @@ __device__ __forceinline__ void tmem_ld_cols(uint32_t taddr, float (&d)[COLS])
     else umma::tmem_ld32(taddr, d);
 }
 
+// Wait for an mbarrier phase with the thread suspended between checks (no
+// polling traffic), bounded by about two seconds of SM clock and abandoned
+// once another thread of the CTA has aborted; the warp agrees on the outcome
+// so that it stays converged.
+__device__ __forceinline__ bool chain_wait(uint64_t* mbar, uint32_t parity, const volatile int* abort_flag)
+{
+    bool ok = umma::mbar_try_wait(mbar, parity);
+    if (!ok) {
+        const long long start = clock64();
+        while (!(ok = umma::mbar_try_wait_suspend(mbar, parity, 20000u))) {
+            if (*abort_flag || clock64() - start > (4ll << 30)) break;
+        }
+    }
+    return __all_sync(0xffffffffu, ok);
+}
+
 template <int DVS>
 __global__ void __launch_bounds__(kChainThreads, 1) scan_chain_kernel(ScanParams p)
 {
     extern __shared__ __align__(1024) unsigned char smem_raw[];
     ChainSmem<DVS>& sm = *reinterpret_cast<ChainSmem<DVS>*>(smem_raw);
     constexpr int SLICES = kHeadDim / DVS;
-    constexpr int COLS = DVS / kChainWG;  // columns per thread
+    constexpr int COLS = DVS / kChainWG;  // columns per compute thread
     constexpr uint32_t kTmemCols = 512;
     // each product takes 2*DVS columns: [hi*hi + lo*hi | hi*lo]
     constexpr uint32_t cD2 = 0, cD3 = 2 * DVS, cD4 = 4 * DVS;
     static_assert(6 * DVS <= (int)kTmemCols, "TMEM columns");
-    constexpr int kGateWarp = 3;   // computes the gates while thread 0 issues MMAs
-    constexpr int kCopyThread = 64;  // issues the bulk copies
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int L = tid & 127;            // TMEM lane of this thread
-    const int wg = tid >> 7;            // column group
-    const int cb = wg * COLS;           // first column of this thread within the slice
     const int h = blockIdx.x / SLICES, slice = blockIdx.x % SLICES, s = blockIdx.y;
     const int j = h / (p.hv / p.hk);
     const int v0 = slice * DVS;
@@ -588,292 +714,386 @@ __global__ void __launch_bounds__(kChainThreads, 1) scan_chain_kernel(ScanParams
     const int n_chunks = (t1 - t0 + kChunk - 1) / kChunk;
     const size_t base = (size_t)slot_base(p, s);
     const size_t sbase = ((size_t)s * p.hv + h) * kHeadDim * kHeadDim;
-    const float qscale = rsqrtf((float)kHeadDim);
     uint32_t* err = reinterpret_cast<uint32_t*>(p.workspace);
+    const volatile int* abort_flag = &sm.abort_flag;
+    // copy warp's bulk copies per destination (bit 0: [K; Q], 1: M, 2: [T; P T] + gates):
+    // `used` = issued at least once, `np` = parity bit the next issue will complete (drained on exit)
+    uint32_t used = 0, np = 0;
+    constexpr uint32_t kBitKq = 1u, kBitM = 2u, kBitAm = 4u;
 
     if (warp == 0) umma::tmem_alloc(&sm.tmem_base, kTmemCols);
     if (tid == 0) {
-        umma::mbar_init(&sm.mbar_mma, 1);
-        umma::mbar_init(&sm.mbar_kq[0], 1);
-        umma::mbar_init(&sm.mbar_kq[1], 1);
-        umma::mbar_init(&sm.mbar_am, 1);
+        umma::mbar_init(&sm.mb_kq, 1);
+        umma::mbar_init(&sm.mb_m, 32);  // one completion arrival per copy-warp lane
+        umma::mbar_init(&sm.mb_am, 1);
+        umma::mbar_init(&sm.mb_f, 1);
+        umma::mbar_init(&sm.mb_d3, 1);
+        umma::mbar_init(&sm.mb_d4, 1);
+        umma::mbar_init(&sm.mb_fin, 1);
+        umma::mbar_init(&sm.mb_x, kChainCompute);
+        umma::mbar_init(&sm.mb_s, kChainCompute);
+        umma::mbar_init(&sm.mb_u, kChainCompute);
+        umma::mbar_init(&sm.mb_grp[0], kChainCompute / 2);
+        umma::mbar_init(&sm.mb_grp[1], kChainCompute / 2);
         sm.abort_flag = 0;
     }
-
-    // state slice: thread (L, wg) holds row L (key index), columns v0 + cb + [0, COLS)
-    float S[COLS];
-    {
-        const float* src = p.S_in + sbase + (size_t)L * kHeadDim + v0 + cb;
-#pragma unroll
-        for (int c = 0; c < COLS; c += 4) {
-            const float4 x = *reinterpret_cast<const float4*>(src + c);
-            S[c] = x.x; S[c + 1] = x.y; S[c + 2] = x.z; S[c + 3] = x.w;
-        }
-#pragma unroll
-        for (int c = 0; c < COLS; c += 8)
-            store_split8(&sm.bs[0][mnmaj(cb + c, L, 128)], &sm.bs[1][mnmaj(cb + c, L, 128)], S + c);
-    }
-    umma::fence_proxy_async();
     umma::fence_before_sync();
     __syncthreads();
     umma::fence_after_sync();
-
     const uint32_t tmem = sm.tmem_base;
-    const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
-    const uint32_t b_s = umma::smem_u32(sm.bs[0]);
-    const uint32_t b_x = umma::smem_u32(sm.bx[0]);
-    const uint32_t a_m[2] = {umma::smem_u32(sm.am[0]), umma::smem_u32(sm.am[1])};
-    uint32_t ph_mma = 0;
-    // outstanding bulk copies (uniform across threads): issued but not yet waited
-    bool pend_kq[2] = {false, false}, pend_am = false;
-
-    // ---- bulk-copy issue helpers -----------------------------------------------------------
-    auto issue_kq = [&](int c) {  // [K; Q] image of chunk c into buffer c & 1
-        if (tid == kCopyThread) {
-            uint64_t* mb = &sm.mbar_kq[c & 1];
-            umma::mbar_arrive_expect_tx(mb, (uint32_t)kKqBytes);
-            umma::bulk_g2s(sm.akq[c & 1], kq_image(p, base + c, j), (uint32_t)kKqBytes, mb);
-        }
-        pend_kq[c & 1] = true;
-    };
-    auto issue_am = [&](int c) {
-        if (tid == kCopyThread) {
-            umma::mbar_arrive_expect_tx(&sm.mbar_am, (uint32_t)kAmBytes);
-            umma::bulk_g2s(sm.am, am_image(p, base + c, h), (uint32_t)kAmBytes, &sm.mbar_am);
-        }
-        pend_am = true;
-    };
-    // V tile of a chunk: every thread loads its float4s into registers one chunk ahead
-    constexpr int kVq = 64 * DVS / 4 / kChainThreads;
-    float4 vpre[kVq];
-    auto load_v = [&](int c) {
-        const int cc0 = t0 + c * kChunk, nn = min(kChunk, t1 - cc0);
-#pragma unroll
-        for (int q = 0; q < kVq; ++q) {
-            const int u = tid + kChainThreads * q, t = u / (DVS / 4), c4 = (u % (DVS / 4)) * 4;
-            vpre[q] = t < nn ? __ldg(reinterpret_cast<const float4*>(p.vc + ((size_t)(cc0 + t) * p.hv + h) * kHeadDim + v0 + c4))
-                             : make_float4(0.f, 0.f, 0.f, 0.f);
-        }
-    };
-    auto store_v = [&]() {
-#pragma unroll
-        for (int q = 0; q < kVq; ++q) {
-            const int u = tid + kChainThreads * q, t = u / (DVS / 4), c4 = (u % (DVS / 4)) * 4;
-            *reinterpret_cast<float4*>(&sm.v[t * (DVS + 4) + c4]) = vpre[q];
-        }
-    };
-    // gates of one chunk, raw values prefetched into the gate warp's registers one chunk ahead
-    float lam_nx[2] = {0.f, 0.f}, bet_nx[2] = {0.f, 0.f};
-    int n_nx = 0;
-    auto load_gates = [&](int c) {
-        const int cc0 = t0 + c * kChunk, nn = min(kChunk, t1 - cc0);
-        n_nx = nn;
-        if (warp == kGateWarp) {
-#pragma unroll
-            for (int q = 0; q < 2; ++q) {
-                const int t = lane + 32 * q;
-                lam_nx[q] = t < nn ? __ldg(p.glog + (size_t)(cc0 + t) * p.hv + h) : 0.0f;
-                bet_nx[q] = t < nn ? __ldg(p.beta + (size_t)(cc0 + t) * p.hv + h) : 0.0f;
-            }
-        }
-    };
 
 #define GDN_WAIT(mbar, parity)                                                 \
     do {                                                                       \
-        if (!umma::mbar_wait((mbar), (parity))) {                              \
-            sm.abort_flag = 1;                                                 \
-            atomicOr(err, kErrTimeout);                                        \
+        if (!chain_wait((mbar), (parity), abort_flag)) {                       \
+            if (lane == 0) {                                                   \
+                sm.abort_flag = 1;                                             \
+                atomicOr(err, kErrTimeout);                                    \
+            }                                                                  \
+            goto done;                                                         \
         }                                                                      \
     } while (0)
-#define GDN_SYNC_OR_ABORT()                                                    \
-    do {                                                                       \
-        __syncthreads();                                                       \
-        if (sm.abort_flag) goto done;                                          \
-        umma::fence_after_sync();                                              \
-    } while (0)
-#define GDN_PUBLISH()                                                          \
-    do {                                                                       \
-        umma::fence_proxy_async();                                             \
-        umma::fence_before_sync();                                             \
-        __syncthreads();                                                       \
-        umma::fence_after_sync();                                              \
-    } while (0)
 
-    if (n_chunks > 0) {
-        issue_kq(0);
-        issue_am(0);
-        load_gates(0);
-        load_v(0);
-        store_v();
-    }
+    if (warp == kCopyWarp) {
+        // ================================ bulk copies ================================
+        const bool leader = lane == 0;
+        auto issue = [&](uint64_t* mb, void* dst, const void* src, uint32_t bytes, uint32_t bit) {
+            if (leader) {
+                umma::mbar_arrive_expect_tx(mb, bytes);
+                umma::bulk_g2s(dst, src, bytes, mb);
+            }
+            used |= bit;
+            np ^= bit;
+        };
+        // [K; Q] of chunk c into slots (R0, R1) (even c) or (R1, R2) (odd c)
+        auto load_kq = [&](int c) {
+            issue(&sm.mb_kq, sm.kh + (c & 1) * kSlotBytes, kq_image(p, base + c, j), (uint32_t)kKqBytes, kBitKq);
+        };
+        auto load_am = [&](int c) {  // [T; P T] and the gate row
+            issue(&sm.mb_am, sm.am, am_image(p, base + c, h), (uint32_t)(kAmBytes + sizeof(ChainGates)), kBitAm);
+        };
 
-    for (int c = 0; c < n_chunks; ++c) {
-        const int c0 = t0 + c * kChunk, n = min(kChunk, t1 - c0);
-        const bool more = c + 1 < n_chunks;
-        if (more) issue_kq(c + 1);  // its buffer was last read by chunk c-1's state update
-
-        // ---- (K S0 ; Q S0) = [K; Q] S0 ------------------------------------------------------------
-        GDN_WAIT(&sm.mbar_kq[c & 1], (c >> 1) & 1);
-        pend_kq[c & 1] = false;
-        GDN_SYNC_OR_ABORT();
-        const uint32_t a_kq_hi = umma::smem_u32(sm.akq[c & 1][0]), a_kq_lo = umma::smem_u32(sm.akq[c & 1][1]);
-        if (tid == 0) {
-            mma_split2(tmem + cD2, a_kq_hi, a_kq_lo, 128, 2048, 256, b_s, 2048, 256, 8, DVS, false, true);
-            umma::commit(&sm.mbar_mma);
+        // Each wait below precedes the copy that lets its barrier advance twice, so a
+        // parity wait never sees a phase two ahead.
+        if (n_chunks > 0) {
+            load_kq(0);
+            load_am(0);
         }
-        // ---- meanwhile: gates e^G, beta, e^{G_L - G}, e^{G_L}; next chunk's gates and V ---------
-        if (warp == kGateWarp) {
-            float lam[2];
-#pragma unroll
-            for (int q = 0; q < 2; ++q) lam[q] = (lane + 32 * q) < n_nx ? fmaxf(lam_nx[q], kLamFloor) : 0.0f;
-            const float b0 = bet_nx[0], b1 = bet_nx[1];
-            if (more) load_gates(c + 1);
-            const float GL = warp_chunk_cumsum(lam, lane);
-            sm.eG[lane] = __expf(lam[0]);
-            sm.eG[lane + 32] = __expf(lam[1]);
-            sm.kdec[lane] = __expf(GL - lam[0]);
-            sm.kdec[lane + 32] = __expf(GL - lam[1]);
-            sm.beta[lane] = b0;
-            sm.beta[lane + 32] = b1;
-            if (lane == 0) sm.gL = __expf(GL);
-        } else if (more) {
-            n_nx = min(kChunk, t1 - (c0 + kChunk));
+        for (int c = 0; c + 1 < n_chunks; ++c) {
+            // R1 (Q_c) and M free once (K S ; Q S) of chunk c is complete; the slot of K_{c-1}
+            // once that chunk's state update is done
+            GDN_WAIT(&sm.mb_f, c & 1);
+            if (c >= 1) GDN_WAIT(&sm.mb_d4, (c - 1) & 1);
+            load_kq(c + 1);
+            {   // M through the load/store path (16-byte asynchronous copies, the whole warp), which
+                // keeps the bulk-copy engine free for the other two images
+                const unsigned char* src = m_image(p, base + c + 1, j);
+                const uint32_t dst = umma::smem_u32(sm.mm);
+#pragma unroll 8
+                for (int q = 0; q < (int)(kMBytes / 512); ++q)
+                    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst + q * 512 + lane * 16),
+                                 "l"(src + q * 512 + lane * 16)
+                                 : "memory");
+                asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(umma::smem_u32(&sm.mb_m))
+                             : "memory");
+                used |= kBitM;
+                np ^= kBitM;
+            }
+            // [T; P T] of chunk c consumed (every compute thread read its gates at chunk start)
+            GDN_WAIT(&sm.mb_d3, c & 1);
+            load_am(c + 1);
         }
-        if (more) load_v(c + 1);
-        GDN_WAIT(&sm.mbar_mma, ph_mma);
-        ph_mma ^= 1u;
-        GDN_SYNC_OR_ABORT();
+    } else if (warp == kMmaWarp) {
+        // ================================ MMA issue ================================
+        const bool leader = lane == 0;
+        // [K; Q] tiles: K-major, row groups 4 KB apart with the lo plane 2 KB behind the hi one
+        const uint32_t kh0 = umma::smem_u32(sm.kh);
+        const uint32_t b_s = umma::smem_u32(sm.bs[0]), b_x = umma::smem_u32(sm.bx[0]), b_u = umma::smem_u32(sm.bu[0]);
+        const uint32_t a_m_hi = umma::smem_u32(sm.mm[0]), a_m_lo = umma::smem_u32(sm.mm[1]);
+        const uint32_t a_t_hi = umma::smem_u32(sm.am[0]), a_t_lo = umma::smem_u32(sm.am[1]);
+        auto kslot = [](int c) { return (c & 1) ? 2u : 0u; };
 
-        // ---- X = beta (V - e^G K S0) -> bx;  keep e^G Q S0 / sqrt(dk) --------------------------------
-        float qs[COLS];
+        if (n_chunks > 0) {  // (K S0 ; Q S0) of chunk 0
+            GDN_WAIT(&sm.mb_s, 0);
+            GDN_WAIT(&sm.mb_kq, 0);
+            umma::fence_after_sync();
+            if (leader) {
+                mma_split2(tmem + cD2, kh0, kh0 + 2048, 128, 4096, 256, b_s, 2048, 256, 8, DVS, false, true);
+                umma::commit(&sm.mb_f);
+            }
+            __syncwarp();
+        }
+        for (int c = 0; c < n_chunks; ++c) {
+            const bool more = c + 1 < n_chunks;
+            // (U ; P U) = [T; P T] X
+            GDN_WAIT(&sm.mb_x, c & 1);
+            GDN_WAIT(&sm.mb_am, c & 1);
+            umma::fence_after_sync();
+            if (leader) {
+                mma_split2(tmem + cD3, a_t_hi, a_t_lo, 128, 1024, 256, b_x, 1024, 256, 4, DVS, false, true);
+                umma::commit(&sm.mb_d3);
+            }
+            __syncwarp();
+            // [K; Q]_{c+1} (g_c S_c) once the compute threads have published g_c S_c
+            if (more) {
+                GDN_WAIT(&sm.mb_s, (c + 1) & 1);
+                GDN_WAIT(&sm.mb_kq, (c + 1) & 1);
+                umma::fence_after_sync();
+                const uint32_t a = kh0 + ((c + 1) & 1) * kSlotBytes;  // stacked from R1 (odd) or R0 (even)
+                if (leader)
+                    mma_split2(tmem + cD2, a, a + 2048, 128, 4096, 256, b_s, 2048, 256, 8, DVS, false, true);
+                __syncwarp();
+            }
+            // U'_c published: M_{c+1} U'_c on top (the chunk-to-chunk path), then K_c^T U'_c
+            GDN_WAIT(&sm.mb_u, c & 1);
+            if (more) GDN_WAIT(&sm.mb_m, c & 1);
+            umma::fence_after_sync();
+            if (leader) {
+                if (more) {
+                    mma_split2(tmem + cD2, a_m_hi, a_m_lo, 128, 1024, 256, b_u, 1024, 256, 4, DVS, false, true, true);
+                    umma::commit(&sm.mb_f);
+                }
+                // K_c^T: MN-major view of the K half (token groups 4 KB apart, key groups 128 B)
+                const uint32_t kb = kh0 + kslot(c) * kSlotBytes;
+                mma_split2(tmem + cD4, kb, kb + 2048, 4096, 128, 8192, b_u, 1024, 256, 4, DVS, true, true);
+                umma::commit(&sm.mb_d4);
+            }
+            __syncwarp();
+        }
+    } else {
+        // ================================ compute ================================
+        const int L = tid & 127;   // TMEM lane of this thread
+        const int wg = tid >> 7;   // column group
+        const int cb = wg * COLS;  // first column of this thread within the slice
+        const int t = L & 63;      // chunk row this thread owns
+        const int grp = L >> 6;    // row group: K side of even chunks (0) or of odd chunks (1)
+        const int tig = t + 64 * wg;  // index within the row group, 0..255
+        const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
+        const float qscale = rsqrtf((float)kHeadDim);
+        float* stage = reinterpret_cast<float*>(sm.bx[0]);
+        uint32_t gph = 0;  // parity of this row group's next mbarrier phase
+        // all 256 threads of the row group have arrived (generic shared-memory writes published)
+#define GDN_GROUP_SYNC()                                                       \
+    do {                                                                       \
+        umma::mbar_arrive(&sm.mb_grp[grp]);                                    \
+        GDN_WAIT(&sm.mb_grp[grp], gph);                                        \
+        gph ^= 1u;                                                             \
+    } while (0)
+        // 16-byte piece (row r, chunk k) of a chunk's V tile -> the same place of the staging
+        // tile, asynchronously (rows past the chunk's end read as zero)
+        auto fetch_v_piece = [&](int cc0, int nn, int r, int k) {
+            const float* src = p.vc + ((size_t)(cc0 + min(r, nn - 1)) * p.hv + h) * kHeadDim + v0 + 4 * k;
+            asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(umma::smem_u32(stage + stage_off(r, k))),
+                         "l"(src), "r"(r < nn ? 16 : 0)
+                         : "memory");
+        };
+        // completion of this thread's V pieces arrives on its row group's mbarrier
+        auto v_arrive = [&]() {
+            asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(umma::smem_u32(&sm.mb_grp[grp]))
+                         : "memory");
+        };
+
+        // state slice: row L (key index), columns v0 + cb + [0, COLS)
+        float S[COLS];
         {
-            const int t = L & 63;
-            float d[COLS], d2[COLS];
-            tmem_ld_cols<COLS>(tmem + lane_off + cD2 + cb, d);
-            tmem_ld_cols<COLS>(tmem + lane_off + cD2 + DVS + cb, d2);
-            umma::tmem_wait_ld();
+            const float* src = p.S_in + sbase + (size_t)L * kHeadDim + v0 + cb;
 #pragma unroll
-            for (int e = 0; e < COLS; ++e) d[e] += d2[e];
-            if (L < 64) {
-                const float bt = sm.beta[t], eg = sm.eG[t];
-                const float4* vr = reinterpret_cast<const float4*>(&sm.v[t * (DVS + 4) + cb]);
+            for (int e = 0; e < COLS; e += 4) {
+                const float4 x = *reinterpret_cast<const float4*>(src + e);
+                S[e] = x.x; S[e + 1] = x.y; S[e + 2] = x.z; S[e + 3] = x.w;
+            }
+        }
+        if (n_chunks > 0) {
 #pragma unroll
-                for (int cc = 0; cc < COLS; cc += 8) {
-                    const float4 va = vr[cc / 4], vb = vr[cc / 4 + 1];
-                    const float vv[8] = {va.x, va.y, va.z, va.w, vb.x, vb.y, vb.z, vb.w};
+            for (int e = 0; e < COLS; e += 8)
+                store_split8(&sm.bs[0][mnmaj(cb + e, L, 128)], &sm.bs[1][mnmaj(cb + e, L, 128)], S + e);
+            umma::fence_proxy_async();
+            umma::mbar_arrive(&sm.mb_s);
+            if (grp == 0) {  // V of chunk 0, by the row group that owns its K side
+                const int nn = min(kChunk, t1 - t0);
+#pragma unroll
+                for (int q = 0; q < 4; ++q) fetch_v_piece(t0, nn, (tig + 256 * q) >> 4, (tig + 256 * q) & 15);
+                v_arrive();
+            }
+        }
+        float gl_prev = 1.0f;
+
+        for (int c = 0; c < n_chunks; ++c) {
+            const int c0 = t0 + c * kChunk, n = min(kChunk, t1 - c0);
+            const bool kside = grp == (c & 1);
+
+            // ---- X = beta (V - e^G K S) -> bx;  keep e^G Q S / sqrt(dk) ------------------------------
+            GDN_WAIT(&sm.mb_am, c & 1);  // gate row of chunk c (with its [T; P T] image)
+            // this thread's gates; the buffer is reloaded once every thread is past this phase
+            const float g_eG = sm.gb.eG[t], g_beta = sm.gb.beta[t], g_kdec = sm.gb.kdec[t], gl = sm.gb.gL;
+            GDN_WAIT(&sm.mb_f, c & 1);
+            umma::fence_after_sync();
+            float qs[COLS];
+            {
+                float d[COLS], d2[COLS];
+                tmem_ld_cols<COLS>(tmem + lane_off + cD2 + cb, d);
+                tmem_ld_cols<COLS>(tmem + lane_off + cD2 + DVS + cb, d2);
+                umma::tmem_wait_ld();
+#pragma unroll
+                for (int e = 0; e < COLS; ++e) d[e] += d2[e];
+                if (kside) {
+                    GDN_WAIT(&sm.mb_grp[grp], gph);  // V tile landed
+                    gph ^= 1u;
+                    const float bt = g_beta, eg = g_eG;
+#pragma unroll
+                    for (int e = 0; e < COLS; e += 4) {  // X in place of K S
+                        const float4 v = *reinterpret_cast<const float4*>(stage + stage_off(t, (cb + e) >> 2));
+                        d[e] = bt * (v.x - eg * d[e]);
+                        d[e + 1] = bt * (v.y - eg * d[e + 1]);
+                        d[e + 2] = bt * (v.z - eg * d[e + 2]);
+                        d[e + 3] = bt * (v.w - eg * d[e + 3]);
+                    }
+                    GDN_GROUP_SYNC();  // every V read done before X overwrites the tile
+#pragma unroll
+                    for (int e = 0; e < COLS; e += 8)
+                        store_split8(&sm.bx[0][mnmaj(cb + e, t, 64)], &sm.bx[1][mnmaj(cb + e, t, 64)], d + e);
+                    umma::fence_proxy_async();
+                } else {
+                    const float f = g_eG * qscale;
+#pragma unroll
+                    for (int e = 0; e < COLS; ++e) qs[e] = f * d[e];
+                }
+            }
+            umma::fence_before_sync();
+            umma::mbar_arrive(&sm.mb_x);
+            // the next chunk's V rows -> L2 (one line per thread of half this row group), so that
+            // its later fetch into the staging tile hits there
+            if (!kside && c + 1 < n_chunks && tig < 128) {
+                const int r = tig >> 1, cc0 = t0 + (c + 1) * kChunk;
+                if (cc0 + r < t1)
+                    asm volatile("prefetch.global.L2 [%0];" ::"l"(p.vc + ((size_t)(cc0 + r) * p.hv + h) * kHeadDim + v0 +
+                                                                   32 * (tig & 1)));
+            }
+
+            // ---- S_c = g_{c-1} S_{c-1} + K_{c-1}^T U'_{c-1};  g_c S_c -> bs ----------------------------
+            if (c > 0) {
+                GDN_WAIT(&sm.mb_d4, (c - 1) & 1);
+                umma::fence_after_sync();
+                float d[COLS], d2[COLS];
+                tmem_ld_cols<COLS>(tmem + lane_off + cD4 + cb, d);
+                tmem_ld_cols<COLS>(tmem + lane_off + cD4 + DVS + cb, d2);
+                umma::tmem_wait_ld();
+#pragma unroll
+                for (int e = 0; e < COLS; ++e) S[e] = fmaf(gl_prev, S[e], d[e] + d2[e]);
+            }
+            if (c + 1 < n_chunks) {
+#pragma unroll
+                for (int e = 0; e < COLS; e += 8) {
                     float x[8];
 #pragma unroll
-                    for (int e = 0; e < 8; ++e) x[e] = bt * (vv[e] - eg * d[cc + e]);
-                    store_split8(&sm.bx[0][mnmaj(cb + cc, t, 64)], &sm.bx[1][mnmaj(cb + cc, t, 64)], x);
+                    for (int q = 0; q < 8; ++q) x[q] = gl * S[e + q];
+                    store_split8(&sm.bs[0][mnmaj(cb + e, L, 128)], &sm.bs[1][mnmaj(cb + e, L, 128)], x);
                 }
-            } else {
-                const float f = sm.eG[t] * qscale;
+                umma::fence_proxy_async();
+                umma::fence_before_sync();
+                umma::mbar_arrive(&sm.mb_s);
+            }
+            gl_prev = gl;
+
+            // ---- U' = e^{G_L-G} U -> bu;  O = e^G Q S / sqrt(dk) + P U -> staging -> global -------------
+            GDN_WAIT(&sm.mb_d3, c & 1);  // X consumed: the staging tile is free
+            umma::fence_after_sync();
+            {
+                float d[COLS], d2[COLS];
+                tmem_ld_cols<COLS>(tmem + lane_off + cD3 + cb, d);
+                tmem_ld_cols<COLS>(tmem + lane_off + cD3 + DVS + cb, d2);
+                umma::tmem_wait_ld();
 #pragma unroll
-                for (int e = 0; e < COLS; ++e) qs[e] = f * d[e];
+                for (int e = 0; e < COLS; ++e) d[e] += d2[e];
+                if (kside) {
+                    const float kd = g_kdec;
+#pragma unroll
+                    for (int e = 0; e < COLS; e += 8) {
+                        float x[8];
+#pragma unroll
+                        for (int q = 0; q < 8; ++q) x[q] = kd * d[e + q];
+                        store_split8(&sm.bu[0][mnmaj(cb + e, t, 64)], &sm.bu[1][mnmaj(cb + e, t, 64)], x);
+                    }
+                    umma::fence_proxy_async();
+                } else {
+#pragma unroll
+                    for (int e = 0; e < COLS; e += 4)
+                        *reinterpret_cast<float4*>(stage + stage_off(t, (cb + e) >> 2)) =
+                            make_float4(qs[e] + d[e], qs[e + 1] + d[e + 1], qs[e + 2] + d[e + 2], qs[e + 3] + d[e + 3]);
+                }
+            }
+            umma::fence_before_sync();
+            umma::mbar_arrive(&sm.mb_u);
+            if (!kside) {
+                GDN_GROUP_SYNC();  // O tile staged
+                // coalesced copy-out (16 threads per 256-byte row); each piece read out is at once
+                // refilled with the next chunk's V piece for the same place, which this group (the
+                // next chunk's K side) reads after its mbarrier completes
+                const bool more = c + 1 < n_chunks;
+                const int cn0 = c0 + kChunk, nn = more ? min(kChunk, t1 - cn0) : 0;
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    const int u = tig + 256 * q, r = u >> 4, k = u & 15;
+                    const float4 ov = *reinterpret_cast<const float4*>(stage + stage_off(r, k));
+                    // a chunk followed by another is full, so every piece is stored, and the refill
+                    // is issued after that store has consumed the piece
+                    if (r < n)
+                        __stcs(reinterpret_cast<float4*>(p.o + ((size_t)(c0 + r) * p.hv + h) * kHeadDim + v0) + k, ov);
+                    if (more) fetch_v_piece(cn0, nn, r, k);
+                }
+                if (more) v_arrive();
             }
         }
-        GDN_PUBLISH();
-
-        // ---- (U ; P U) = [T; P T] X --------------------------------------------------------------------
-        GDN_WAIT(&sm.mbar_am, c & 1);
-        pend_am = false;
-        GDN_SYNC_OR_ABORT();
-        if (tid == 0) {
-            mma_split2(tmem + cD3, a_m[0], a_m[1], 128, 1024, 256, b_x, 1024, 256, 4, DVS, false, true);
-            umma::commit(&sm.mbar_mma);
-        }
-        GDN_WAIT(&sm.mbar_mma, ph_mma);
-        ph_mma ^= 1u;
-        GDN_SYNC_OR_ABORT();
-        if (more) issue_am(c + 1);  // [T; P T] image consumed
-
-        // ---- e^{G_L-G} U -> bx;  O = e^G Q S0 / sqrt(dk) + P U -> the V tile ----------------------------
-        {
-            const int t = L & 63;
-            float d[COLS], d2[COLS];
-            tmem_ld_cols<COLS>(tmem + lane_off + cD3 + cb, d);
-            tmem_ld_cols<COLS>(tmem + lane_off + cD3 + DVS + cb, d2);
-            umma::tmem_wait_ld();
-#pragma unroll
-            for (int e = 0; e < COLS; ++e) d[e] += d2[e];
-            if (L < 64) {
-                const float kd = sm.kdec[t];
-#pragma unroll
-                for (int e = 0; e < COLS; ++e) d[e] *= kd;
-#pragma unroll
-                for (int cc = 0; cc < COLS; cc += 8)
-                    store_split8(&sm.bx[0][mnmaj(cb + cc, t, 64)], &sm.bx[1][mnmaj(cb + cc, t, 64)], d + cc);
-            } else {  // O row t -> the (consumed) V tile, written out coalesced below
-                float* dst = &sm.v[t * (DVS + 4) + cb];
-#pragma unroll
-                for (int e = 0; e < COLS; e += 4)
-                    *reinterpret_cast<float4*>(dst + e) =
-                        make_float4(qs[e] + d[e], qs[e + 1] + d[e + 1], qs[e + 2] + d[e + 2], qs[e + 3] + d[e + 3]);
-            }
-        }
-        GDN_PUBLISH();
-
-        // ---- dS = K^T (e^{G_L-G} U): K^T is the K half of the [K; Q] image, MN-major ------------------
-        if (tid == 0) {
-            mma_split2(tmem + cD4, a_kq_hi, a_kq_lo, 2048, 128, 4096, b_x, 1024, 256, 4, DVS, true, true);
-            umma::commit(&sm.mbar_mma);
-        }
-        // O tile -> global while the state update runs: DVS/4 threads per row
-#pragma unroll
-        for (int q = 0; q < kVq; ++q) {
-            const int u = tid + kChainThreads * q, t = u / (DVS / 4), c4 = (u % (DVS / 4)) * 4;
-            if (t < n)
-                __stcs(reinterpret_cast<float4*>(p.o + ((size_t)(c0 + t) * p.hv + h) * kHeadDim + v0 + c4),
-                       *reinterpret_cast<const float4*>(&sm.v[t * (DVS + 4) + c4]));
-        }
-        GDN_WAIT(&sm.mbar_mma, ph_mma);
-        ph_mma ^= 1u;
-        GDN_SYNC_OR_ABORT();
-        if (more) store_v();  // O tile written out: the next chunk's V goes in
-
-        // ---- S = e^{G_L} S + dS -> registers and bs ----------------------------------------------------
-        {
-            const float gl = sm.gL;
+        if (n_chunks > 0) {  // the last chunk's state update
+            GDN_WAIT(&sm.mb_d4, (n_chunks - 1) & 1);
+            umma::fence_after_sync();
             float d[COLS], d2[COLS];
             tmem_ld_cols<COLS>(tmem + lane_off + cD4 + cb, d);
             tmem_ld_cols<COLS>(tmem + lane_off + cD4 + DVS + cb, d2);
             umma::tmem_wait_ld();
 #pragma unroll
-            for (int e = 0; e < COLS; ++e) S[e] = fmaf(gl, S[e], d[e] + d2[e]);
-#pragma unroll
-            for (int cc = 0; cc < COLS; cc += 8)
-                store_split8(&sm.bs[0][mnmaj(cb + cc, L, 128)], &sm.bs[1][mnmaj(cb + cc, L, 128)], S + cc);
+            for (int e = 0; e < COLS; ++e) S[e] = fmaf(gl_prev, S[e], d[e] + d2[e]);
         }
-        GDN_PUBLISH();
-    }
-
-    {
-        float* dst = p.S_out + sbase + (size_t)L * kHeadDim + v0 + cb;
+        {
+            float* dst = p.S_out + sbase + (size_t)L * kHeadDim + v0 + cb;
 #pragma unroll
-        for (int c = 0; c < COLS; c += 4)
-            *reinterpret_cast<float4*>(dst + c) = make_float4(S[c], S[c + 1], S[c + 2], S[c + 3]);
+            for (int e = 0; e < COLS; e += 4)
+                *reinterpret_cast<float4*>(dst + e) = make_float4(S[e], S[e + 1], S[e + 2], S[e + 3]);
+        }
+#undef GDN_GROUP_SYNC
     }
 
 done:
-    // drain any copy still in flight into this CTA's shared memory (bounded), free TMEM
-    if (tid == kCopyThread) {
-        for (int b = 0; b < 2; ++b)
-            if (pend_kq[b]) umma::mbar_wait(&sm.mbar_kq[b], 0, 1u << 16), umma::mbar_wait(&sm.mbar_kq[b], 1, 1u << 16);
-        if (pend_am) umma::mbar_wait(&sm.mbar_am, 0, 1u << 16), umma::mbar_wait(&sm.mbar_am, 1, 1u << 16);
+    if (warp == kCopyWarp) {  // drain the copies into this CTA's shared memory (bounded)
+        asm volatile("cp.async.wait_all;" ::: "memory");
+        if (lane == 0) {
+            auto drain = [&](uint64_t* mb, int r) {
+                if ((used >> r) & 1u) umma::mbar_wait(mb, ((np >> r) & 1u) ^ 1u, 1u << 16);
+            };
+            drain(&sm.mb_kq, 0);
+            drain(&sm.mb_m, 1);
+            drain(&sm.mb_am, 2);
+        }
+        __syncwarp();
+    } else if (warp == kMmaWarp) {  // every MMA issued has completed (bounded)
+        if (lane == 0) {
+            umma::commit(&sm.mb_fin);
+            umma::mbar_wait(&sm.mb_fin, 0, 1u << 16);
+        }
+        __syncwarp();
+    } else {
+        asm volatile("cp.async.wait_all;" ::: "memory");  // no copy into this CTA's shared memory outlives it
     }
     umma::fence_before_sync();
     __syncthreads();
     if (warp == 0) umma::tmem_dealloc(sm.tmem_base, kTmemCols);
 #undef GDN_WAIT
-#undef GDN_SYNC_OR_ABORT
-#undef GDN_PUBLISH
 }
 
 }  // namespace
 
 size_t scan_workspace_bytes(int hk, int hv, int n_seq, int T)
 {
-    return kWsHeader + n_slots(T, n_seq) * ((size_t)hv * kAmBytes + (size_t)hk * (kKqBytes + kGramBytes));
+    return kWsHeader + n_slots(T, n_seq) * ((size_t)hv * kAmBlock + (size_t)hk * (kKqBytes + kGramBytes + kMBytes));
 }
 
 cudaError_t launch_scan(const ScanParams& p, cudaStream_t stream)

@@ -153,6 +153,22 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* mbar, uint32_t parity)
     return ok != 0;
 }
 
+// As mbar_try_wait, but the thread may be suspended for up to `hint_ns`
+// nanoseconds waiting for the phase, instead of polling: waiting warps then
+// take no issue or shared-memory slots from the warps doing work.
+__device__ __forceinline__ bool mbar_try_wait_suspend(uint64_t* mbar, uint32_t parity, uint32_t hint_ns)
+{
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(mbar)), "r"(parity), "r"(hint_ns)
+        : "memory");
+    return ok != 0;
+}
+
 // Bounded wait for phase `parity` of an mbarrier.  Returns false if the
 // barrier did not complete within `max_polls` polls (each poll itself blocks
 // for a hardware-defined time slice), so no caller can spin forever.
@@ -161,6 +177,12 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* mbar, uint32_t parity, uint3
     for (uint32_t i = 0; i < max_polls; ++i)
         if (mbar_try_wait(mbar, parity)) return true;
     return false;
+}
+
+// plain arrival (release at CTA scope)
+__device__ __forceinline__ void mbar_arrive(uint64_t* mbar)
+{
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(mbar)) : "memory");
 }
 
 // ---- bulk async copy global -> shared, completion counted on an mbarrier ------------
@@ -177,6 +199,12 @@ __device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t by
                  :
                  : "r"(smem_u32(dst)), "l"(src), "r"(bytes), "r"(smem_u32(mbar))
                  : "memory");
+}
+
+// global -> L2 only (no completion tracking); src 16-byte aligned, bytes a multiple of 16
+__device__ __forceinline__ void bulk_prefetch_l2(const void* src, uint32_t bytes)
+{
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
 }
 
 // ---- bf16 split: x ~= hi + lo with hi = bf16(x), lo = bf16(x - hi) --------------------
