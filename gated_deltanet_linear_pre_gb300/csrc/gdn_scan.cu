@@ -24,20 +24,20 @@
 //
 // Three kernels:
 //  * scan_gram_kernel, one CTA per (chunk, key head), fully parallel: splits
-//    [K; Q] into the tensor-core layout (the chain's [K; Q] image) and forms
-//    (K K^T ; Q K^T) in fp32.
-//  * scan_prep_kernel, one CTA per (chunk, key head), fully parallel: for each
-//    value head reading that key head, A and P, the inverse of I + A
-//    (recursive halving with 16x16 diagonal blocks by forward substitution,
-//    on CUDA cores) and P T on the tensor core; writes the [T; P T] image per
-//    (chunk, value head).
+//    [K; Q] into the tensor-core layout (the chain's [K; Q] image), forms
+//    (K K^T ; Q K^T) in fp32, and M = [K; Q] K_prev^T against the previous
+//    chunk's keys (the chain's look-ahead operand).
+//  * scan_prep_kernel, one CTA per (chunk, value head), fully parallel: A and
+//    P from the key head's gram rows and the head's gates, the inverse of
+//    I + A (recursive halving with 16x16 diagonal blocks by forward
+//    substitution, on CUDA cores) and P T on the tensor core; writes the
+//    [T; P T] image and the chain's gate row.
 //  * scan_chain_kernel, one CTA per (sequence, value head, 64-column slice):
 //    the state-dependent part, chunk after chunk, with the fp32 state slice
-//    in registers.  The images stream in with bulk asynchronous copies one
-//    chunk ahead ([K; Q] double-buffered), V and the gates through registers
-//    one chunk ahead, so each chunk costs three MMA groups and three short
-//    CUDA-core phases.  K^T for the state update is
-//    the K half of the [K; Q] image read through an MN-major descriptor.
+//    in registers.  The next chunk's [K; Q] S is split into a part issued a
+//    chunk early and a K = 64 correction through M, so the chunk-to-chunk path
+//    is two MMA groups and two short CUDA-core phases; one warp issues the
+//    MMAs, one the operand copies, sixteen do the CUDA-core work.
 //
 // Every MMA is issued by one thread and completes on an mbarrier; every wait
 // is bounded and, on expiry, the CTA records an error code in the workspace,
@@ -333,7 +333,7 @@ __global__ void __launch_bounds__(kGramThreads) scan_gram_kernel(ScanParams p)
 }
 
 // =======================================================================================
-// prep: one CTA per (chunk slot, key head); its value heads one after another
+// prep: one CTA per (chunk slot, value head)
 // =======================================================================================
 constexpr int kPrepThreads = 256;  // two warpgroups: each covers all 128 TMEM lanes, half the columns
 
@@ -355,8 +355,7 @@ __global__ void __launch_bounds__(kPrepThreads, 3) scan_prep_kernel(ScanParams p
     PrepSmem& sm = *reinterpret_cast<PrepSmem*>(smem_raw);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int L = tid & 127, wg = tid >> 7;  // TMEM lane, column half
-    const int slot = blockIdx.x, j = blockIdx.y;
-    const int group = p.hv / p.hk;
+    const int slot = blockIdx.x, h = blockIdx.y, j = h / (p.hv / p.hk);
     uint32_t* err = reinterpret_cast<uint32_t*>(p.workspace);
     constexpr int ST = 68;  // fp32 row stride of A and T
     int c0, n;
@@ -369,21 +368,18 @@ __global__ void __launch_bounds__(kPrepThreads, 3) scan_prep_kernel(ScanParams p
         umma::mbar_init(&sm.mbar, 1);
         sm.abort_flag = 0;
     }
-    // raw gates of a value head, loaded by warp 0 one head ahead
+    // raw gates of the value head (warp 0)
     float raw_lam[2] = {0.f, 0.f}, raw_beta[2] = {0.f, 0.f};
-    auto load_gates = [&](int h) {
-        if (warp == 0) {
+    if (warp == 0) {
 #pragma unroll
-            for (int q = 0; q < 2; ++q) {
-                const int t = lane + 32 * q;
-                raw_lam[q] = t < n ? __ldg(p.glog + (size_t)(c0 + t) * p.hv + h) : 0.0f;
-                raw_beta[q] = t < n ? __ldg(p.beta + (size_t)(c0 + t) * p.hv + h) : 0.0f;
-            }
+        for (int q = 0; q < 2; ++q) {
+            const int t = lane + 32 * q;
+            raw_lam[q] = t < n ? __ldg(p.glog + (size_t)(c0 + t) * p.hv + h) : 0.0f;
+            raw_beta[q] = t < n ? __ldg(p.beta + (size_t)(c0 + t) * p.hv + h) : 0.0f;
         }
-    };
-    load_gates(j * group);
-    // this thread's 32 entries of the gram rows: row L (K K^T for L < 64, Q K^T
-    // for L >= 64), columns [32 wg, 32 wg + 32); shared by all value heads
+    }
+    // this thread's 32 entries of the gram rows of the key head: row L (K K^T for
+    // L < 64, Q K^T for L >= 64), columns [32 wg, 32 wg + 32)
     float d[32];
     {
         const float4* src = reinterpret_cast<const float4*>(gram_rows(p, slot, j) + L * 64 + 32 * wg);
@@ -403,15 +399,13 @@ __global__ void __launch_bounds__(kPrepThreads, 3) scan_prep_kernel(ScanParams p
     float* A = sm.A;
     float* Tm = sm.T;
 
-    for (int hh = 0; hh < group; ++hh) {
-        const int h = j * group + hh;
+    {
         // gates of value head h: running log-decay G and beta
         if (warp == 0) {
             float lam[2];
 #pragma unroll
             for (int q = 0; q < 2; ++q) lam[q] = (lane + 32 * q) < n ? fmaxf(raw_lam[q], kLamFloor) : 0.0f;
             const float b0 = raw_beta[0], b1 = raw_beta[1];
-            if (hh + 1 < group) load_gates(h + 1);
             const float GL = warp_chunk_cumsum(lam, lane);
             sm.G[lane] = lam[0];
             sm.G[lane + 32] = lam[1];
@@ -1113,7 +1107,7 @@ cudaError_t launch_scan(const ScanParams& p, cudaStream_t stream)
         scan_gram_kernel<<<dim3((unsigned)slots, (unsigned)p.hk), kGramThreads, gram_smem, stream>>>(p);
         e = cudaGetLastError();
         if (e != cudaSuccess) return e;
-        scan_prep_kernel<<<dim3((unsigned)slots, (unsigned)p.hk), kPrepThreads, prep_smem, stream>>>(p);
+        scan_prep_kernel<<<dim3((unsigned)slots, (unsigned)p.hv), kPrepThreads, prep_smem, stream>>>(p);
         e = cudaGetLastError();
         if (e != cudaSuccess) return e;
     }
