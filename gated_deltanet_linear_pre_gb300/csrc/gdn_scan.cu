@@ -219,46 +219,58 @@ struct __align__(1024) GramSmem {
     uint64_t mbar;
 };
 
-// split 64 token rows x 128 fp32 of one key head into a K-major bf16 tile
-// (rows `row0 + t`), optionally mirroring the bytes to rows `img_row0 + t` of a
-// [K; Q] image
+// 64 token rows x 128 fp32 of one key head, 32 values per thread: unit u = tid + kThreads q
+// covers row t (8 rows per group of 8 core-matrix rows) and columns [8 g, 8 g + 8)
 template <int kThreads>
-__device__ __forceinline__ void load_split_rows(const float* src_base, size_t row_stride, int n, uint16_t* hi,
-                                                uint16_t* lo, int row0, int tile_k, unsigned char* img,
-                                                int img_row0, int tid)
-{
-    constexpr int kU = 64 * 16 / kThreads;
-    float4 ld[2 * kU];
+struct RowTile {
+    static constexpr int kU = 64 * 16 / kThreads;
+    float4 v[2 * kU];
+    __device__ __forceinline__ static void unit(int u, int& t, int& g)
+    {
+        const int tg = (u >> 7) & 7;
+        g = (u >> 3) & 15;
+        t = tg * 8 + (u & 7);
+    }
+    // issue the loads (rows t >= n read as zero)
+    __device__ __forceinline__ void fetch(const float* src_base, size_t row_stride, int n, int tid)
+    {
 #pragma unroll
-    for (int q = 0; q < kU; ++q) {
-        const int u = tid + kThreads * q;
-        const int tg = (u >> 7) & 7, g = (u >> 3) & 15, t = tg * 8 + (u & 7);
-        if (t < n) {
-            const float4* src = reinterpret_cast<const float4*>(src_base + (size_t)t * row_stride + g * 8);
-            ld[2 * q] = __ldg(src);
-            ld[2 * q + 1] = __ldg(src + 1);
-        } else {
-            ld[2 * q] = ld[2 * q + 1] = make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int q = 0; q < kU; ++q) {
+            int t, g;
+            unit(tid + kThreads * q, t, g);
+            if (t < n) {
+                const float4* src = reinterpret_cast<const float4*>(src_base + (size_t)t * row_stride + g * 8);
+                v[2 * q] = __ldg(src);
+                v[2 * q + 1] = __ldg(src + 1);
+            } else {
+                v[2 * q] = v[2 * q + 1] = make_float4(0.f, 0.f, 0.f, 0.f);
+            }
         }
     }
+    // split into a K-major bf16 tile (rows row0 + t), optionally mirrored to rows img_row0 + t of a
+    // [K; Q] image
+    __device__ __forceinline__ void store(uint16_t* hi, uint16_t* lo, int row0, int tile_k, unsigned char* img,
+                                          int img_row0, int tid) const
+    {
 #pragma unroll
-    for (int q = 0; q < kU; ++q) {
-        const int u = tid + kThreads * q;
-        const int tg = (u >> 7) & 7, g = (u >> 3) & 15, t = tg * 8 + (u & 7);
-        const float x[8] = {ld[2 * q].x, ld[2 * q].y, ld[2 * q].z, ld[2 * q].w,
-                            ld[2 * q + 1].x, ld[2 * q + 1].y, ld[2 * q + 1].z, ld[2 * q + 1].w};
-        uint4 vh, vl;
-        split8(x, vh, vl);
-        const int off = kmaj(row0 + t, g * 8, tile_k);
-        *reinterpret_cast<uint4*>(hi + off) = vh;
-        *reinterpret_cast<uint4*>(lo + off) = vl;
-        if (img) {
-            const int io = kq_off(img_row0 + t, g * 8);
-            *reinterpret_cast<uint4*>(img + io) = vh;
-            *reinterpret_cast<uint4*>(img + io + 2048) = vl;
+        for (int q = 0; q < kU; ++q) {
+            int t, g;
+            unit(tid + kThreads * q, t, g);
+            const float x[8] = {v[2 * q].x, v[2 * q].y, v[2 * q].z, v[2 * q].w,
+                                v[2 * q + 1].x, v[2 * q + 1].y, v[2 * q + 1].z, v[2 * q + 1].w};
+            uint4 vh, vl;
+            split8(x, vh, vl);
+            const int off = kmaj(row0 + t, g * 8, tile_k);
+            *reinterpret_cast<uint4*>(hi + off) = vh;
+            *reinterpret_cast<uint4*>(lo + off) = vl;
+            if (img) {
+                const int io = kq_off(img_row0 + t, g * 8);
+                *reinterpret_cast<uint4*>(img + io) = vh;
+                *reinterpret_cast<uint4*>(img + io + 2048) = vl;
+            }
         }
     }
-}
+};
 
 __global__ void __launch_bounds__(kGramThreads) scan_gram_kernel(ScanParams p)
 {
@@ -279,14 +291,17 @@ __global__ void __launch_bounds__(kGramThreads) scan_gram_kernel(ScanParams p)
     }
     const size_t rs = (size_t)p.hk * kHeadDim;
     unsigned char* img = kq_image(p, slot, j);
+    // K and Q loads in flight together, the previous chunk's K (always full) behind them;
     // image rows in the chunk's stacking order: [K; Q] for even chunks, [Q; K] for odd ones
-    load_split_rows<kGramThreads>(p.kn + (size_t)c0 * rs + (size_t)j * kHeadDim, rs, n, sm.akq[0], sm.akq[1], 0, 128,
-                                  img, odd ? 64 : 0, tid);
-    load_split_rows<kGramThreads>(p.qn + (size_t)c0 * rs + (size_t)j * kHeadDim, rs, n, sm.akq[0], sm.akq[1], 64, 128,
-                                  img, odd ? 0 : 64, tid);
-    if (has_prev)  // the previous chunk is always full
-        load_split_rows<kGramThreads>(p.kn + (size_t)(c0 - kChunk) * rs + (size_t)j * kHeadDim, rs, kChunk, sm.bkp[0],
-                                      sm.bkp[1], 0, 128, nullptr, 0, tid);
+    {
+        RowTile<kGramThreads> tk, tq;
+        tk.fetch(p.kn + (size_t)c0 * rs + (size_t)j * kHeadDim, rs, n, tid);
+        tq.fetch(p.qn + (size_t)c0 * rs + (size_t)j * kHeadDim, rs, n, tid);
+        tk.store(sm.akq[0], sm.akq[1], 0, 128, img, odd ? 64 : 0, tid);
+        if (has_prev) tk.fetch(p.kn + (size_t)(c0 - kChunk) * rs + (size_t)j * kHeadDim, rs, kChunk, tid);
+        tq.store(sm.akq[0], sm.akq[1], 64, 128, img, odd ? 0 : 64, tid);
+        if (has_prev) tk.store(sm.bkp[0], sm.bkp[1], 0, 128, nullptr, 0, tid);
+    }
     umma::fence_proxy_async();
     umma::fence_before_sync();
     __syncthreads();
@@ -427,8 +442,11 @@ __global__ void __launch_bounds__(kPrepThreads, 3) scan_prep_kernel(ScanParams p
             const int i = L & 63, cb = 32 * wg;
             const float Gi = sm.G[i];
             const float4* G4 = reinterpret_cast<const float4*>(sm.G + cb);
+            // (a warp's 32 rows lie in one half, so for rows < 32 the columns of wg = 1 are all above
+            // the diagonal: A's block there is never read, P's is zero)
             if (L < 64) {
                 const float bi = sm.beta[i];
+                if (cb <= i)
 #pragma unroll
                 for (int q = 0; q < 8; ++q) {
                     const float4 g = G4[q];
@@ -440,6 +458,12 @@ __global__ void __launch_bounds__(kPrepThreads, 3) scan_prep_kernel(ScanParams p
                         a[e] = jj < i ? bi * __expf(Gi - gg[e]) * d[4 * q + e] : 0.0f;
                     }
                     *reinterpret_cast<float4*>(&A[i * ST + cb + 4 * q]) = make_float4(a[0], a[1], a[2], a[3]);
+                }
+            } else if (cb > i) {
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    *reinterpret_cast<uint4*>(&sm.ap[0][kmaj(i, cb + 8 * q, 64)]) = make_uint4(0u, 0u, 0u, 0u);
+                    *reinterpret_cast<uint4*>(&sm.ap[1][kmaj(i, cb + 8 * q, 64)]) = make_uint4(0u, 0u, 0u, 0u);
                 }
             } else {
 #pragma unroll
