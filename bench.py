@@ -9,6 +9,7 @@ through the whole stack.  The 36 layers' inputs (~2.3 GB) are larger than
 the 129 MB L2, so no flush is needed between steps.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
+  python bench.py --mode decode [--batch B]   # one decode step per sequence
 
 Under torchrun (N > 1) every rank runs its own replica of the stack on its
 own GPU (weak scaling, no collective on the data path); rank 0 prints one
@@ -62,6 +63,8 @@ def parse():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--layers", type=int, default=LAYERS,
                     help="layers in the stack (fewer only for profiling captures; the metric is 36)")
+    ap.add_argument("--mode", default="prefill", choices=["prefill", "decode"])
+    ap.add_argument("--batch", type=int, default=256, help="sequences per decode step (--mode decode)")
     return ap.parse_args()
 
 
@@ -237,6 +240,96 @@ def run_reference(args, rank, world):
     return 0
 
 
+# ---- decode mode: one token per sequence through the 36-layer stack ------------------------------
+DECODE_METRIC = "GDN decode tokens/s (36 layers, one token per sequence, fused gdn_step)"
+
+
+def decode_bytes_per_layer(B: int) -> int:
+    """Algorithmic HBM bytes of one decode step of one layer for B sequences."""
+    per_seq = (C * 2 + 2 * C * 3 * 2 + 2 * HV * 2 + 2 * HV * DV * 2   # qkv, hist in+out, a, b, z, y
+               + 2 * HV * DK * DV * 4)                               # state in + out
+    return B * per_seq + C * 16 + 2 * HV * 4 + DV * 4                # + conv_w, A_log, dt_bias, gamma
+
+
+def run_decode(args, rank, world, local):
+    import torch
+    from gated_deltanet_linear_pre_gb300 import build as gbuild
+    import gated_deltanet_linear_pre_gb300 as gdn
+    gbuild.build()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    d = gdn.dims(HK, HV, DK, DV, 1e-6)
+    B, n_layers = args.batch, args.layers
+    with ThreadPoolExecutor(max_workers=min(16, os.cpu_count() or 1)) as ex:
+        layers_np = list(ex.map(lambda l: gin.decode_batch(B, l + 1000 * rank), range(n_layers)))
+    t = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to(dev)
+    devl = [dict(qkv=t(L.qkv), conv_w=t(L.conv_w), hist=t(L.hist), a=t(L.a), b=t(L.b), z=t(L.z),
+                 A_log=t(L.A_log), dt_bias=t(L.dt_bias), gamma=t(L.gamma), S0=t(L.S0)) for L in layers_np]
+    y = [torch.empty((B, HV, DV), device=dev, dtype=torch.float16) for _ in range(n_layers)]
+    hist_out = [torch.empty_like(x["hist"]) for x in devl]
+    S_out = [torch.empty_like(x["S0"]) for x in devl]
+    stream = torch.cuda.current_stream(dev)
+
+    def step(events=None):
+        for l, x in enumerate(devl):
+            if events is not None:
+                events[l][0].record(stream)
+            gdn.gdn_step(d, B, x["qkv"], x["conv_w"], x["hist"], hist_out[l], x["a"], x["b"], x["z"], x["A_log"],
+                         x["dt_bias"], x["gamma"], x["S0"], S_out[l], False, y[l])
+            if events is not None:
+                events[l][1].record(stream)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    barrier(world)
+    ev = [[[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(n_layers)]
+          for _ in range(args.steps)]
+    clocks = ClockSampler(local)
+    with clocks:
+        barrier(world)
+        torch.cuda.synchronize()
+        for k in range(args.steps):
+            step(ev[k])
+        torch.cuda.synchronize()
+    barrier(world)
+    total_ms = max_over_ranks(ev[0][0][0].elapsed_time(ev[-1][-1][1]), world)
+    launch_ms = sum(ev[k][l][0].elapsed_time(ev[k][l][1]) for k in range(args.steps)
+                    for l in range(n_layers)) / (args.steps * n_layers)
+    ms_per_step = total_ms / args.steps
+    value = world * B * args.steps / (total_ms / 1e3)  # new tokens through the whole stack per second
+    hbm_peak, _, peak_src = load_peaks()
+    nbytes = decode_bytes_per_layer(B)
+    gbs = nbytes / (launch_ms * 1e-3) / 1e9
+    roofline = {"bound": "hbm", "kernel": "gdn_step", "achieved": gbs, "peak": hbm_peak, "unit": "GB/s",
+                "frac": gbs / hbm_peak, "traffic": None, "alg_bytes_per_launch": nbytes,
+                "peak_source": f"{peak_src} (MEASURED_PEAKS.json hbm_gbs)" if peak_src == "measured" else "fallback"}
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        import oracle
+        oracle.build()
+        n_cpu = min(4, n_layers)
+        t0 = time.perf_counter()
+        for L in layers_np[:n_cpu]:
+            oracle.layer(L)
+        dt = time.perf_counter() - t0
+        cpu = {"value": B * n_cpu / dt / METRIC_LAYERS, "unit": "tokens/s", "cores": oracle.threads(),
+               "kind": "oracle", "sample": f"{n_cpu} of the 36 layers x {B} one-token sequences, fp64 oracle "
+                                           f"({dt:.1f} s wall), scaled to the 36-layer stack"}
+    if rank == 0:
+        line = {"metric": DECODE_METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+                "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
+                "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+                "config": {"workload": f"36 independent GDN layers x one decode step of {B} sequences "
+                                       "(hk=16, hv=48, dk=dv=128), fp16 activations, fp32 state, fp16 output",
+                           "layers": n_layers, "global_batch": world * B, "parallelism": f"replicas{world}",
+                           "l2": f"inputs larger than L2 ({n_layers * nbytes / 2**30:.1f} GB per step)"},
+                "roofline": roofline, "ms_per_launch": launch_ms, "cpu_baseline": cpu, "e2e": None,
+                "gpu_launches": n_layers * args.steps, "clocks": clocks.summary()}
+        print(json.dumps(line), flush=True)
+    return 0
+
+
 # ---- GPU arm ----------------------------------------------------------------------------------
 def main():
     args = parse()
@@ -251,6 +344,13 @@ def main():
             dist.init_process_group("nccl", device_id=torch.device("cuda", local))
     if args.impl == "reference":
         rc = run_reference(args, rank, world)
+        if world > 1:
+            import torch.distributed as dist
+            dist.destroy_process_group()
+        return rc
+
+    if args.mode == "decode":
+        rc = run_decode(args, rank, world, local)
         if world > 1:
             import torch.distributed as dist
             dist.destroy_process_group()
@@ -416,7 +516,8 @@ def main():
                 "config": {"workload": WORKLOAD, "layers": LAYERS, "seq_len": T, "global_batch": world,
                            "parallelism": f"replicas{world}", "l2": "inputs larger than L2 (36-layer set ~2.3 GB)"},
                 "roofline": roofline, "stages": stages, "cpu_baseline": cpu, "e2e": e2e,
-                "gpu_launches": 3 * LAYERS * args.steps, "clocks": clocks.summary()}
+                # per layer: pre, the scan's gram, prep and chain kernels, post
+                "gpu_launches": 5 * LAYERS * args.steps, "clocks": clocks.summary()}
         print(json.dumps(line), flush=True)
     if world > 1:
         import torch.distributed as dist

@@ -4,13 +4,13 @@ The product is the CUDA library libgdn.so (C ABI: include/gdn.h), built for
 sm_103a by ``gated_deltanet_linear_pre_gb300.build``.  This package re-exports
 its thin ctypes binding under the ABI's names:
 
-    gdn_pre, gdn_scan, gdn_post, gdn_layer,
+    gdn_pre, gdn_scan, gdn_scan_noalloc, gdn_post, gdn_layer, gdn_step,
     gdn_scan_workspace_bytes, gdn_layer_workspace_bytes, dims, GdnError
 
 ``inputs`` draws the seeded synthetic workloads.  Nothing here computes the
 method on the CPU.
 """
-_BINDING = ("gdn_pre", "gdn_scan", "gdn_scan_noalloc", "gdn_post", "gdn_layer", "gdn_scan_workspace_bytes",
+_BINDING = ("gdn_pre", "gdn_scan", "gdn_scan_noalloc", "gdn_post", "gdn_layer", "gdn_step", "gdn_scan_workspace_bytes",
             "gdn_layer_workspace_bytes", "dims", "gdn_dims", "GdnError", "lib", "library_path")
 
 __all__ = list(_BINDING) + ["inputs", "build"]

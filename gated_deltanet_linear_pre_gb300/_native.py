@@ -77,6 +77,8 @@ def lib():
             L.gdn_layer_workspace_bytes.argtypes = [D, _i32, _i32]
             L.gdn_layer.restype = ctypes.c_int
             L.gdn_layer.argtypes = [D, _i32, _i32] + [_p] * 13 + [_i32, _p, _p, _sz, _p]
+            L.gdn_step.restype = ctypes.c_int
+            L.gdn_step.argtypes = [D, _i32] + [_p] * 12 + [_i32, _p, _p]
             _lib = L
     return _lib
 
@@ -202,3 +204,20 @@ def gdn_layer(d: gdn_dims, cu_seqlens, total_tokens, qkv, conv_w, hist_in, hist_
                          _ptr(y, "y", ydt, (T, hv, dv)), _ptr(workspace, "workspace", torch.uint8),
                          workspace.numel() if workspace is not None else 0, _stream(stream))
     _check("gdn_layer", st)
+
+
+def gdn_step(d: gdn_dims, n_seq: int, qkv, conv_w, hist_in, hist_out, a, b, z, A_log, dt_bias, gamma, S_in, S_out,
+             out_f32: bool, y, stream=None):
+    """One decode step: one token per sequence (qkv [n_seq, C]) through pre, the recurrence and post."""
+    n = int(n_seq)
+    C, hv, dk, dv = _C(d), d.hv, d.dk, d.dv
+    f16, f32 = torch.float16, torch.float32
+    ydt = f32 if out_f32 else f16
+    st = lib().gdn_step(ctypes.byref(d), n, _ptr(qkv, "qkv", f16, (n, C)), _ptr(conv_w, "conv_w", f32, (C, 4)),
+                        _ptr(hist_in, "hist_in", f16, (n, C, 3)), _ptr(hist_out, "hist_out", f16, (n, C, 3)),
+                        _ptr(a, "a", f16, (n, hv)), _ptr(b, "b", f16, (n, hv)), _ptr(z, "z", f16, (n, hv, dv)),
+                        _ptr(A_log, "A_log", f32, (hv,)), _ptr(dt_bias, "dt_bias", f32, (hv,)),
+                        _ptr(gamma, "gamma", f32, (dv,)), _ptr(S_in, "S_in", f32, (n, hv, dk, dv)),
+                        _ptr(S_out, "S_out", f32, (n, hv, dk, dv)), 1 if out_f32 else 0,
+                        _ptr(y, "y", ydt, (n, hv, dv)), _stream(stream))
+    _check("gdn_step", st)

@@ -335,3 +335,51 @@ gdn_status gdn_layer(const gdn_dims* dims, int32_t n_seq, int32_t T, const int32
 }
 
 }  // extern "C"
+
+extern "C" {
+
+gdn_status gdn_step(const gdn_dims* dims, int32_t n_seq, const uint16_t* qkv, const float* conv_w,
+                    const uint16_t* hist_in, uint16_t* hist_out, const uint16_t* a, const uint16_t* b,
+                    const uint16_t* z, const float* A_log, const float* dt_bias, const float* gamma,
+                    const float* S_in, float* S_out, int32_t out_f32, void* y, struct CUstream_st* stream)
+{
+    gdn_status st;
+    if ((st = check_dims(dims)) != GDN_OK) return st;
+    if (n_seq < 0) return fail(GDN_ERR_INVALID_ARG, "negative n_seq");
+    if (n_seq > 65535) return fail(GDN_ERR_UNSUPPORTED, "n_seq=%d above 65535", n_seq);
+    if (out_f32 != 0 && out_f32 != 1) return fail(GDN_ERR_INVALID_ARG, "out_f32 must be 0 or 1");
+    const size_t C = (size_t)channels(dims), hv = dims->hv, d = dims->dk, ns = (size_t)n_seq;
+    const Buf bufs[] = {
+        {qkv, ns * C * 2, "qkv"},          {conv_w, C * 16, "conv_w"},
+        {hist_in, ns * C * 6, "hist_in"},  {a, ns * hv * 2, "a"},
+        {b, ns * hv * 2, "b"},             {z, ns * hv * d * 2, "z"},
+        {A_log, hv * 4, "A_log"},          {dt_bias, hv * 4, "dt_bias"},
+        {gamma, d * 4, "gamma"},           {S_in, ns * hv * d * d * 4, "S_in"},
+        {hist_out, ns * C * 6, "hist_out"}, {S_out, ns * hv * d * d * 4, "S_out"},
+        {y, ns * hv * d * (out_f32 ? 4 : 2), "y"},
+    };
+    if ((st = check_bufs(bufs, sizeof bufs / sizeof bufs[0])) != GDN_OK) return st;
+    if (bufs[9].p != bufs[11].p && overlap(bufs[9], bufs[11]))
+        return fail(GDN_ERR_INVALID_ARG, "S_out partially overlaps S_in (identical buffers are allowed)");
+    const Buf ins[] = {bufs[0], bufs[1], bufs[2], bufs[3], bufs[4], bufs[5], bufs[6], bufs[7], bufs[8]};
+    const Buf outs[] = {bufs[10], bufs[11], bufs[12]};
+    if ((st = check_disjoint(outs, 3, ins, 9)) != GDN_OK) return st;
+    if (overlap(bufs[10], bufs[9]) || overlap(bufs[12], bufs[9]))
+        return fail(GDN_ERR_INVALID_ARG, "hist_out or y overlaps S_in");
+    if (n_seq == 0) return GDN_OK;
+    gdn::StepParams p{};
+    p.hk = dims->hk; p.hv = dims->hv; p.C = (int)C; p.n_seq = n_seq; p.eps = dims->eps;
+    p.qkv = reinterpret_cast<const __half*>(qkv);
+    p.conv_w = conv_w;
+    p.hist_in = reinterpret_cast<const __half*>(hist_in);
+    p.hist_out = reinterpret_cast<__half*>(hist_out);
+    p.a = reinterpret_cast<const __half*>(a);
+    p.b = reinterpret_cast<const __half*>(b);
+    p.z = reinterpret_cast<const __half*>(z);
+    p.A_log = A_log; p.dt_bias = dt_bias; p.gamma = gamma;
+    p.S_in = S_in; p.S_out = S_out; p.out_f32 = out_f32; p.y = y;
+    cudaError_t e = gdn::launch_step(p, reinterpret_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? GDN_OK : cuda_fail(e, "gdn_step launch");
+}
+
+}  // extern "C"

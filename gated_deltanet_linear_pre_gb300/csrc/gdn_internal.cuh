@@ -55,7 +55,28 @@ struct PostParams {
     void* y;
 };
 
+// one decode step: one token per sequence, the three stages fused
+struct StepParams {
+    int hk, hv, C, n_seq;
+    float eps;
+    const __half* qkv;      // [n_seq][C]
+    const float* conv_w;    // [C][4]
+    const __half* hist_in;  // [n_seq][C][3]
+    __half* hist_out;
+    const __half* a;        // [n_seq][hv]
+    const __half* b;
+    const __half* z;        // [n_seq][hv][dv]
+    const float* A_log;
+    const float* dt_bias;
+    const float* gamma;
+    const float* S_in;      // [n_seq][hv][dk][dv]
+    float* S_out;
+    int out_f32;
+    void* y;                // [n_seq][hv][dv]
+};
+
 cudaError_t launch_pre(const PreParams& p, cudaStream_t stream);
+cudaError_t launch_step(const StepParams& p, cudaStream_t stream);
 size_t scan_workspace_bytes(int hk, int hv, int n_seq, int T);
 cudaError_t launch_scan(const ScanParams& p, cudaStream_t stream);
 cudaError_t launch_post(const PostParams& p, cudaStream_t stream);

@@ -125,3 +125,9 @@ def varlen_batch(n_seq: int = 8, max_len: int = 4096, out_f32: bool = False) -> 
 def long_prompt(T: int = 32768, out_f32: bool = False) -> LayerInputs:
     """One long sequence with decays near 1: A_log = log U(0.01, 0.1)."""
     return make_layer(BASE_SEED, [T], A_log_range=(0.01, 0.1), out_f32=out_f32)
+
+
+def decode_batch(n_seq: int = 256, layer: int = 0, out_f32: bool = False) -> LayerInputs:
+    """One decode step for n_seq sequences: one token each, carried history and
+    state from earlier tokens (nonzero history, S0 ~ N(0, 0.02))."""
+    return make_layer(BASE_SEED + 1000 + layer, [1] * n_seq, hist_nonzero=True, S0_std=0.02, out_f32=out_f32)

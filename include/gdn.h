@@ -18,6 +18,7 @@
  *               o = S^T q / sqrt(dk).
  *   gdn_post  y = o / sqrt(mean(o^2) + eps) * gamma * SiLU(z), fp16 or fp32.
  *   gdn_layer the three stages back to back on one stream.
+ *   gdn_step  one decode step (a single token per sequence) through all three.
  *
  * Conventions shared by every entry point
  * ----------------------------------------
@@ -209,6 +210,37 @@ GDN_API gdn_status gdn_layer(const gdn_dims* dims, int32_t n_seq, int32_t total_
                      const float* dt_bias, const float* gamma, const float* S_in, float* S_out,
                      int32_t out_f32, void* y, void* workspace, size_t workspace_bytes,
                      struct CUstream_st* stream);
+
+/*
+ * gdn_step -- one decode step: a single new token for each of n_seq
+ * sequences through the whole layer (pre, the recurrence for that token, and
+ * post), fused into one launch.  Per token it computes exactly what gdn_layer
+ * computes for a batch in which every sequence holds one token: the
+ * token-sequential recurrence of "Round 30 Track C Audit: gdn_pre, gdn_post,
+ * and gdn_scanr_4", section 1 (gdn_scan_r's per-token decay, delta update and
+ * k/q products against the fp32 state), with that section's pre and post
+ * arithmetic for the token.
+ *
+ * In:  qkv      fp16 [n_seq][C]         the token's raw projections, q | k | v
+ *      conv_w   fp32 [C][4]             as for gdn_pre
+ *      hist_in  fp16 [n_seq][C][3]      the 3 inputs before the token, oldest first
+ *      a, b     fp16 [n_seq][hv]        gate pre-activations
+ *      z        fp16 [n_seq][hv][dv]    output gate
+ *      A_log, dt_bias fp32 [hv];  gamma fp32 [dv]
+ *      S_in     fp32 [n_seq][hv][dk][dv]  state before the token
+ * Out: hist_out fp16 [n_seq][C][3]      history after the token (slots 1, 2 of
+ *                                       hist_in, then the token); bit copies.
+ *                                       Must not overlap any input.
+ *      S_out    fp32 [n_seq][hv][dk][dv]  state after the token; may be the same
+ *                                       buffer as S_in (not a partial overlap)
+ *      y        fp16 [n_seq][hv][dv] when out_f32 == 0, else fp32
+ * No workspace.  n_seq == 0 is a no-op.  Errors as for the other entry points.
+ */
+GDN_API gdn_status gdn_step(const gdn_dims* dims, int32_t n_seq, const uint16_t* qkv, const float* conv_w,
+                            const uint16_t* hist_in, uint16_t* hist_out, const uint16_t* a,
+                            const uint16_t* b, const uint16_t* z, const float* A_log,
+                            const float* dt_bias, const float* gamma, const float* S_in, float* S_out,
+                            int32_t out_f32, void* y, struct CUstream_st* stream);
 
 #ifdef __cplusplus
 }

@@ -27,7 +27,7 @@ def declared_symbols():
 
 def test_header_declares_the_boundary():
     syms = declared_symbols()
-    for name in ("gdn_pre", "gdn_scan", "gdn_post", "gdn_layer", "gdn_scan_workspace_bytes",
+    for name in ("gdn_pre", "gdn_scan", "gdn_post", "gdn_layer", "gdn_step", "gdn_scan_workspace_bytes",
                  "gdn_layer_workspace_bytes", "gdn_status_string", "gdn_last_error_string"):
         assert name in syms
 
@@ -126,6 +126,31 @@ def test_post_rejects_bad_arguments(L):
     assert L.gdn_post(ctypes.byref(d), 4, FAKE, 2 * FAKE, 3 * FAKE, 0, FAKE, None) == 1
     assert L.gdn_post(ctypes.byref(d), -1, FAKE, 2 * FAKE, 3 * FAKE, 0, 4 * FAKE, None) == 1
     assert L.gdn_post(ctypes.byref(d), 4, FAKE + 4, 2 * FAKE, 3 * FAKE, 0, 4 * FAKE, None) == 3
+
+
+def test_step_rejects_bad_arguments(L):
+    from gated_deltanet_linear_pre_gb300 import _native as N
+    d = N.dims()
+    F = 1 << 26  # buffers 64 MB apart: no accidental overlap
+    # qkv conv_w hist_in hist_out a b z A_log dt_bias gamma S_in S_out y
+    good = [F * (i + 1) for i in range(13)]
+
+    def call(n_seq=2, out_f32=0, **kw):
+        names = ["qkv", "conv_w", "hist_in", "hist_out", "a", "b", "z", "A_log", "dt_bias", "gamma", "S_in",
+                 "S_out", "y"]
+        ptrs = [kw.get(nm, good[i]) for i, nm in enumerate(names)]
+        return L.gdn_step(ctypes.byref(d), n_seq, *ptrs[:12], out_f32, ptrs[12], None)
+
+    assert call(n_seq=-1) == 1
+    assert call(out_f32=2) == 1
+    assert call(qkv=None) == 1
+    assert call(z=good[6] + 8) == 3
+    assert call(hist_out=good[2]) == 1             # history in place is not allowed
+    assert "overlaps" in L.gdn_last_error_string().decode()
+    assert call(S_out=good[10] + 16) == 1          # partial state overlap
+    assert call(y=good[11]) == 1                   # y overlaps S_out
+    assert L.gdn_step(None, 2, *good[:12], 0, good[12], None) == 1
+    assert call(n_seq=0) == 0                      # empty batch: nothing to do
 
 
 def test_layer_rejects_small_workspace(L):
