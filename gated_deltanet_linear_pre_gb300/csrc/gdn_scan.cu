@@ -354,9 +354,11 @@ constexpr int kPrepThreads = 256;  // two warpgroups: each covers all 128 TMEM l
 
 struct __align__(1024) PrepSmem {
     uint16_t ap[2][64 * 64];   // P (K-major, 64 rows); an M = 128 descriptor reads its rows 64-127 from
-    uint16_t bt[2][64 * 64];   //   the next 16 KB (here), whose products are never read
-    float A[64 * 68];          // fp32 A and T (rows padded to 68 floats)
-    float T[64 * 68];
+    union {                    //   the next 16 KB (here), whose products are never read
+        float A[64 * 68];      // fp32 A (rows padded to 68 floats), until the solve is done
+        uint16_t bt[2][64 * 64];  // then T split (MN-major B tile)
+    } u;
+    float T[64 * 68];          // fp32 T
     float W[32 * 32];          // off-diagonal block products of the solve
     float G[64], beta[64];
     uint32_t tmem_base;
@@ -364,7 +366,7 @@ struct __align__(1024) PrepSmem {
     uint64_t mbar;
 };
 
-__global__ void __launch_bounds__(kPrepThreads, 3) scan_prep_kernel(ScanParams p)
+__global__ void __launch_bounds__(kPrepThreads, 4) scan_prep_kernel(ScanParams p)
 {
     extern __shared__ __align__(1024) unsigned char smem_raw[];
     PrepSmem& sm = *reinterpret_cast<PrepSmem*>(smem_raw);
@@ -409,9 +411,9 @@ __global__ void __launch_bounds__(kPrepThreads, 3) scan_prep_kernel(ScanParams p
     const uint32_t tmem = sm.tmem_base;
     const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
     const uint32_t a_p[2] = {umma::smem_u32(sm.ap[0]), umma::smem_u32(sm.ap[1])};
-    const uint32_t b_t[2] = {umma::smem_u32(sm.bt[0]), umma::smem_u32(sm.bt[1])};
+    const uint32_t b_t[2] = {umma::smem_u32(sm.u.bt[0]), umma::smem_u32(sm.u.bt[1])};
     uint32_t phase = 0;
-    float* A = sm.A;
+    float* A = sm.u.A;
     float* Tm = sm.T;
 
     {
@@ -572,7 +574,7 @@ __global__ void __launch_bounds__(kPrepThreads, 3) scan_prep_kernel(ScanParams p
 #pragma unroll
                     for (int e = 0; e < 8; ++e) tr[e] = 0.0f;
                 }
-                store_split8(&sm.bt[0][mnmaj(g * 8, m, 64)], &sm.bt[1][mnmaj(g * 8, m, 64)], tr);
+                store_split8(&sm.u.bt[0][mnmaj(g * 8, m, 64)], &sm.u.bt[1][mnmaj(g * 8, m, 64)], tr);
             }
         }
         umma::fence_proxy_async();
@@ -592,35 +594,35 @@ __global__ void __launch_bounds__(kPrepThreads, 3) scan_prep_kernel(ScanParams p
         if (sm.abort_flag) goto done;
         umma::fence_after_sync();
 
-        // [T; P T] image (K-major, split; [P T; T] for odd chunks): threads L >= 64 write T row
-        // L - 64 (from shared memory), threads L < 64 write P T row L (from TMEM lane L); columns of wg
+        // [T; P T] image (K-major, split; [P T; T] for odd chunks): threads L >= 64 copy T row L - 64
+        // from the split T tile (its 8-column groups are contiguous there), threads L < 64 split and
+        // write P T row L from TMEM lane L; columns of wg
         {
             unsigned char* img = am_image(p, slot, h);
             const int cb = 32 * wg;
-            float x[32];
-            int row;
             if (L < 64) {
+                float x[32];
                 umma::tmem_ld32(tmem + lane_off + cb, x);
                 umma::tmem_wait_ld();
-                row = 64 + L;
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    uint4 vh, vl;
+                    split8(x + 8 * q, vh, vl);
+                    const int off = kmaj(odd ? L : 64 + L, cb + 8 * q, 64);
+                    *reinterpret_cast<uint4*>(img + off * 2) = vh;
+                    *reinterpret_cast<uint4*>(img + kAmBytes / 2 + off * 2) = vl;
+                }
             } else {
                 const int m = L - 64;
 #pragma unroll
-                for (int q = 0; q < 8; ++q) {
-                    const int g = (cb + 4 * q) >> 3;
-                    float4 t4 = make_float4(0.f, 0.f, 0.f, 0.f);
-                    if ((g >> 1) <= (m >> 4)) t4 = *reinterpret_cast<const float4*>(&Tm[m * ST + cb + 4 * q]);
-                    x[4 * q] = t4.x; x[4 * q + 1] = t4.y; x[4 * q + 2] = t4.z; x[4 * q + 3] = t4.w;
+                for (int q = 0; q < 4; ++q) {
+                    const int e = mnmaj(cb + 8 * q, m, 64);
+                    const uint4 vh = *reinterpret_cast<const uint4*>(&sm.u.bt[0][e]);
+                    const uint4 vl = *reinterpret_cast<const uint4*>(&sm.u.bt[1][e]);
+                    const int off = kmaj(odd ? 64 + m : m, cb + 8 * q, 64);
+                    *reinterpret_cast<uint4*>(img + off * 2) = vh;
+                    *reinterpret_cast<uint4*>(img + kAmBytes / 2 + off * 2) = vl;
                 }
-                row = m;
-            }
-#pragma unroll
-            for (int q = 0; q < 4; ++q) {
-                uint4 vh, vl;
-                split8(x + 8 * q, vh, vl);
-                const int off = kmaj(odd ? (row ^ 64) : row, cb + 8 * q, 64);
-                *reinterpret_cast<uint4*>(img + off * 2) = vh;
-                *reinterpret_cast<uint4*>(img + kAmBytes / 2 + off * 2) = vl;
             }
         }
         umma::fence_before_sync();
