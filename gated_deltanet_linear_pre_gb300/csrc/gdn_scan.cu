@@ -112,16 +112,21 @@ __device__ __forceinline__ void mma_split(uint32_t d, uint32_t a_hi, uint32_t a_
 // D[:, 0:N] += A_lo B_hi, so D[:, 0:N] + D[:, N:2N] = A B to ~16 bits.  Needs B_lo
 // to follow B_hi directly along N in shared memory (b_hilo is the start of
 // both).  Two thirds of the instructions of mma_split for the same tensor work.
-__device__ __forceinline__ void mma_split2(uint32_t d, uint32_t a_hi, uint32_t a_lo, uint32_t a_lbo, uint32_t a_sbo,
-                                           uint32_t a_kstep, uint32_t b_hilo, uint32_t b_sbo, uint32_t b_kstep,
-                                           int ksteps, int N, bool a_mn, bool b_mn, bool acc = false)
+// The K-step count and every stride are compile-time constants so that the
+// issuing thread spends as few instructions as possible per MMA.
+template <int KSTEPS, int N, uint32_t A_LBO, uint32_t A_SBO, uint32_t A_KSTEP, uint32_t B_SBO, uint32_t B_KSTEP,
+          bool A_MN, bool B_MN, bool ACC = false>
+__device__ __forceinline__ void mma_split2(uint32_t d, uint32_t a_hi, uint32_t a_lo, uint32_t b_hilo)
 {
-    const uint64_t dah = umma::desc(a_hi, a_lbo, a_sbo), dal = umma::desc(a_lo, a_lbo, a_sbo);
-    const uint64_t db = umma::desc(b_hilo, 128, b_sbo);
-    const uint64_t sa = a_kstep >> 4, sb = b_kstep >> 4;
-    const uint32_t wide = umma::idesc_bf16(128, 2 * N, a_mn, b_mn), narrow = umma::idesc_bf16(128, N, a_mn, b_mn);
-    for (int ks = 0; ks < ksteps; ++ks) umma::mma_bf16(d, dah + ks * sa, db + ks * sb, wide, acc || ks != 0);
-    for (int ks = 0; ks < ksteps; ++ks) umma::mma_bf16(d, dal + ks * sa, db + ks * sb, narrow, 1u);
+    const uint64_t dah = umma::desc(a_hi, A_LBO, A_SBO), dal = umma::desc(a_lo, A_LBO, A_SBO);
+    const uint64_t db = umma::desc(b_hilo, 128, B_SBO);
+    constexpr uint32_t wide = umma::idesc_bf16(128, 2 * N, A_MN, B_MN), narrow = umma::idesc_bf16(128, N, A_MN, B_MN);
+#pragma unroll
+    for (int ks = 0; ks < KSTEPS; ++ks)
+        umma::mma_bf16(d, dah + ks * (A_KSTEP >> 4), db + ks * (B_KSTEP >> 4), wide, (ACC || ks != 0) ? 1u : 0u);
+#pragma unroll
+    for (int ks = 0; ks < KSTEPS; ++ks)
+        umma::mma_bf16(d, dal + ks * (A_KSTEP >> 4), db + ks * (B_KSTEP >> 4), narrow, 1u);
 }
 
 // Chunk slots: sequence s owns slots [base(s), base(s) + ceil(len_s / 64)) with
@@ -798,7 +803,17 @@ __global__ void __launch_bounds__(kChainThreads, 1) scan_chain_kernel(ScanParams
             load_kq(0);
             load_am(0);
         }
+        // [K; Q] and [T; P T] images of chunk c -> L2 two chunks ahead: their copies are issued only
+        // as buffers free up, often too late to ride out DRAM latency
+        auto prefetch_l2 = [&](int c) {
+            if (leader && c < n_chunks) {
+                umma::bulk_prefetch_l2(kq_image(p, base + c, j), (uint32_t)kKqBytes);
+                umma::bulk_prefetch_l2(am_image(p, base + c, h), (uint32_t)(kAmBytes + sizeof(ChainGates)));
+            }
+        };
+        prefetch_l2(1);
         for (int c = 0; c + 1 < n_chunks; ++c) {
+            prefetch_l2(c + 2);
             // R1 (Q_c) and M free once (K S ; Q S) of chunk c is complete; the slot of K_{c-1}
             // once that chunk's state update is done
             GDN_WAIT(&sm.mb_f, c & 1);
@@ -837,7 +852,7 @@ __global__ void __launch_bounds__(kChainThreads, 1) scan_chain_kernel(ScanParams
             GDN_WAIT(&sm.mb_kq, 0);
             umma::fence_after_sync();
             if (leader) {
-                mma_split2(tmem + cD2, kh0, kh0 + 2048, 128, 4096, 256, b_s, 2048, 256, 8, DVS, false, true);
+                mma_split2<8, DVS, 128, 4096, 256, 2048, 256, false, true>(tmem + cD2, kh0, kh0 + 2048, b_s);
                 umma::commit(&sm.mb_f);
             }
             __syncwarp();
@@ -849,7 +864,7 @@ __global__ void __launch_bounds__(kChainThreads, 1) scan_chain_kernel(ScanParams
             GDN_WAIT(&sm.mb_am, c & 1);
             umma::fence_after_sync();
             if (leader) {
-                mma_split2(tmem + cD3, a_t_hi, a_t_lo, 128, 1024, 256, b_x, 1024, 256, 4, DVS, false, true);
+                mma_split2<4, DVS, 128, 1024, 256, 1024, 256, false, true>(tmem + cD3, a_t_hi, a_t_lo, b_x);
                 umma::commit(&sm.mb_d3);
             }
             __syncwarp();
@@ -860,7 +875,7 @@ __global__ void __launch_bounds__(kChainThreads, 1) scan_chain_kernel(ScanParams
                 umma::fence_after_sync();
                 const uint32_t a = kh0 + ((c + 1) & 1) * kSlotBytes;  // stacked from R1 (odd) or R0 (even)
                 if (leader)
-                    mma_split2(tmem + cD2, a, a + 2048, 128, 4096, 256, b_s, 2048, 256, 8, DVS, false, true);
+                    mma_split2<8, DVS, 128, 4096, 256, 2048, 256, false, true>(tmem + cD2, a, a + 2048, b_s);
                 __syncwarp();
             }
             // U'_c published: M_{c+1} U'_c on top (the chunk-to-chunk path), then K_c^T U'_c
@@ -869,12 +884,12 @@ __global__ void __launch_bounds__(kChainThreads, 1) scan_chain_kernel(ScanParams
             umma::fence_after_sync();
             if (leader) {
                 if (more) {
-                    mma_split2(tmem + cD2, a_m_hi, a_m_lo, 128, 1024, 256, b_u, 1024, 256, 4, DVS, false, true, true);
+                    mma_split2<4, DVS, 128, 1024, 256, 1024, 256, false, true, true>(tmem + cD2, a_m_hi, a_m_lo, b_u);
                     umma::commit(&sm.mb_f);
                 }
                 // K_c^T: MN-major view of the K half (token groups 4 KB apart, key groups 128 B)
                 const uint32_t kb = kh0 + kslot(c) * kSlotBytes;
-                mma_split2(tmem + cD4, kb, kb + 2048, 4096, 128, 8192, b_u, 1024, 256, 4, DVS, true, true);
+                mma_split2<4, DVS, 4096, 128, 8192, 1024, 256, true, true>(tmem + cD4, kb, kb + 2048, b_u);
                 umma::commit(&sm.mb_d4);
             }
             __syncwarp();
