@@ -204,3 +204,16 @@ def test_layer_long_prompt_decays_near_one():
     # T = 32768, g close to 1: fp32 state accumulation over the whole prompt,
     # final state and sampled heads' outputs against the fp64 oracle
     _check_layer(gin.long_prompt(), heads=list(range(0, 48, 5)))
+
+
+@pytest.mark.parametrize("hk,hv", [(2, 2), (4, 8), (2, 8)])
+def test_layer_other_head_counts(hk, hv):
+    # value heads per key head of 1, 2 and 4 (the pages' layer has 3): key/value head
+    # indexing of every stage, on a varlen batch that spans odd and even chunk indices
+    u = U()
+    inp = gin.make_layer(70 + hk * 10 + hv, [200, 0, 1, 130], hist_nonzero=True, S0_std=0.02, dims=(hk, hv, 128, 128))
+    ref = oracle.layer(inp, hk=hk, hv=hv)
+    got = u.run_layer(inp)
+    assert u.max_rel(got["y"], ref["y"]) <= u.TOL_F16
+    assert u.max_rel(got["S_out"], ref["S_out"]) <= u.TOL_F32
+    np.testing.assert_array_equal(got["hist_out"].view(np.uint16), inp_hist_bits(ref["hist_out"]))

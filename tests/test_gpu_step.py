@@ -129,3 +129,14 @@ def test_step_empty_batch_is_a_no_op():
                  e16(0, 48, 128), u.dev(inp.A_log), u.dev(inp.dt_bias), u.dev(inp.gamma), e32(0, 48, 128, 128),
                  e32(0, 48, 128, 128), False, e16(0, 48, 128))
     torch.cuda.synchronize()
+
+
+@pytest.mark.parametrize("hk,hv", [(2, 2), (4, 8), (2, 8)])
+def test_step_other_head_counts(hk, hv):
+    import gpu_util as u
+    inp = gin.make_layer(80 + hk * 10 + hv, [1] * 9, hist_nonzero=True, S0_std=0.02, dims=(hk, hv, 128, 128))
+    ref = oracle.layer(inp, hk=hk, hv=hv)
+    got = run_step(inp)
+    assert u.max_rel(got["y"], ref["y"]) <= u.TOL_F16
+    assert u.max_rel(got["S_out"], ref["S_out"]) <= u.TOL_F32
+    np.testing.assert_array_equal(got["hist_out"].view(np.uint16), _hist_bits(ref["hist_out"]))
