@@ -26,7 +26,7 @@ _i32 = ctypes.c_int32
 _sz = ctypes.c_size_t
 
 STATUS = {0: "GDN_OK", 1: "GDN_ERR_INVALID_ARG", 2: "GDN_ERR_UNSUPPORTED", 3: "GDN_ERR_ALIGNMENT",
-          4: "GDN_ERR_WORKSPACE", 5: "GDN_ERR_CUDA"}
+          4: "GDN_ERR_WORKSPACE", 5: "GDN_ERR_CUDA", 6: "GDN_ERR_TIMEOUT"}
 
 
 class GdnError(RuntimeError):
@@ -77,6 +77,12 @@ def lib():
             L.gdn_layer_workspace_bytes.argtypes = [D, _i32, _i32]
             L.gdn_layer.restype = ctypes.c_int
             L.gdn_layer.argtypes = [D, _i32, _i32] + [_p] * 13 + [_i32, _p, _p, _sz, _p]
+            L.gdn_scan_check.restype = ctypes.c_int
+            L.gdn_scan_check.argtypes = [_p, _p]
+            L.gdn_layer_check.restype = ctypes.c_int
+            L.gdn_layer_check.argtypes = [D, _i32, _i32, _p, _p]
+            L.gdn_scan_selftest_timeout.restype = ctypes.c_int
+            L.gdn_scan_selftest_timeout.argtypes = [D, _i32, _i32] + [_p] * 10 + [_sz, _p]
             L.gdn_step.restype = ctypes.c_int
             L.gdn_step.argtypes = [D, _i32] + [_p] * 12 + [_i32, _p, _p]
             _lib = L
@@ -221,3 +227,31 @@ def gdn_step(d: gdn_dims, n_seq: int, qkv, conv_w, hist_in, hist_out, a, b, z, A
                         _ptr(S_out, "S_out", f32, (n, hv, dk, dv)), 1 if out_f32 else 0,
                         _ptr(y, "y", ydt, (n, hv, dv)), _stream(stream))
     _check("gdn_step", st)
+
+
+def gdn_scan_check(workspace, stream=None):
+    """Raise GdnError (GDN_ERR_TIMEOUT) if the last scan on this workspace reported an expired wait;
+    synchronises the stream."""
+    _check("gdn_scan_check", lib().gdn_scan_check(_ptr(workspace, "workspace", torch.uint8), _stream(stream)))
+
+
+def gdn_layer_check(d: gdn_dims, n_seq: int, total_tokens: int, workspace, stream=None):
+    """As gdn_scan_check for a gdn_layer workspace."""
+    _check("gdn_layer_check", lib().gdn_layer_check(ctypes.byref(d), int(n_seq), int(total_tokens),
+                                                    _ptr(workspace, "workspace", torch.uint8), _stream(stream)))
+
+
+def gdn_scan_selftest_timeout(d: gdn_dims, cu_seqlens, total_tokens, qn, kn, vc, glog, beta, S_in, S_out, o,
+                              workspace, stream=None):
+    """Test hook of the failure report: gdn_scan with one operand copy withheld (outputs invalid)."""
+    n_seq, T = _batch(cu_seqlens, total_tokens)
+    hk, hv, dk, dv = d.hk, d.hv, d.dk, d.dv
+    f32 = torch.float32
+    st = lib().gdn_scan_selftest_timeout(
+        ctypes.byref(d), n_seq, T, _ptr(cu_seqlens, "cu_seqlens", torch.int32), _ptr(qn, "qn", f32, (T, hk, dk)),
+        _ptr(kn, "kn", f32, (T, hk, dk)), _ptr(vc, "vc", f32, (T, hv, dv)), _ptr(glog, "glog", f32, (T, hv)),
+        _ptr(beta, "beta", f32, (T, hv)), _ptr(S_in, "S_in", f32, (n_seq, hv, dk, dv)),
+        _ptr(S_out, "S_out", f32, (n_seq, hv, dk, dv)), _ptr(o, "o", f32, (T, hv, dv)),
+        _ptr(workspace, "workspace", torch.uint8), workspace.numel() if workspace is not None else 0,
+        _stream(stream))
+    _check("gdn_scan_selftest_timeout", st)

@@ -115,6 +115,7 @@ const char* gdn_status_string(gdn_status s)
     case GDN_ERR_ALIGNMENT: return "GDN_ERR_ALIGNMENT";
     case GDN_ERR_WORKSPACE: return "GDN_ERR_WORKSPACE";
     case GDN_ERR_CUDA: return "GDN_ERR_CUDA";
+    case GDN_ERR_TIMEOUT: return "GDN_ERR_TIMEOUT";
     }
     return "GDN_ERR_UNKNOWN";
 }
@@ -203,9 +204,33 @@ gdn_status prep_scan(const gdn_dims* dims, int32_t n_seq, int32_t T, const int32
 
 gdn_status run_scan(const gdn::ScanParams& p, struct CUstream_st* stream)
 {
-    if (p.n_seq == 0) return GDN_OK;
+    if (p.n_seq == 0) {  // nothing to compute; the failure record still starts clean
+        cudaError_t e = p.workspace ? cudaMemsetAsync(p.workspace, 0, 4, reinterpret_cast<cudaStream_t>(stream))
+                                    : cudaSuccess;
+        return e == cudaSuccess ? GDN_OK : cuda_fail(e, "gdn_scan workspace clear");
+    }
     cudaError_t e = gdn::launch_scan(p, reinterpret_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? GDN_OK : cuda_fail(e, "gdn_scan launch");
+}
+
+// the scan's failure record: the first 4 bytes of its workspace
+gdn_status read_failure_word(const void* word, struct CUstream_st* stream)
+{
+    if (!word) return fail(GDN_ERR_INVALID_ARG, "workspace is NULL");
+    uint32_t h = 0;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    cudaError_t e = cudaMemcpyAsync(&h, word, sizeof h, cudaMemcpyDeviceToHost, s);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+    if (e != cudaSuccess) return cuda_fail(e, "reading the scan's failure record");
+    if (h) return fail(GDN_ERR_TIMEOUT, "a bounded wait in the scan kernels expired (record 0x%x); outputs are invalid", h);
+    return GDN_OK;
+}
+
+// offset of the scan workspace inside a gdn_layer workspace (the stage tensors come first)
+size_t layer_scan_offset(const gdn_dims* dims, int32_t T)
+{
+    const size_t hk = dims->hk, hv = dims->hv, d = dims->dk, tt = (size_t)T;
+    return align256(tt * hk * d * 4) * 2 + align256(tt * hv * d * 4) * 2 + align256(tt * hv * 4) * 2;
 }
 
 gdn_status prep_post(const gdn_dims* dims, int32_t T, const float* o, const uint16_t* z, const float* gamma,
@@ -380,6 +405,38 @@ gdn_status gdn_step(const gdn_dims* dims, int32_t n_seq, const uint16_t* qkv, co
     p.S_in = S_in; p.S_out = S_out; p.out_f32 = out_f32; p.y = y;
     cudaError_t e = gdn::launch_step(p, reinterpret_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? GDN_OK : cuda_fail(e, "gdn_step launch");
+}
+
+}  // extern "C"
+
+extern "C" {
+
+gdn_status gdn_scan_check(const void* workspace, struct CUstream_st* stream)
+{
+    return read_failure_word(workspace, stream);
+}
+
+gdn_status gdn_layer_check(const gdn_dims* dims, int32_t n_seq, int32_t T, const void* workspace,
+                           struct CUstream_st* stream)
+{
+    gdn_status st;
+    if ((st = check_dims(dims)) != GDN_OK) return st;
+    if (n_seq < 0 || T < 0) return fail(GDN_ERR_INVALID_ARG, "negative n_seq or total_tokens");
+    if (!workspace) return fail(GDN_ERR_INVALID_ARG, "workspace is NULL");
+    return read_failure_word(static_cast<const char*>(workspace) + layer_scan_offset(dims, T), stream);
+}
+
+gdn_status gdn_scan_selftest_timeout(const gdn_dims* dims, int32_t n_seq, int32_t T, const int32_t* cu_seqlens,
+                                     const float* qn, const float* kn, const float* vc, const float* glog,
+                                     const float* beta, const float* S_in, float* S_out, float* o, void* workspace,
+                                     size_t workspace_bytes, struct CUstream_st* stream)
+{
+    gdn::ScanParams p;
+    gdn_status st = prep_scan(dims, n_seq, T, cu_seqlens, qn, kn, vc, glog, beta, S_in, S_out, o, workspace,
+                              workspace_bytes, p);
+    if (st != GDN_OK) return st;
+    p.withhold_first_copy = 1;
+    return run_scan(p, stream);
 }
 
 }  // extern "C"

@@ -43,6 +43,7 @@ struct ScanParams {
     float* o;
     void* workspace;
     size_t workspace_bytes;
+    int withhold_first_copy;  // failure-report self-test only (gdn_scan_selftest_timeout)
 };
 
 struct PostParams {

@@ -800,7 +800,7 @@ __global__ void __launch_bounds__(kChainThreads, 1) scan_chain_kernel(ScanParams
         // Each wait below precedes the copy that lets its barrier advance twice, so a
         // parity wait never sees a phase two ahead.
         if (n_chunks > 0) {
-            load_kq(0);
+            if (!p.withhold_first_copy) load_kq(0);  // withheld only by the failure-report self-test
             load_am(0);
         }
         // [K; Q] and [T; P T] images of chunk c -> L2 two chunks ahead: their copies are issued only

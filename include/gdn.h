@@ -71,7 +71,9 @@ typedef enum gdn_status {
     GDN_ERR_UNSUPPORTED = 2, /* shape outside what the kernels implement       */
     GDN_ERR_ALIGNMENT = 3,   /* a pointer is not 16-byte aligned               */
     GDN_ERR_WORKSPACE = 4,   /* workspace missing or smaller than required     */
-    GDN_ERR_CUDA = 5         /* a CUDA runtime call or launch failed            */
+    GDN_ERR_CUDA = 5,        /* a CUDA runtime call or launch failed            */
+    GDN_ERR_TIMEOUT = 6      /* a bounded wait inside a kernel expired: that
+                                call's outputs are invalid (gdn_*_check)        */
 } gdn_status;
 
 /* Model shape.  Implemented: dk == dv == 128, 1 <= hk, hv % hk == 0,
@@ -210,6 +212,35 @@ GDN_API gdn_status gdn_layer(const gdn_dims* dims, int32_t n_seq, int32_t total_
                      const float* dt_bias, const float* gamma, const float* S_in, float* S_out,
                      int32_t out_f32, void* y, void* workspace, size_t workspace_bytes,
                      struct CUstream_st* stream);
+
+/*
+ * Failure reports of the scan.  Every wait inside the scan kernels is
+ * bounded (about two seconds); one that expires makes its CTA record an
+ * error in the scan workspace, release what it holds and stop, so the CUDA
+ * context stays usable but the call's outputs are invalid.  These functions
+ * read that record for the last gdn_scan (or gdn_layer) that used the
+ * workspace: they enqueue a 4-byte device-to-host copy on `stream`,
+ * SYNCHRONISE the stream and return GDN_OK or GDN_ERR_TIMEOUT (GDN_ERR_CUDA if
+ * the copy fails).  gdn_layer_check takes the layer's shape to find the scan
+ * part of the layer workspace.
+ */
+GDN_API gdn_status gdn_scan_check(const void* workspace, struct CUstream_st* stream);
+GDN_API gdn_status gdn_layer_check(const gdn_dims* dims, int32_t n_seq, int32_t total_tokens,
+                                   const void* workspace, struct CUstream_st* stream);
+
+/*
+ * gdn_scan_selftest_timeout -- test hook of the failure report, not a
+ * computation: runs gdn_scan with the recurrence kernel's first operand copy
+ * withheld, so that a bounded wait in every CTA of that kernel expires (no
+ * fault, no trap, no unbounded wait).  Arguments as for gdn_scan; the
+ * outputs are invalid and gdn_scan_check on the workspace returns
+ * GDN_ERR_TIMEOUT.  Takes about two seconds.
+ */
+GDN_API gdn_status gdn_scan_selftest_timeout(const gdn_dims* dims, int32_t n_seq, int32_t total_tokens,
+                                             const int32_t* cu_seqlens, const float* qn, const float* kn,
+                                             const float* vc, const float* glog, const float* beta,
+                                             const float* S_in, float* S_out, float* o, void* workspace,
+                                             size_t workspace_bytes, struct CUstream_st* stream);
 
 /*
  * gdn_step -- one decode step: a single new token for each of n_seq

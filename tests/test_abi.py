@@ -45,9 +45,9 @@ def test_library_exports_every_declared_symbol(L):
 
 
 def test_status_strings(L):
-    names = [L.gdn_status_string(i).decode() for i in range(6)]
+    names = [L.gdn_status_string(i).decode() for i in range(7)]
     assert names == ["GDN_OK", "GDN_ERR_INVALID_ARG", "GDN_ERR_UNSUPPORTED", "GDN_ERR_ALIGNMENT",
-                     "GDN_ERR_WORKSPACE", "GDN_ERR_CUDA"]
+                     "GDN_ERR_WORKSPACE", "GDN_ERR_CUDA", "GDN_ERR_TIMEOUT"]
 
 
 def test_header_compiles_as_c(tmp_path):
