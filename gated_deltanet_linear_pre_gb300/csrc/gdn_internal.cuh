@@ -85,6 +85,32 @@ cudaError_t launch_post(const PostParams& p, cudaStream_t stream);
 // record the detail string returned by gdn_last_error_string on this thread
 void set_last_error(const char* msg);
 
+// ---- programmatic dependent launch ---------------------------------------------
+// Kernels launched with launch_k(..., pdl = true) may start while the previous
+// kernel on the stream is still draining.  Every kernel calls pdl_wait() before
+// its first read of global memory (a no-op when launched without the
+// attribute) and pdl_launch_dependents() early, which lets the next kernel's
+// CTAs be scheduled once every CTA of this one has started.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
+template <typename... KArgs, typename... Args>
+cudaError_t launch_k(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream, bool pdl,
+                     Args... args)
+{
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = pdl ? attr : nullptr;
+    cfg.numAttrs = pdl ? 1 : 0;
+    return cudaLaunchKernelEx(&cfg, kernel, args...);
+}
+
 // ---- small device helpers ---------------------------------------------------
 __device__ __forceinline__ float warp_sum(float v)
 {

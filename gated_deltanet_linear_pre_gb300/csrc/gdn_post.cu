@@ -23,6 +23,8 @@ constexpr int kRows = 4;
 template <bool kF32>
 __global__ void __launch_bounds__(kThreads) post_kernel(PostParams p, long long n_rows)
 {
+    pdl_launch_dependents();
+    pdl_wait();
     const int lane = threadIdx.x & 31;
     const long long warp_global = (long long)blockIdx.x * kWarps + (threadIdx.x >> 5);
     const long long n_warps = (long long)gridDim.x * kWarps;
@@ -83,11 +85,8 @@ cudaError_t launch_post(const PostParams& p, cudaStream_t stream)
     // batches beyond 2^31 blocks
     const long long want = (n_rows + (long long)kWarps * kRows - 1) / ((long long)kWarps * kRows);
     const int grid = (int)(want < 0x7fffffffLL ? want : 0x7fffffffLL);
-    if (p.out_f32)
-        post_kernel<true><<<grid, kThreads, 0, stream>>>(p, n_rows);
-    else
-        post_kernel<false><<<grid, kThreads, 0, stream>>>(p, n_rows);
-    return cudaGetLastError();
+    return p.out_f32 ? launch_k(post_kernel<true>, dim3(grid), dim3(kThreads), 0, stream, true, p, n_rows)
+                     : launch_k(post_kernel<false>, dim3(grid), dim3(kThreads), 0, stream, true, p, n_rows);
 }
 
 }  // namespace gdn

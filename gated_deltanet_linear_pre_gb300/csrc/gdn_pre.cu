@@ -77,6 +77,8 @@ __global__ void __launch_bounds__(kThreads, 4)
 pre_kernel(PreParams p, int n_slots, int head_groups, int n_conv_blocks)
 {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    pdl_launch_dependents();
+    pdl_wait();
 
     if ((int)blockIdx.x >= n_conv_blocks) {
         // ---- carried history: the last 3 inputs of sequence s, channel c --
@@ -196,8 +198,8 @@ cudaError_t launch_pre(const PreParams& p, cudaStream_t stream)
     const long long blocks = n_conv_blocks + n_hist_blocks;
     if (blocks == 0) return cudaSuccess;
     if (blocks > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
-    pre_kernel<<<(unsigned)blocks, kThreads, 0, stream>>>(p, n_slots, head_groups, (int)n_conv_blocks);
-    return cudaGetLastError();
+    return launch_k(pre_kernel, dim3((unsigned)blocks), dim3(kThreads), 0, stream, true, p, n_slots, head_groups,
+                    (int)n_conv_blocks);
 }
 
 }  // namespace gdn

@@ -285,6 +285,8 @@ __global__ void __launch_bounds__(kGramThreads) scan_gram_kernel(ScanParams p)
     const int L = tid & 127, wg = tid >> 7;
     const int slot = blockIdx.x, j = blockIdx.y;
     uint32_t* err = reinterpret_cast<uint32_t*>(p.workspace);
+    pdl_launch_dependents();
+    pdl_wait();
     int c0, n;
     bool has_prev, odd;
     if (!slot_chunk(p, slot, c0, n, &has_prev, &odd)) return;  // unused slot (whole CTA)
@@ -379,6 +381,8 @@ __global__ void __launch_bounds__(kPrepThreads, 4) scan_prep_kernel(ScanParams p
     const int L = tid & 127, wg = tid >> 7;  // TMEM lane, column half
     const int slot = blockIdx.x, h = blockIdx.y, j = h / (p.hv / p.hk);
     uint32_t* err = reinterpret_cast<uint32_t*>(p.workspace);
+    pdl_launch_dependents();
+    pdl_wait();
     constexpr int ST = 68;  // fp32 row stride of A and T
     int c0, n;
     bool odd;
@@ -724,6 +728,8 @@ __global__ void __launch_bounds__(kChainThreads, 1) scan_chain_kernel(ScanParams
 {
     extern __shared__ __align__(1024) unsigned char smem_raw[];
     ChainSmem<DVS>& sm = *reinterpret_cast<ChainSmem<DVS>*>(smem_raw);
+    pdl_launch_dependents();
+    pdl_wait();
     constexpr int SLICES = kHeadDim / DVS;
     constexpr int COLS = DVS / kChainWG;  // columns per compute thread
     constexpr uint32_t kTmemCols = 512;
@@ -1145,16 +1151,17 @@ cudaError_t launch_scan(const ScanParams& p, cudaStream_t stream)
     if (e != cudaSuccess) return e;
     const size_t slots = n_slots(p.T, p.n_seq);
     if (p.T > 0) {
-        scan_gram_kernel<<<dim3((unsigned)slots, (unsigned)p.hk), kGramThreads, gram_smem, stream>>>(p);
-        e = cudaGetLastError();
+        // gram follows the failure-record clear in plain stream order; prep and the chain may
+        // start while their predecessor drains (each waits for it before reading anything)
+        e = launch_k(scan_gram_kernel, dim3((unsigned)slots, (unsigned)p.hk), dim3(kGramThreads), gram_smem, stream,
+                     false, p);
         if (e != cudaSuccess) return e;
-        scan_prep_kernel<<<dim3((unsigned)slots, (unsigned)p.hv), kPrepThreads, prep_smem, stream>>>(p);
-        e = cudaGetLastError();
+        e = launch_k(scan_prep_kernel, dim3((unsigned)slots, (unsigned)p.hv), dim3(kPrepThreads), prep_smem, stream,
+                     true, p);
         if (e != cudaSuccess) return e;
     }
-    scan_chain_kernel<kDVS><<<dim3((unsigned)(p.hv * (kHeadDim / kDVS)), (unsigned)p.n_seq), kChainThreads,
-                              chain_smem, stream>>>(p);
-    return cudaGetLastError();
+    return launch_k(scan_chain_kernel<kDVS>, dim3((unsigned)(p.hv * (kHeadDim / kDVS)), (unsigned)p.n_seq),
+                    dim3(kChainThreads), chain_smem, stream, p.T > 0, p);
 }
 
 }  // namespace gdn

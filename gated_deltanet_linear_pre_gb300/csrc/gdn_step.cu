@@ -61,6 +61,8 @@ __global__ void __launch_bounds__(kThreads, 2) step_kernel(StepParams p)
     __shared__ float wsum[8];
     __shared__ float s_g, s_beta;
 
+    pdl_launch_dependents();
+    pdl_wait();
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int h = blockIdx.x, s = blockIdx.y;
     const int group = p.hv / p.hk, j = h / group;
@@ -184,8 +186,7 @@ __global__ void __launch_bounds__(kThreads, 2) step_kernel(StepParams p)
 cudaError_t launch_step(const StepParams& p, cudaStream_t stream)
 {
     if (p.n_seq == 0) return cudaSuccess;
-    step_kernel<<<dim3((unsigned)p.hv, (unsigned)p.n_seq), kThreads, 0, stream>>>(p);
-    return cudaGetLastError();
+    return launch_k(step_kernel, dim3((unsigned)p.hv, (unsigned)p.n_seq), dim3(kThreads), 0, stream, true, p);
 }
 
 }  // namespace gdn
