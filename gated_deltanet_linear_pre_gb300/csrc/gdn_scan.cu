@@ -287,6 +287,9 @@ __global__ void __launch_bounds__(kGramThreads) scan_gram_kernel(ScanParams p)
     uint32_t* err = reinterpret_cast<uint32_t*>(p.workspace);
     pdl_launch_dependents();
     pdl_wait();
+    // the failure record starts clean: the first CTA clears it before anything could set it (an
+    // expired wait takes seconds; the later kernels of the scan start only after this one ends)
+    if (slot == 0 && j == 0 && tid == 0) *err = 0u;
     int c0, n;
     bool has_prev, odd;
     if (!slot_chunk(p, slot, c0, n, &has_prev, &odd)) return;  // unused slot (whole CTA)
@@ -1147,14 +1150,14 @@ cudaError_t launch_scan(const ScanParams& p, cudaStream_t stream)
     if (e != cudaSuccess) return e;
     e = cudaFuncSetAttribute(scan_chain_kernel<kDVS>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)chain_smem);
     if (e != cudaSuccess) return e;
-    e = cudaMemsetAsync(p.workspace, 0, 4, stream);
-    if (e != cudaSuccess) return e;
     const size_t slots = n_slots(p.T, p.n_seq);
-    if (p.T > 0) {
-        // gram follows the failure-record clear in plain stream order; prep and the chain may
-        // start while their predecessor drains (each waits for it before reading anything)
+    if (p.T == 0) {  // no gram launch to clear the failure record (rare: every sequence empty)
+        e = cudaMemsetAsync(p.workspace, 0, 4, stream);
+        if (e != cudaSuccess) return e;
+    } else {
+        // each kernel may start while its predecessor drains and waits for it before reading
         e = launch_k(scan_gram_kernel, dim3((unsigned)slots, (unsigned)p.hk), dim3(kGramThreads), gram_smem, stream,
-                     false, p);
+                     true, p);
         if (e != cudaSuccess) return e;
         e = launch_k(scan_prep_kernel, dim3((unsigned)slots, (unsigned)p.hv), dim3(kPrepThreads), prep_smem, stream,
                      true, p);
