@@ -152,7 +152,8 @@ class ClockSampler:
                 "samples": len(sm)}
 
 
-STAGE_SOURCES = {"pre": ["gdn_pre.cu"], "scan": ["gdn_scan.cu", "umma.cuh"], "post": ["gdn_post.cu"]}
+STAGE_SOURCES = {"pre": ["gdn_pre.cu"], "scan": ["gdn_scan.cu", "umma.cuh"], "post": ["gdn_post.cu"],
+                 "step": ["gdn_step.cu"]}
 
 
 def source_digest(stage: str) -> str:
@@ -309,7 +310,8 @@ def run_decode(args, rank, world, local):
     nbytes = decode_bytes_per_layer(B)
     gbs = nbytes / (launch_ms * 1e-3) / 1e9
     roofline = {"bound": "hbm", "kernel": "gdn_step", "achieved": gbs, "peak": hbm_peak, "unit": "GB/s",
-                "frac": gbs / hbm_peak, "traffic": None, "alg_bytes_per_launch": nbytes,
+                "frac": gbs / hbm_peak, "traffic": stage_traffic("step") if B == 256 else None,
+                "alg_bytes_per_launch": nbytes,
                 "peak_source": f"{peak_src} (MEASURED_PEAKS.json hbm_gbs)" if peak_src == "measured" else "fallback"}
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
