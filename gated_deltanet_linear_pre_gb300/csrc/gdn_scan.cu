@@ -547,24 +547,29 @@ __global__ void __launch_bounds__(kPrepThreads, 4) scan_prep_kernel(ScanParams p
                 *reinterpret_cast<float2*>(&Tm[(ro + r) * ST + co + c2]) = make_float2(-t0, -t1);
             }
             __syncthreads();
-            {   // (3) rows 32-63 x cols 0-31; T1 and T2 are block lower triangular
+            {   // (3) rows 32-63 x cols 0-31; T1 and T2 are block lower triangular.  Both loops are
+                // fully unrolled; the structurally zero 16-wide blocks (never written, so they may
+                // hold any bits) are selected away, not multiplied, so every load is in flight at once
                 const int r = tid >> 3, c4 = 4 * (tid & 7);
+                const bool hi_c = (c4 >> 4) != 0;  // T1[m][c] for m < 16 is zero when c >= 16
+                const float4 z4 = make_float4(0.f, 0.f, 0.f, 0.f);
                 float acc[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll 8
+#pragma unroll
                 for (int m = 0; m < 32; ++m) {
-                    if ((m >> 4) < (c4 >> 4)) continue;  // T1[m][c] = 0 above the block diagonal
                     const float a = A[(32 + r) * ST + m];
-                    const float4 t4 = *reinterpret_cast<const float4*>(&Tm[m * ST + c4]);
+                    const float4 t4l = *reinterpret_cast<const float4*>(&Tm[m * ST + c4]);
+                    const float4 t4 = (m < 16 && hi_c) ? z4 : t4l;
                     acc[0] = fmaf(a, t4.x, acc[0]); acc[1] = fmaf(a, t4.y, acc[1]);
                     acc[2] = fmaf(a, t4.z, acc[2]); acc[3] = fmaf(a, t4.w, acc[3]);
                 }
                 *reinterpret_cast<float4*>(&sm.W[r * 32 + c4]) = make_float4(acc[0], acc[1], acc[2], acc[3]);
                 __syncthreads();
+                const bool lo_r = (r >> 4) == 0;  // T2[r][m] for m >= 16 is zero when r < 16
                 float t[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll 8
+#pragma unroll
                 for (int m = 0; m < 32; ++m) {
-                    if ((m >> 4) > (r >> 4)) continue;  // T2[r][m] = 0 above the block diagonal
-                    const float a = Tm[(32 + r) * ST + 32 + m];
+                    const float al = Tm[(32 + r) * ST + 32 + m];
+                    const float a = (m >= 16 && lo_r) ? 0.0f : al;
                     const float4 w4 = *reinterpret_cast<const float4*>(&sm.W[m * 32 + c4]);
                     t[0] = fmaf(a, w4.x, t[0]); t[1] = fmaf(a, w4.y, t[1]);
                     t[2] = fmaf(a, w4.z, t[2]); t[3] = fmaf(a, w4.w, t[3]);
