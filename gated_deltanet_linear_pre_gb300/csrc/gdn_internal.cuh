@@ -44,6 +44,7 @@ struct ScanParams {
     void* workspace;
     size_t workspace_bytes;
     int withhold_first_copy;  // failure-report self-test only (gdn_scan_selftest_timeout)
+    unsigned long long epoch;  // this call's tag for the per-chunk ready flags (set by launch_scan)
 };
 
 struct PostParams {

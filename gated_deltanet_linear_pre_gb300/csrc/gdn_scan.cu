@@ -42,6 +42,9 @@
 // Every MMA is issued by one thread and completes on an mbarrier; every wait
 // is bounded and, on expiry, the CTA records an error code in the workspace,
 // drains its own copies in flight (bounded), frees its TMEM and stops.
+#include <atomic>
+#include <chrono>
+
 #include "gdn_internal.cuh"
 #include "umma.cuh"
 
@@ -168,6 +171,39 @@ struct ChainGates {
     float gL, pad[3];
 };
 static_assert(sizeof(ChainGates) % 16 == 0 && sizeof(ChainGates) <= kGateBytes, "gate row");
+
+// per (chunk slot, value head): the call's epoch once prep has written that chunk's [T; P T]
+// image and gate row (and, through its wait on gram, everything before it is complete)
+__device__ __forceinline__ unsigned long long* ready_flag(const ScanParams& p, size_t slot, int h)
+{
+    return reinterpret_cast<unsigned long long*>(
+               static_cast<unsigned char*>(p.workspace) + kWsHeader +
+               n_slots(p.T, p.n_seq) * ((size_t)p.hv * kAmBlock + (size_t)p.hk * (kKqBytes + kGramBytes + kMBytes))) +
+           slot * p.hv + h;
+}
+
+__device__ __forceinline__ void flag_publish(unsigned long long* f, unsigned long long v)
+{
+    asm volatile("st.release.gpu.global.u64 [%0], %1;" ::"l"(f), "l"(v) : "memory");
+}
+
+__device__ __forceinline__ unsigned long long flag_read(const unsigned long long* f)
+{
+    unsigned long long v;
+    asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(f) : "memory");
+    return v;
+}
+
+// bounded wait (about two seconds of SM clock) for a ready flag; false on expiry
+__device__ __forceinline__ bool flag_wait(const unsigned long long* f, unsigned long long v)
+{
+    const long long start = clock64();
+    while (flag_read(f) != v) {
+        if (clock64() - start > (4ll << 30)) return false;
+        __nanosleep(128);
+    }
+    return true;
+}
 
 __device__ __forceinline__ ChainGates* gate_row(const ScanParams& p, size_t slot, int h)
 {
@@ -647,6 +683,12 @@ __global__ void __launch_bounds__(kPrepThreads, 4) scan_prep_kernel(ScanParams p
         umma::fence_after_sync();
     }
 
+    // everything this chunk's chain needs is written: publish it (release, GPU scope)
+    if (tid == 0) {
+        __threadfence();
+        flag_publish(ready_flag(p, slot, h), p.epoch);
+    }
+
 done:
     umma::fence_before_sync();
     __syncthreads();
@@ -736,8 +778,10 @@ __global__ void __launch_bounds__(kChainThreads, 1) scan_chain_kernel(ScanParams
 {
     extern __shared__ __align__(1024) unsigned char smem_raw[];
     ChainSmem<DVS>& sm = *reinterpret_cast<ChainSmem<DVS>*>(smem_raw);
+    // no grid-wide wait on the prep kernel: the CTA waits for the ready flag of its first chunk
+    // (which implies every earlier kernel of the call has completed) and the copy warp for each
+    // later chunk's flag, so the recurrence starts while prep's last CTAs still run
     pdl_launch_dependents();
-    pdl_wait();
     constexpr int SLICES = kHeadDim / DVS;
     constexpr int COLS = DVS / kChainWG;  // columns per compute thread
     constexpr uint32_t kTmemCols = 512;
@@ -775,11 +819,17 @@ __global__ void __launch_bounds__(kChainThreads, 1) scan_chain_kernel(ScanParams
         umma::mbar_init(&sm.mb_grp[0], kChainCompute / 2);
         umma::mbar_init(&sm.mb_grp[1], kChainCompute / 2);
         sm.abort_flag = 0;
+        if (n_chunks > 0 && !flag_wait(ready_flag(p, base, h), p.epoch)) {
+            sm.abort_flag = 1;
+            atomicOr(err, kErrTimeout);
+        }
     }
+    if (n_chunks == 0) pdl_wait();  // no chunk, no flag: wait for the whole prep grid
     umma::fence_before_sync();
     __syncthreads();
     umma::fence_after_sync();
     const uint32_t tmem = sm.tmem_base;
+    if (sm.abort_flag) goto done;
 
 #define GDN_WAIT(mbar, parity)                                                 \
     do {                                                                       \
@@ -828,6 +878,17 @@ __global__ void __launch_bounds__(kChainThreads, 1) scan_chain_kernel(ScanParams
         prefetch_l2(1);
         for (int c = 0; c + 1 < n_chunks; ++c) {
             prefetch_l2(c + 2);
+            {   // chunk c+1's operands are written (bounded wait for its ready flag)
+                bool ok = true;
+                if (leader) ok = flag_wait(ready_flag(p, base + c + 1, h), p.epoch);
+                if (!__shfl_sync(0xffffffffu, ok ? 1 : 0, 0)) {
+                    if (leader) {
+                        sm.abort_flag = 1;
+                        atomicOr(err, kErrTimeout);
+                    }
+                    goto done;
+                }
+            }
             // R1 (Q_c) and M free once (K S ; Q S) of chunk c is complete; the slot of K_{c-1}
             // once that chunk's state update is done
             GDN_WAIT(&sm.mb_f, c & 1);
@@ -1142,11 +1203,22 @@ done:
 
 size_t scan_workspace_bytes(int hk, int hv, int n_seq, int T)
 {
-    return kWsHeader + n_slots(T, n_seq) * ((size_t)hv * kAmBlock + (size_t)hk * (kKqBytes + kGramBytes + kMBytes));
+    return kWsHeader + n_slots(T, n_seq) * ((size_t)hv * (kAmBlock + 8) + (size_t)hk * (kKqBytes + kGramBytes + kMBytes));
 }
 
-cudaError_t launch_scan(const ScanParams& p, cudaStream_t stream)
+// a fresh 64-bit tag per scan call for the ready flags: a workspace's stale flags (from an
+// earlier call, or uninitialised memory) never equal the current call's tag in practice
+unsigned long long next_epoch()
 {
+    static std::atomic<unsigned long long> counter{
+        (unsigned long long)std::chrono::steady_clock::now().time_since_epoch().count() * 0x9E3779B97F4A7C15ull};
+    return counter.fetch_add(0x9E3779B97F4A7C15ull) | 1ull;
+}
+
+cudaError_t launch_scan(const ScanParams& p_in, cudaStream_t stream)
+{
+    ScanParams p = p_in;
+    p.epoch = next_epoch();
     if (p.n_seq == 0) return cudaSuccess;
     const size_t gram_smem = sizeof(GramSmem), prep_smem = sizeof(PrepSmem), chain_smem = sizeof(ChainSmem<kDVS>);
     cudaError_t e = cudaFuncSetAttribute(scan_gram_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)gram_smem);
