@@ -418,7 +418,9 @@ __global__ void __launch_bounds__(kPrepThreads, 4) scan_prep_kernel(ScanParams p
     PrepSmem& sm = *reinterpret_cast<PrepSmem*>(smem_raw);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int L = tid & 127, wg = tid >> 7;  // TMEM lane, column half
-    const int slot = blockIdx.x, h = blockIdx.y, j = h / (p.hv / p.hk);
+    // value head fastest: chunk slots complete in order across all heads, so the chain (which
+    // consumes chunk after chunk and starts during prep's last wave) finds its early chunks ready
+    const int h = blockIdx.x, slot = blockIdx.y, j = h / (p.hv / p.hk);
     uint32_t* err = reinterpret_cast<uint32_t*>(p.workspace);
     pdl_launch_dependents();
     pdl_wait();
@@ -1236,7 +1238,7 @@ cudaError_t launch_scan(const ScanParams& p_in, cudaStream_t stream)
         e = launch_k(scan_gram_kernel, dim3((unsigned)slots, (unsigned)p.hk), dim3(kGramThreads), gram_smem, stream,
                      true, p);
         if (e != cudaSuccess) return e;
-        e = launch_k(scan_prep_kernel, dim3((unsigned)slots, (unsigned)p.hv), dim3(kPrepThreads), prep_smem, stream,
+        e = launch_k(scan_prep_kernel, dim3((unsigned)p.hv, (unsigned)slots), dim3(kPrepThreads), prep_smem, stream,
                      true, p);
         if (e != cudaSuccess) return e;
     }
