@@ -45,7 +45,6 @@ struct ScanParams {
     size_t workspace_bytes;
     int withhold_first_copy;  // failure-report self-test only (gdn_scan_selftest_timeout)
     unsigned long long epoch;  // this call's tag for the per-chunk ready flags (set by launch_scan)
-    int prep_keep;  // prep CTAs that stay after the first round of tasks (set by launch_scan)
 };
 
 struct PostParams {

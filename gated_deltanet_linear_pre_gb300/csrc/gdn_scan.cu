@@ -27,14 +27,11 @@
 //    [K; Q] into the tensor-core layout (the chain's [K; Q] image), forms
 //    (K K^T ; Q K^T) in fp32, and M = [K; Q] K_prev^T against the previous
 //    chunk's keys (the chain's look-ahead operand).
-//  * scan_prep_kernel, one task per (chunk, value head), fully parallel: A and
+//  * scan_prep_kernel, one CTA per (chunk, value head), fully parallel: A and
 //    P from the key head's gram rows and the head's gates, the inverse of
 //    I + A (recursive halving with 16x16 diagonal blocks by forward
 //    substitution, on CUDA cores) and P T on the tensor core; writes the
-//    [T; P T] image and the chain's gate row.  One CTA per SM runs four
-//    256-thread task groups; after one round over all SMs only the CTAs on
-//    the SMs the chain leaves free go on, so the chain starts early and
-//    consumes the chunks while prep finishes them.
+//    [T; P T] image and the chain's gate row.
 //  * scan_chain_kernel, one CTA per (sequence, value head, 64-column slice):
 //    the state-dependent part, chunk after chunk, with the fp32 state slice
 //    in registers.  The next chunk's [K; Q] S is split into a part issued a
@@ -397,17 +394,9 @@ __global__ void __launch_bounds__(kGramThreads) scan_gram_kernel(ScanParams p)
 }
 
 // =======================================================================================
-// prep: task groups of 256 threads, one task per (chunk slot, value head)
-//
-// A CTA holds four groups (one CTA fills an SM's shared memory); tasks are
-// numbered in slot order, the value head fastest, so the chunk slots complete
-// in order across all heads.  In the first round every group of every CTA
-// takes one task; after it only the first prep_keep CTAs go on (round robin),
-// the others exit and their SMs take the chain's CTAs, which start on the
-// first round's chunks while the remaining CTAs keep ahead of them.
+// prep: one CTA per (chunk slot, value head)
 // =======================================================================================
-constexpr int kPrepThreads = 256;  // one group: two warpgroups, each covers all 128 TMEM lanes, half the columns
-constexpr int kPrepGroups = 4;     // groups per CTA
+constexpr int kPrepThreads = 256;  // two warpgroups: each covers all 128 TMEM lanes, half the columns
 
 struct __align__(1024) PrepSmem {
     uint16_t ap[2][64 * 64];   // P (K-major, 64 rows); an M = 128 descriptor reads its rows 64-127 from
@@ -422,25 +411,23 @@ struct __align__(1024) PrepSmem {
     int abort_flag;
     uint64_t mbar;
 };
-static_assert(kPrepGroups * sizeof(PrepSmem) <= 227 * 1024, "prep groups exceed the shared memory of a CTA");
 
-// barrier of one prep group (id 0 stays __syncthreads')
-__device__ __forceinline__ void group_sync(int id)
-{
-    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(kPrepThreads) : "memory");
-}
-
-__global__ void __launch_bounds__(kPrepThreads * kPrepGroups, 1) scan_prep_kernel(ScanParams p)
+__global__ void __launch_bounds__(kPrepThreads, 4) scan_prep_kernel(ScanParams p)
 {
     extern __shared__ __align__(1024) unsigned char smem_raw[];
-    const int grp = threadIdx.x / kPrepThreads, bar = 1 + grp;
-    PrepSmem& sm = reinterpret_cast<PrepSmem*>(smem_raw)[grp];
-    const int tid = threadIdx.x % kPrepThreads, warp = tid >> 5, lane = tid & 31;
+    PrepSmem& sm = *reinterpret_cast<PrepSmem*>(smem_raw);
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int L = tid & 127, wg = tid >> 7;  // TMEM lane, column half
+    // value head fastest: chunk slots complete in order across all heads, so the chain (which
+    // consumes chunk after chunk and starts during prep's last wave) finds its early chunks ready
+    const int h = blockIdx.x, slot = blockIdx.y, j = h / (p.hv / p.hk);
     uint32_t* err = reinterpret_cast<uint32_t*>(p.workspace);
     pdl_launch_dependents();
     pdl_wait();
     constexpr int ST = 68;  // fp32 row stride of A and T
+    int c0, n;
+    bool odd;
+    if (!slot_chunk(p, slot, c0, n, nullptr, &odd)) return;  // unused slot (whole CTA)
     const float qscale = rsqrtf((float)kHeadDim);
 
     if (warp == 0) umma::tmem_alloc(&sm.tmem_base, 64);
@@ -448,50 +435,38 @@ __global__ void __launch_bounds__(kPrepThreads * kPrepGroups, 1) scan_prep_kerne
         umma::mbar_init(&sm.mbar, 1);
         sm.abort_flag = 0;
     }
-    umma::fence_before_sync();
-    group_sync(bar);
+    // raw gates of the value head (warp 0)
+    float raw_lam[2] = {0.f, 0.f}, raw_beta[2] = {0.f, 0.f};
+    if (warp == 0) {
+#pragma unroll
+        for (int q = 0; q < 2; ++q) {
+            const int t = lane + 32 * q;
+            raw_lam[q] = t < n ? __ldg(p.glog + (size_t)(c0 + t) * p.hv + h) : 0.0f;
+            raw_beta[q] = t < n ? __ldg(p.beta + (size_t)(c0 + t) * p.hv + h) : 0.0f;
+        }
+    }
+    // this thread's 32 entries of the gram rows of the key head: row L (K K^T for
+    // L < 64, Q K^T for L >= 64), columns [32 wg, 32 wg + 32)
+    float d[32];
+    {
+        const float4* src = reinterpret_cast<const float4*>(gram_rows(p, slot, j) + L * 64 + 32 * wg);
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+            const float4 x = __ldg(src + q);
+            d[4 * q] = x.x; d[4 * q + 1] = x.y; d[4 * q + 2] = x.z; d[4 * q + 3] = x.w;
+        }
+    }
+    __syncthreads();
     umma::fence_after_sync();
     const uint32_t tmem = sm.tmem_base;
-    const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;  // a group's warps start at a multiple of 4
+    const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
     const uint32_t a_p[2] = {umma::smem_u32(sm.ap[0]), umma::smem_u32(sm.ap[1])};
     const uint32_t b_t[2] = {umma::smem_u32(sm.u.bt[0]), umma::smem_u32(sm.u.bt[1])};
     uint32_t phase = 0;
     float* A = sm.u.A;
     float* Tm = sm.T;
 
-    const size_t n_tasks = n_slots(p.T, p.n_seq) * (size_t)p.hv, round1 = (size_t)gridDim.x * kPrepGroups;
-    const size_t keep = (size_t)p.prep_keep;
-    auto next_task = [&](size_t t) -> size_t {
-        if (t >= round1) return t + keep * kPrepGroups;
-        return blockIdx.x < keep ? round1 + (size_t)grp * keep + blockIdx.x : n_tasks;
-    };
-    for (size_t task = (size_t)grp * gridDim.x + blockIdx.x; task < n_tasks; task = next_task(task)) {
-        const int h = (int)(task % (size_t)p.hv), slot = (int)(task / (size_t)p.hv), j = h / (p.hv / p.hk);
-        int c0, n;
-        bool odd;
-        if (!slot_chunk(p, slot, c0, n, nullptr, &odd)) continue;  // unused slot (whole group)
-        // raw gates of the value head (warp 0)
-        float raw_lam[2] = {0.f, 0.f}, raw_beta[2] = {0.f, 0.f};
-        if (warp == 0) {
-#pragma unroll
-            for (int q = 0; q < 2; ++q) {
-                const int t = lane + 32 * q;
-                raw_lam[q] = t < n ? __ldg(p.glog + (size_t)(c0 + t) * p.hv + h) : 0.0f;
-                raw_beta[q] = t < n ? __ldg(p.beta + (size_t)(c0 + t) * p.hv + h) : 0.0f;
-            }
-        }
-        // this thread's 32 entries of the gram rows of the key head: row L (K K^T for
-        // L < 64, Q K^T for L >= 64), columns [32 wg, 32 wg + 32)
-        float d[32];
-        {
-            const float4* src = reinterpret_cast<const float4*>(gram_rows(p, slot, j) + L * 64 + 32 * wg);
-#pragma unroll
-            for (int q = 0; q < 8; ++q) {
-                const float4 x = __ldg(src + q);
-                d[4 * q] = x.x; d[4 * q + 1] = x.y; d[4 * q + 2] = x.z; d[4 * q + 3] = x.w;
-            }
-        }
-
+    {
         // gates of value head h: running log-decay G and beta
         if (warp == 0) {
             float lam[2];
@@ -512,7 +487,7 @@ __global__ void __launch_bounds__(kPrepThreads * kPrepGroups, 1) scan_prep_kerne
             gr->beta[lane + 32] = b1;
             if (lane == 0) gr->gL = __expf(GL);
         }
-        group_sync(bar);
+        __syncthreads();
 
         // A (fp32, rows L < 64) and P (split, rows L - 64 for L >= 64), columns of wg
         {
@@ -557,7 +532,7 @@ __global__ void __launch_bounds__(kPrepThreads * kPrepGroups, 1) scan_prep_kerne
                 }
             }
         }
-        group_sync(bar);
+        __syncthreads();
 
         // T = (I + A)^-1 (A strictly lower), recursively by halves: T = [[T1, 0], [-T2 A21 T1, T2]].
         // (1) the four 16x16 diagonal blocks by forward substitution (thread (b, c): column c;
@@ -585,7 +560,7 @@ __global__ void __launch_bounds__(kPrepThreads * kPrepGroups, 1) scan_prep_kerne
 #pragma unroll
                 for (int r = 0; r < 16; ++r) Tm[(o + r) * ST + o + c] = col[r];
             }
-            group_sync(bar);
+            __syncthreads();
             {   // (2) pairs b = 1 (rows 16-31 x cols 0-15) and b = 3 (rows 48-63 x cols 32-47)
                 const int pr = tid >> 7, r = (tid >> 3) & 15, c2 = 2 * (tid & 7);
                 const int ro = 32 * pr + 16, co = 32 * pr;  // block (b, b-1) origin
@@ -598,7 +573,7 @@ __global__ void __launch_bounds__(kPrepThreads * kPrepGroups, 1) scan_prep_kerne
                     w1 = fmaf(a, t2.y, w1);
                 }
                 *reinterpret_cast<float2*>(&sm.W[pr * 256 + r * 16 + c2]) = make_float2(w0, w1);
-                group_sync(bar);
+                __syncthreads();
                 float t0 = 0.f, t1 = 0.f;
 #pragma unroll
                 for (int m = 0; m < 16; ++m) {
@@ -609,7 +584,7 @@ __global__ void __launch_bounds__(kPrepThreads * kPrepGroups, 1) scan_prep_kerne
                 }
                 *reinterpret_cast<float2*>(&Tm[(ro + r) * ST + co + c2]) = make_float2(-t0, -t1);
             }
-            group_sync(bar);
+            __syncthreads();
             {   // (3) rows 32-63 x cols 0-31; T1 and T2 are block lower triangular.  Both loops are
                 // fully unrolled; the structurally zero 16-wide blocks (never written, so they may
                 // hold any bits) are selected away, not multiplied, so every load is in flight at once
@@ -626,7 +601,7 @@ __global__ void __launch_bounds__(kPrepThreads * kPrepGroups, 1) scan_prep_kerne
                     acc[2] = fmaf(a, t4.z, acc[2]); acc[3] = fmaf(a, t4.w, acc[3]);
                 }
                 *reinterpret_cast<float4*>(&sm.W[r * 32 + c4]) = make_float4(acc[0], acc[1], acc[2], acc[3]);
-                group_sync(bar);
+                __syncthreads();
                 const bool lo_r = (r >> 4) == 0;  // T2[r][m] for m >= 16 is zero when r < 16
                 float t[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
@@ -639,7 +614,7 @@ __global__ void __launch_bounds__(kPrepThreads * kPrepGroups, 1) scan_prep_kerne
                 }
                 *reinterpret_cast<float4*>(&Tm[(32 + r) * ST + c4]) = make_float4(-t[0], -t[1], -t[2], -t[3]);
             }
-            group_sync(bar);
+            __syncthreads();
             // T -> MN-major B tile (element (n = column, k = row)); row fastest across
             // lanes; column groups right of the row's diagonal block are zero
             for (int u = tid; u < 64 * 8; u += kPrepThreads) {
@@ -659,7 +634,7 @@ __global__ void __launch_bounds__(kPrepThreads * kPrepGroups, 1) scan_prep_kerne
         }
         umma::fence_proxy_async();
         umma::fence_before_sync();
-        group_sync(bar);
+        __syncthreads();
         umma::fence_after_sync();
 
         // P T  (M = 128 descriptor over the 64-row P tile; rows 64-127 of the product unused)
@@ -670,8 +645,8 @@ __global__ void __launch_bounds__(kPrepThreads * kPrepGroups, 1) scan_prep_kerne
         }
         if (!umma::mbar_wait(&sm.mbar, phase)) { sm.abort_flag = 1; atomicOr(err, kErrTimeout); }
         phase ^= 1u;
-        group_sync(bar);
-        if (sm.abort_flag) break;
+        __syncthreads();
+        if (sm.abort_flag) goto done;
         umma::fence_after_sync();
 
         // [T; P T] image (K-major, split; [P T; T] for odd chunks): threads L >= 64 copy T row L - 64
@@ -706,18 +681,19 @@ __global__ void __launch_bounds__(kPrepThreads * kPrepGroups, 1) scan_prep_kerne
             }
         }
         umma::fence_before_sync();
-        group_sync(bar);
+        __syncthreads();
         umma::fence_after_sync();
-
-        // everything this chunk's chain needs is written: publish it (release, GPU scope)
-        if (tid == 0) {
-            __threadfence();
-            flag_publish(ready_flag(p, slot, h), p.epoch);
-        }
     }
 
+    // everything this chunk's chain needs is written: publish it (release, GPU scope)
+    if (tid == 0) {
+        __threadfence();
+        flag_publish(ready_flag(p, slot, h), p.epoch);
+    }
+
+done:
     umma::fence_before_sync();
-    group_sync(bar);
+    __syncthreads();
     if (warp == 0) umma::tmem_dealloc(sm.tmem_base, 64);
 }
 
@@ -1241,46 +1217,15 @@ unsigned long long next_epoch()
     return counter.fetch_add(0x9E3779B97F4A7C15ull) | 1ull;
 }
 
-int sm_count()
-{
-    static int cached[64] = {};
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
-    if (cached[dev] == 0) {
-        int v = 0;
-        if (cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
-        cached[dev] = v;
-    }
-    return cached[dev];
-}
-
-// prep grid: one CTA per SM (no more than there are groups of work); after the first round the
-// CTAs on the SMs that the chain's CTAs leave free stay (at least a quarter of the GPU); with more
-// chain CTAs than SMs the chain runs in waves anyway and every prep CTA stays
-void prep_grid(ScanParams& p, size_t slots, int& ctas)
-{
-    const long long sms = sm_count() > 0 ? sm_count() : 1;
-    const long long tasks = (long long)slots * p.hv;
-    const long long need = (tasks + kPrepGroups - 1) / kPrepGroups;
-    const long long grid = sms < need ? sms : need;
-    const long long chain_ctas = (long long)p.hv * (kHeadDim / kDVS) * p.n_seq;
-    long long keep = chain_ctas < sms ? sms - chain_ctas : sms;
-    if (keep < (sms + 3) / 4) keep = (sms + 3) / 4;
-    ctas = (int)grid;
-    p.prep_keep = (int)(keep < grid ? keep : grid);
-}
-
 cudaError_t launch_scan(const ScanParams& p_in, cudaStream_t stream)
 {
     ScanParams p = p_in;
     p.epoch = next_epoch();
-    p.prep_keep = 0;
     if (p.n_seq == 0) return cudaSuccess;
     const size_t gram_smem = sizeof(GramSmem), prep_smem = sizeof(PrepSmem), chain_smem = sizeof(ChainSmem<kDVS>);
     cudaError_t e = cudaFuncSetAttribute(scan_gram_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)gram_smem);
     if (e != cudaSuccess) return e;
-    e = cudaFuncSetAttribute(scan_prep_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)(kPrepGroups * prep_smem));
+    e = cudaFuncSetAttribute(scan_prep_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)prep_smem);
     if (e != cudaSuccess) return e;
     e = cudaFuncSetAttribute(scan_chain_kernel<kDVS>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)chain_smem);
     if (e != cudaSuccess) return e;
@@ -1290,13 +1235,11 @@ cudaError_t launch_scan(const ScanParams& p_in, cudaStream_t stream)
         if (e != cudaSuccess) return e;
     } else {
         // each kernel may start while its predecessor drains and waits for it before reading
-        int prep_ctas = 1;
-        prep_grid(p, slots, prep_ctas);
         e = launch_k(scan_gram_kernel, dim3((unsigned)slots, (unsigned)p.hk), dim3(kGramThreads), gram_smem, stream,
                      true, p);
         if (e != cudaSuccess) return e;
-        e = launch_k(scan_prep_kernel, dim3((unsigned)prep_ctas), dim3(kPrepThreads * kPrepGroups),
-                     kPrepGroups * prep_smem, stream, true, p);
+        e = launch_k(scan_prep_kernel, dim3((unsigned)p.hv, (unsigned)slots), dim3(kPrepThreads), prep_smem, stream,
+                     true, p);
         if (e != cudaSuccess) return e;
     }
     return launch_k(scan_chain_kernel<kDVS>, dim3((unsigned)(p.hv * (kHeadDim / kDVS)), (unsigned)p.n_seq),
