@@ -73,6 +73,32 @@ __device__ __forceinline__ float conv4(float w0, float w1, float w2, float w3, f
     return acc;
 }
 
+// A whole block inside one sequence: no per-token checks, the output pointer
+// advances by a fixed row stride.  kNorm: a q/k head (L2-normalised).
+template <bool kNorm>
+__device__ __forceinline__ void conv_block(const uint2 (&cur)[kTokBlk], F4 win0, F4 win1, F4 win2, const float4& w0,
+                                           const float4& w1, const float4& w2, const float4& w3, float* dst,
+                                           size_t dstride, float eps)
+{
+#pragma unroll
+    for (int i = 0; i < kTokBlk; ++i) {
+        const F4 x = unpack_half4(cur[i]);
+        float y0 = silu_fast(conv4(w0.x, w0.y, w0.z, w0.w, win0.x, win1.x, win2.x, x.x));
+        float y1 = silu_fast(conv4(w1.x, w1.y, w1.z, w1.w, win0.y, win1.y, win2.y, x.y));
+        float y2 = silu_fast(conv4(w2.x, w2.y, w2.z, w2.w, win0.z, win1.z, win2.z, x.z));
+        float y3 = silu_fast(conv4(w3.x, w3.y, w3.z, w3.w, win0.w, win1.w, win2.w, x.w));
+        win0 = win1;
+        win1 = win2;
+        win2 = x;
+        if (kNorm) {
+            const float inv = rsqrtf(warp_sum(y0 * y0 + y1 * y1 + y2 * y2 + y3 * y3) + eps);
+            y0 *= inv; y1 *= inv; y2 *= inv; y3 *= inv;
+        }
+        *reinterpret_cast<float4*>(dst) = make_float4(y0, y1, y2, y3);
+        dst += dstride;
+    }
+}
+
 __global__ void __launch_bounds__(kThreads, 4)
 pre_kernel(PreParams p, int n_slots, int head_groups, int n_conv_blocks)
 {
@@ -137,6 +163,17 @@ pre_kernel(PreParams p, int n_slots, int head_groups, int n_conv_blocks)
         win2 = tap4(p, seq, seq_start, pos - 1, c);
     }
 
+    if (t_end - t_begin == kTokBlk && t_end <= seq_end) {  // the common case
+        if (vh >= 0)
+            conv_block<false>(cur, win0, win1, win2, w0, w1, w2, w3,
+                              p.vc + ((size_t)t_begin * p.hv + vh) * kHeadDim + lane * 4, (size_t)p.hv * kHeadDim,
+                              p.eps);
+        else
+            conv_block<true>(cur, win0, win1, win2, w0, w1, w2, w3,
+                             (is_k ? p.kn : p.qn) + ((size_t)t_begin * hk + (is_q ? slot : slot - hk)) * kHeadDim +
+                                 lane * 4,
+                             (size_t)hk * kHeadDim, p.eps);
+    } else {
 #pragma unroll
     for (int i = 0; i < kTokBlk; ++i) {
         const int t = t_begin + i;
@@ -174,15 +211,16 @@ pre_kernel(PreParams p, int n_slots, int head_groups, int n_conv_blocks)
         }
         *reinterpret_cast<float4*>(dst) = make_float4(y0, y1, y2, y3);
     }
+    }
 
     // gates of value head vh for the block's tokens: one lane per token
     if (vh >= 0 && lane < t_end - t_begin) {
         const int t = t_begin + lane;
         const float av = __half2float(p.a[(size_t)t * p.hv + vh]) + __ldg(p.dt_bias + vh);
         const float bv = __half2float(p.b[(size_t)t * p.hv + vh]);
-        const float sp = fmaxf(av, 0.0f) + log1pf(expf(-fabsf(av)));  // softplus
-        p.glog[(size_t)t * p.hv + vh] = -expf(__ldg(p.A_log + vh)) * sp;
-        p.beta[(size_t)t * p.hv + vh] = sigmoidf_(bv);
+        const float sp = fmaxf(av, 0.0f) + __logf(1.0f + __expf(-fabsf(av)));  // softplus
+        p.glog[(size_t)t * p.hv + vh] = -__expf(__ldg(p.A_log + vh)) * sp;
+        p.beta[(size_t)t * p.hv + vh] = __fdividef(1.0f, 1.0f + __expf(-bv));
     }
 }
 
