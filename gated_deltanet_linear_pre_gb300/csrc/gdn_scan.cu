@@ -23,7 +23,7 @@
 // so (Q S0) and (P U) land in the same TMEM lanes and O needs no exchange.
 //
 // Three kernels:
-//  * scan_gram_kernel, one CTA per (chunk, key head), fully parallel: splits
+//  * scan_gram_kernel, one CTA per (two chunks, key head), fully parallel: splits
 //    [K; Q] into the tensor-core layout (the chain's [K; Q] image), forms
 //    (K K^T ; Q K^T) in fp32, and M = [K; Q] K_prev^T against the previous
 //    chunk's keys (the chain's look-ahead operand).
@@ -245,10 +245,12 @@ __device__ __forceinline__ float warp_chunk_cumsum(float (&lam)[2], int lane)
 }
 
 // =======================================================================================
-// gram: one CTA per (chunk slot, key head): split [K; Q] (the chain's operand
-// image), (K K^T ; Q K^T) in fp32 for the prep kernel, and, for every chunk but
-// a sequence's first, M = [K; Q] K_prev^T against the previous chunk's keys
-// (the chain's look-ahead operand)
+// gram: one CTA per (pair of consecutive chunk slots, key head); per chunk: split
+// [K; Q] (the chain's operand image), (K K^T ; Q K^T) in fp32 for the prep kernel,
+// and, for every chunk but a sequence's first, M = [K; Q] K_prev^T against the
+// previous chunk's keys (the chain's look-ahead operand).  The second chunk's
+// loads overlap the first one's products, and its K_prev is the first one's K,
+// still in shared memory.
 // =======================================================================================
 constexpr int kGramThreads = 256;
 
@@ -313,22 +315,26 @@ struct RowTile {
     }
 };
 
-__global__ void __launch_bounds__(kGramThreads) scan_gram_kernel(ScanParams p)
+__global__ void __launch_bounds__(kGramThreads, 2) scan_gram_kernel(ScanParams p)
 {
     extern __shared__ __align__(1024) unsigned char smem_raw[];
     GramSmem& sm = *reinterpret_cast<GramSmem*>(smem_raw);
     const int tid = threadIdx.x, warp = tid >> 5;
     const int L = tid & 127, wg = tid >> 7;
-    const int slot = blockIdx.x, j = blockIdx.y;
+    // two consecutive chunk slots of key head j; key head fastest, so the slots complete in order
+    const int j = blockIdx.x, slot0 = 2 * (int)blockIdx.y;
     uint32_t* err = reinterpret_cast<uint32_t*>(p.workspace);
     pdl_launch_dependents();
     pdl_wait();
     // the failure record starts clean: the first CTA clears it before anything could set it (an
     // expired wait takes seconds; the later kernels of the scan start only after this one ends)
-    if (slot == 0 && j == 0 && tid == 0) *err = 0u;
-    int c0, n;
-    bool has_prev, odd;
-    if (!slot_chunk(p, slot, c0, n, &has_prev, &odd)) return;  // unused slot (whole CTA)
+    if (slot0 == 0 && j == 0 && tid == 0) *err = 0u;
+    int c0[2], n[2];
+    bool has_prev[2], odd[2], used[2];
+    used[0] = slot_chunk(p, slot0, c0[0], n[0], &has_prev[0], &odd[0]);
+    used[1] = (size_t)(slot0 + 1) < n_slots(p.T, p.n_seq) &&
+              slot_chunk(p, slot0 + 1, c0[1], n[1], &has_prev[1], &odd[1]);
+    if (!used[0] && !used[1]) return;  // unused slots (whole CTA)
 
     if (warp == 0) umma::tmem_alloc(&sm.tmem_base, 128);
     if (tid == 0) {
@@ -336,57 +342,91 @@ __global__ void __launch_bounds__(kGramThreads) scan_gram_kernel(ScanParams p)
         sm.abort_flag = 0;
     }
     const size_t rs = (size_t)p.hk * kHeadDim;
-    unsigned char* img = kq_image(p, slot, j);
-    // K and Q loads in flight together, the previous chunk's K (always full) behind them;
-    // image rows in the chunk's stacking order: [K; Q] for even chunks, [Q; K] for odd ones
-    {
-        RowTile<kGramThreads> tk, tq;
-        tk.fetch(p.kn + (size_t)c0 * rs + (size_t)j * kHeadDim, rs, n, tid);
-        tq.fetch(p.qn + (size_t)c0 * rs + (size_t)j * kHeadDim, rs, n, tid);
-        tk.store(sm.akq[0], sm.akq[1], 0, 128, img, odd ? 64 : 0, tid);
-        if (has_prev) tk.fetch(p.kn + (size_t)(c0 - kChunk) * rs + (size_t)j * kHeadDim, rs, kChunk, tid);
-        tq.store(sm.akq[0], sm.akq[1], 64, 128, img, odd ? 0 : 64, tid);
-        if (has_prev) tk.store(sm.bkp[0], sm.bkp[1], 0, 128, nullptr, 0, tid);
+    const float* kbase = p.kn + (size_t)j * kHeadDim;
+    const float* qbase = p.qn + (size_t)j * kHeadDim;
+    RowTile<kGramThreads> tk, tq;
+    {   // K and Q loads of the first used slot in flight together
+        const int f = used[0] ? 0 : 1;
+        tk.fetch(kbase + (size_t)(f ? c0[1] : c0[0]) * rs, rs, f ? n[1] : n[0], tid);
+        tq.fetch(qbase + (size_t)(f ? c0[1] : c0[0]) * rs, rs, f ? n[1] : n[0], tid);
     }
-    umma::fence_proxy_async();
-    umma::fence_before_sync();
-    __syncthreads();
-    umma::fence_after_sync();
-    const uint32_t tmem = sm.tmem_base;
-    // (K K^T ; Q K^T) = [K; Q] K^T  (B = the K rows of the same tile);  M = [K; Q] K_prev^T
-    if (tid == 0) {
-        const uint32_t a_hi = umma::smem_u32(sm.akq[0]), a_lo = umma::smem_u32(sm.akq[1]);
-        mma_split(tmem, a_hi, a_lo, 128, 2048, 256, a_hi, a_lo, 2048, 256, 8, umma::idesc_bf16(128, 64, false, false));
-        if (has_prev)
-            mma_split(tmem + 64, a_hi, a_lo, 128, 2048, 256, umma::smem_u32(sm.bkp[0]), umma::smem_u32(sm.bkp[1]), 2048,
-                      256, 8, umma::idesc_bf16(128, 64, false, false));
-        umma::commit(&sm.mbar);
-    }
-    if (!umma::mbar_wait(&sm.mbar, 0)) { sm.abort_flag = 1; atomicOr(err, kErrTimeout); }
-    __syncthreads();
-    if (!sm.abort_flag) {
+    uint32_t phase = 0;
+#pragma unroll
+    for (int t = 0; t < 2; ++t) {
+        if (!used[t]) continue;
+        const int slot = slot0 + t;
+        unsigned char* img = kq_image(p, slot, j);
+        // the second chunk's predecessor is the first one, whose split K is still in the tile
+        const bool prev_here = t == 1 && used[0] && has_prev[1];
+        if (prev_here) {
+            const uint4* src0 = reinterpret_cast<const uint4*>(sm.akq[0]);
+            const uint4* src1 = reinterpret_cast<const uint4*>(sm.akq[1]);
+            uint4* dst0 = reinterpret_cast<uint4*>(sm.bkp[0]);
+            uint4* dst1 = reinterpret_cast<uint4*>(sm.bkp[1]);
+#pragma unroll
+            for (int q = 0; q < (64 * 128 * 2) / (16 * kGramThreads); ++q) {
+                dst0[tid + kGramThreads * q] = src0[tid + kGramThreads * q];
+                dst1[tid + kGramThreads * q] = src1[tid + kGramThreads * q];
+            }
+            __syncthreads();
+        }
+        // image rows in the chunk's stacking order: [K; Q] for even chunks, [Q; K] for odd ones
+        tk.store(sm.akq[0], sm.akq[1], 0, 128, img, odd[t] ? 64 : 0, tid);
+        if (has_prev[t] && !prev_here) tk.fetch(kbase + (size_t)(c0[t] - kChunk) * rs, rs, kChunk, tid);
+        tq.store(sm.akq[0], sm.akq[1], 64, 128, img, odd[t] ? 0 : 64, tid);
+        if (has_prev[t] && !prev_here) tk.store(sm.bkp[0], sm.bkp[1], 0, 128, nullptr, 0, tid);
+        umma::fence_proxy_async();
+        umma::fence_before_sync();
+        __syncthreads();
         umma::fence_after_sync();
-        const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
-        float d[32];
-        umma::tmem_ld32(tmem + lane_off + 32 * wg, d);
-        umma::tmem_wait_ld();
-        float4* dst = reinterpret_cast<float4*>(gram_rows(p, slot, j) + L * 64 + 32 * wg);
-#pragma unroll
-        for (int q = 0; q < 8; ++q) dst[q] = make_float4(d[4 * q], d[4 * q + 1], d[4 * q + 2], d[4 * q + 3]);
-        if (has_prev) {  // M rows -> split K-major image (K = 64 tokens of the previous chunk), Q rows first for odd chunks
-            const int mrow = odd ? (L ^ 64) : L;
-            umma::tmem_ld32(tmem + lane_off + 64 + 32 * wg, d);
+        const uint32_t tmem = sm.tmem_base;
+        // (K K^T ; Q K^T) = [K; Q] K^T  (B = the K rows of the same tile);  M = [K; Q] K_prev^T
+        if (tid == 0) {
+            const uint32_t a_hi = umma::smem_u32(sm.akq[0]), a_lo = umma::smem_u32(sm.akq[1]);
+            mma_split(tmem, a_hi, a_lo, 128, 2048, 256, a_hi, a_lo, 2048, 256, 8,
+                      umma::idesc_bf16(128, 64, false, false));
+            if (has_prev[t])
+                mma_split(tmem + 64, a_hi, a_lo, 128, 2048, 256, umma::smem_u32(sm.bkp[0]), umma::smem_u32(sm.bkp[1]),
+                          2048, 256, 8, umma::idesc_bf16(128, 64, false, false));
+            umma::commit(&sm.mbar);
+        }
+        // the second chunk's K and Q loads fly while this chunk's products and epilogue run
+        if (t == 0 && used[1]) {
+            tk.fetch(kbase + (size_t)c0[1] * rs, rs, n[1], tid);
+            tq.fetch(qbase + (size_t)c0[1] * rs, rs, n[1], tid);
+        }
+        if (!umma::mbar_wait(&sm.mbar, phase)) { sm.abort_flag = 1; atomicOr(err, kErrTimeout); }
+        phase ^= 1u;
+        __syncthreads();
+        if (sm.abort_flag) break;
+        umma::fence_after_sync();
+        {
+            const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
+            float d[32];
+            umma::tmem_ld32(tmem + lane_off + 32 * wg, d);
             umma::tmem_wait_ld();
-            unsigned char* mimg = m_image(p, slot, j);
+            float4* dst = reinterpret_cast<float4*>(gram_rows(p, slot, j) + L * 64 + 32 * wg);
 #pragma unroll
-            for (int q = 0; q < 4; ++q) {
-                uint4 vh, vl;
-                split8(d + 8 * q, vh, vl);
-                const int off = kmaj(mrow, 32 * wg + 8 * q, 64);
-                *reinterpret_cast<uint4*>(mimg + off * 2) = vh;
-                *reinterpret_cast<uint4*>(mimg + kMBytes / 2 + off * 2) = vl;
+            for (int q = 0; q < 8; ++q) dst[q] = make_float4(d[4 * q], d[4 * q + 1], d[4 * q + 2], d[4 * q + 3]);
+            if (has_prev[t]) {  // M rows -> split K-major image (K = 64 tokens of the previous chunk), Q rows first for odd chunks
+                const int mrow = odd[t] ? (L ^ 64) : L;
+                umma::tmem_ld32(tmem + lane_off + 64 + 32 * wg, d);
+                umma::tmem_wait_ld();
+                unsigned char* mimg = m_image(p, slot, j);
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    uint4 vh, vl;
+                    split8(d + 8 * q, vh, vl);
+                    const int off = kmaj(mrow, 32 * wg + 8 * q, 64);
+                    *reinterpret_cast<uint4*>(mimg + off * 2) = vh;
+                    *reinterpret_cast<uint4*>(mimg + kMBytes / 2 + off * 2) = vl;
+                }
             }
         }
+        // TMEM read out and the tiles consumed before the next chunk overwrites them
+        umma::fence_before_sync();
+        __syncthreads();
+        umma::fence_after_sync();
     }
     umma::fence_before_sync();
     __syncthreads();
@@ -1235,8 +1275,8 @@ cudaError_t launch_scan(const ScanParams& p_in, cudaStream_t stream)
         if (e != cudaSuccess) return e;
     } else {
         // each kernel may start while its predecessor drains and waits for it before reading
-        e = launch_k(scan_gram_kernel, dim3((unsigned)slots, (unsigned)p.hk), dim3(kGramThreads), gram_smem, stream,
-                     true, p);
+        e = launch_k(scan_gram_kernel, dim3((unsigned)p.hk, (unsigned)((slots + 1) / 2)), dim3(kGramThreads), gram_smem,
+                     stream, true, p);
         if (e != cudaSuccess) return e;
         e = launch_k(scan_prep_kernel, dim3((unsigned)p.hv, (unsigned)slots), dim3(kPrepThreads), prep_smem, stream,
                      true, p);
