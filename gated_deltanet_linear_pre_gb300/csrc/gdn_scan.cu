@@ -475,15 +475,29 @@ __global__ void __launch_bounds__(kPrepThreads, 4) scan_prep_kernel(ScanParams p
         umma::mbar_init(&sm.mbar, 1);
         sm.abort_flag = 0;
     }
-    // raw gates of the value head (warp 0)
-    float raw_lam[2] = {0.f, 0.f}, raw_beta[2] = {0.f, 0.f};
+    // gates of value head h (warp 0): running log-decay G and beta, for this CTA and the chain's
+    // copy; computed while the other warps' gram-row loads are in flight, so one barrier serves both
     if (warp == 0) {
+        float lam[2], bt[2];
 #pragma unroll
         for (int q = 0; q < 2; ++q) {
             const int t = lane + 32 * q;
-            raw_lam[q] = t < n ? __ldg(p.glog + (size_t)(c0 + t) * p.hv + h) : 0.0f;
-            raw_beta[q] = t < n ? __ldg(p.beta + (size_t)(c0 + t) * p.hv + h) : 0.0f;
+            lam[q] = t < n ? fmaxf(__ldg(p.glog + (size_t)(c0 + t) * p.hv + h), kLamFloor) : 0.0f;
+            bt[q] = t < n ? __ldg(p.beta + (size_t)(c0 + t) * p.hv + h) : 0.0f;
         }
+        const float GL = warp_chunk_cumsum(lam, lane);
+        sm.G[lane] = lam[0];
+        sm.G[lane + 32] = lam[1];
+        sm.beta[lane] = bt[0];
+        sm.beta[lane + 32] = bt[1];
+        ChainGates* gr = gate_row(p, slot, h);
+        gr->eG[lane] = __expf(lam[0]);
+        gr->eG[lane + 32] = __expf(lam[1]);
+        gr->kdec[lane] = __expf(GL - lam[0]);
+        gr->kdec[lane + 32] = __expf(GL - lam[1]);
+        gr->beta[lane] = bt[0];
+        gr->beta[lane + 32] = bt[1];
+        if (lane == 0) gr->gL = __expf(GL);
     }
     // this thread's 32 entries of the gram rows of the key head: row L (K K^T for
     // L < 64, Q K^T for L >= 64), columns [32 wg, 32 wg + 32)
@@ -507,28 +521,6 @@ __global__ void __launch_bounds__(kPrepThreads, 4) scan_prep_kernel(ScanParams p
     float* Tm = sm.T;
 
     {
-        // gates of value head h: running log-decay G and beta
-        if (warp == 0) {
-            float lam[2];
-#pragma unroll
-            for (int q = 0; q < 2; ++q) lam[q] = (lane + 32 * q) < n ? fmaxf(raw_lam[q], kLamFloor) : 0.0f;
-            const float b0 = raw_beta[0], b1 = raw_beta[1];
-            const float GL = warp_chunk_cumsum(lam, lane);
-            sm.G[lane] = lam[0];
-            sm.G[lane + 32] = lam[1];
-            sm.beta[lane] = b0;
-            sm.beta[lane + 32] = b1;
-            ChainGates* gr = gate_row(p, slot, h);  // the chain's copy
-            gr->eG[lane] = __expf(lam[0]);
-            gr->eG[lane + 32] = __expf(lam[1]);
-            gr->kdec[lane] = __expf(GL - lam[0]);
-            gr->kdec[lane + 32] = __expf(GL - lam[1]);
-            gr->beta[lane] = b0;
-            gr->beta[lane + 32] = b1;
-            if (lane == 0) gr->gL = __expf(GL);
-        }
-        __syncthreads();
-
         // A (fp32, rows L < 64) and P (split, rows L - 64 for L >= 64), columns of wg
         {
             const int i = L & 63, cb = 32 * wg;
@@ -572,7 +564,9 @@ __global__ void __launch_bounds__(kPrepThreads, 4) scan_prep_kernel(ScanParams p
                 }
             }
         }
-        __syncthreads();
+        // A's writers (warps 0, 1, 4, 5) meet before the diagonal solve (warps 0, 1); the P warps
+        // join at the barrier after it
+        if (L < 64) asm volatile("bar.sync 1, 128;" ::: "memory");
 
         // T = (I + A)^-1 (A strictly lower), recursively by halves: T = [[T1, 0], [-T2 A21 T1, T2]].
         // (1) the four 16x16 diagonal blocks by forward substitution (thread (b, c): column c;
