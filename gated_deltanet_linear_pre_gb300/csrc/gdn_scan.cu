@@ -205,6 +205,22 @@ __device__ __forceinline__ bool flag_wait(const unsigned long long* f, unsigned 
     return true;
 }
 
+// prep's task counter and count of CTAs done with round one (header words 16 and 17), cleared by gram
+__device__ __forceinline__ unsigned int* prep_counter(const ScanParams& p)
+{
+    return reinterpret_cast<unsigned int*>(static_cast<unsigned char*>(p.workspace) + 64);
+}
+
+// whether this CTA's SM keeps taking prep tasks after round one: the SMs in the first
+// prep_keep / prep_sms of the SM-id range (ids may leave gaps up to %nsmid)
+__device__ __forceinline__ bool prep_sm_stays(const ScanParams& p)
+{
+    uint32_t smid, nsmid;
+    asm volatile("mov.u32 %0, %%smid;" : "=r"(smid));
+    asm volatile("mov.u32 %0, %%nsmid;" : "=r"(nsmid));
+    return (unsigned long long)smid * (unsigned)p.prep_sms < (unsigned long long)p.prep_keep * nsmid;
+}
+
 __device__ __forceinline__ ChainGates* gate_row(const ScanParams& p, size_t slot, int h)
 {
     return reinterpret_cast<ChainGates*>(am_image(p, slot, h) + kAmBytes);
@@ -326,9 +342,14 @@ __global__ void __launch_bounds__(kGramThreads, 2) scan_gram_kernel(ScanParams p
     uint32_t* err = reinterpret_cast<uint32_t*>(p.workspace);
     pdl_launch_dependents();
     pdl_wait();
-    // the failure record starts clean: the first CTA clears it before anything could set it (an
-    // expired wait takes seconds; the later kernels of the scan start only after this one ends)
-    if (slot0 == 0 && j == 0 && tid == 0) *err = 0u;
+    // the failure record and prep's task counter start clean: the first CTA clears them before
+    // anything could use them (an expired wait takes seconds; the later kernels of the scan
+    // start only after this one ends)
+    if (slot0 == 0 && j == 0 && tid == 0) {
+        *err = 0u;
+        prep_counter(p)[0] = 0u;
+        prep_counter(p)[1] = 0u;
+    }
     int c0[2], n[2];
     bool has_prev[2], odd[2], used[2];
     used[0] = slot_chunk(p, slot0, c0[0], n[0], &has_prev[0], &odd[0]);
@@ -449,6 +470,7 @@ struct __align__(1024) PrepSmem {
     float G[64], beta[64];
     uint32_t tmem_base;
     int abort_flag;
+    uint32_t next[2];  // the next task, broadcast from thread 0 (alternating slots)
     uint64_t mbar;
 };
 
@@ -458,16 +480,10 @@ __global__ void __launch_bounds__(kPrepThreads, 4) scan_prep_kernel(ScanParams p
     PrepSmem& sm = *reinterpret_cast<PrepSmem*>(smem_raw);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int L = tid & 127, wg = tid >> 7;  // TMEM lane, column half
-    // value head fastest: chunk slots complete in order across all heads, so the chain (which
-    // consumes chunk after chunk and starts during prep's last wave) finds its early chunks ready
-    const int h = blockIdx.x, slot = blockIdx.y, j = h / (p.hv / p.hk);
     uint32_t* err = reinterpret_cast<uint32_t*>(p.workspace);
     pdl_launch_dependents();
     pdl_wait();
     constexpr int ST = 68;  // fp32 row stride of A and T
-    int c0, n;
-    bool odd;
-    if (!slot_chunk(p, slot, c0, n, nullptr, &odd)) return;  // unused slot (whole CTA)
     const float qscale = rsqrtf((float)kHeadDim);
 
     if (warp == 0) umma::tmem_alloc(&sm.tmem_base, 64);
@@ -475,257 +491,283 @@ __global__ void __launch_bounds__(kPrepThreads, 4) scan_prep_kernel(ScanParams p
         umma::mbar_init(&sm.mbar, 1);
         sm.abort_flag = 0;
     }
-    // gates of value head h (warp 0): running log-decay G and beta, for this CTA and the chain's
-    // copy; computed while the other warps' gram-row loads are in flight, so one barrier serves both
-    if (warp == 0) {
-        float lam[2], bt[2];
-#pragma unroll
-        for (int q = 0; q < 2; ++q) {
-            const int t = lane + 32 * q;
-            lam[q] = t < n ? fmaxf(__ldg(p.glog + (size_t)(c0 + t) * p.hv + h), kLamFloor) : 0.0f;
-            bt[q] = t < n ? __ldg(p.beta + (size_t)(c0 + t) * p.hv + h) : 0.0f;
-        }
-        const float GL = warp_chunk_cumsum(lam, lane);
-        sm.G[lane] = lam[0];
-        sm.G[lane + 32] = lam[1];
-        sm.beta[lane] = bt[0];
-        sm.beta[lane + 32] = bt[1];
-        ChainGates* gr = gate_row(p, slot, h);
-        gr->eG[lane] = __expf(lam[0]);
-        gr->eG[lane + 32] = __expf(lam[1]);
-        gr->kdec[lane] = __expf(GL - lam[0]);
-        gr->kdec[lane + 32] = __expf(GL - lam[1]);
-        gr->beta[lane] = bt[0];
-        gr->beta[lane + 32] = bt[1];
-        if (lane == 0) gr->gL = __expf(GL);
-    }
-    // this thread's 32 entries of the gram rows of the key head: row L (K K^T for
-    // L < 64, Q K^T for L >= 64), columns [32 wg, 32 wg + 32)
-    float d[32];
-    {
-        const float4* src = reinterpret_cast<const float4*>(gram_rows(p, slot, j) + L * 64 + 32 * wg);
-#pragma unroll
-        for (int q = 0; q < 8; ++q) {
-            const float4 x = __ldg(src + q);
-            d[4 * q] = x.x; d[4 * q + 1] = x.y; d[4 * q + 2] = x.z; d[4 * q + 3] = x.w;
-        }
-    }
-    __syncthreads();
-    umma::fence_after_sync();
-    const uint32_t tmem = sm.tmem_base;
-    const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
-    const uint32_t a_p[2] = {umma::smem_u32(sm.ap[0]), umma::smem_u32(sm.ap[1])};
-    const uint32_t b_t[2] = {umma::smem_u32(sm.u.bt[0]), umma::smem_u32(sm.u.bt[1])};
     uint32_t phase = 0;
-    float* A = sm.u.A;
-    float* Tm = sm.T;
-
-    {
-        // A (fp32, rows L < 64) and P (split, rows L - 64 for L >= 64), columns of wg
-        {
-            const int i = L & 63, cb = 32 * wg;
-            const float Gi = sm.G[i];
-            const float4* G4 = reinterpret_cast<const float4*>(sm.G + cb);
-            // (a warp's 32 rows lie in one half, so for rows < 32 the columns of wg = 1 are all above
-            // the diagonal: A's block there is never read, P's is zero)
-            if (L < 64) {
-                const float bi = sm.beta[i];
-                if (cb <= i)
+    // Tasks (chunk slot, value head) in slot order, the value head fastest, so the chunk slots
+    // complete in order across all heads.  Round one: CTA b takes task b.  After it only the CTAs
+    // on the SMs chosen to stay take further tasks, in order, from the counter that gram cleared;
+    // the others exit, and their SMs take the chain's CTAs, which start on the first round's
+    // chunks while the remaining prep CTAs keep ahead of them.
+    const unsigned n_tasks = (unsigned)(n_slots(p.T, p.n_seq) * (size_t)p.hv);
+    bool stays = prep_sm_stays(p);
+    unsigned int* counter = prep_counter(p);
+    bool first = true;
+    int nx = 0;
+    for (unsigned task = blockIdx.x; task < n_tasks;) {
+        const int h = (int)(task % (unsigned)p.hv), slot = (int)(task / (unsigned)p.hv), j = h / (p.hv / p.hk);
+        int c0, n;
+        bool odd;
+        if (slot_chunk(p, slot, c0, n, nullptr, &odd)) {
+            // gates of value head h (warp 0): running log-decay G and beta, for this CTA and the chain's
+            // copy; computed while the other warps' gram-row loads are in flight, so one barrier serves both
+            if (warp == 0) {
+                float lam[2], bt[2];
+#pragma unroll
+                for (int q = 0; q < 2; ++q) {
+                    const int t = lane + 32 * q;
+                    lam[q] = t < n ? fmaxf(__ldg(p.glog + (size_t)(c0 + t) * p.hv + h), kLamFloor) : 0.0f;
+                    bt[q] = t < n ? __ldg(p.beta + (size_t)(c0 + t) * p.hv + h) : 0.0f;
+                }
+                const float GL = warp_chunk_cumsum(lam, lane);
+                sm.G[lane] = lam[0];
+                sm.G[lane + 32] = lam[1];
+                sm.beta[lane] = bt[0];
+                sm.beta[lane + 32] = bt[1];
+                ChainGates* gr = gate_row(p, slot, h);
+                gr->eG[lane] = __expf(lam[0]);
+                gr->eG[lane + 32] = __expf(lam[1]);
+                gr->kdec[lane] = __expf(GL - lam[0]);
+                gr->kdec[lane + 32] = __expf(GL - lam[1]);
+                gr->beta[lane] = bt[0];
+                gr->beta[lane + 32] = bt[1];
+                if (lane == 0) gr->gL = __expf(GL);
+            }
+            // this thread's 32 entries of the gram rows of the key head: row L (K K^T for
+            // L < 64, Q K^T for L >= 64), columns [32 wg, 32 wg + 32)
+            float d[32];
+            {
+                const float4* src = reinterpret_cast<const float4*>(gram_rows(p, slot, j) + L * 64 + 32 * wg);
 #pragma unroll
                 for (int q = 0; q < 8; ++q) {
-                    const float4 g = G4[q];
-                    const float gg[4] = {g.x, g.y, g.z, g.w};
-                    float a[4];
-#pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        const int jj = cb + 4 * q + e;
-                        a[e] = jj < i ? bi * __expf(Gi - gg[e]) * d[4 * q + e] : 0.0f;
-                    }
-                    *reinterpret_cast<float4*>(&A[i * ST + cb + 4 * q]) = make_float4(a[0], a[1], a[2], a[3]);
-                }
-            } else if (cb > i) {
-#pragma unroll
-                for (int q = 0; q < 4; ++q) {
-                    *reinterpret_cast<uint4*>(&sm.ap[0][kmaj(i, cb + 8 * q, 64)]) = make_uint4(0u, 0u, 0u, 0u);
-                    *reinterpret_cast<uint4*>(&sm.ap[1][kmaj(i, cb + 8 * q, 64)]) = make_uint4(0u, 0u, 0u, 0u);
-                }
-            } else {
-#pragma unroll
-                for (int q = 0; q < 4; ++q) {
-                    const float4 ga = G4[2 * q], gb = G4[2 * q + 1];
-                    const float gg[8] = {ga.x, ga.y, ga.z, ga.w, gb.x, gb.y, gb.z, gb.w};
-                    float pr[8];
-#pragma unroll
-                    for (int e = 0; e < 8; ++e) {
-                        const int jj = cb + 8 * q + e;
-                        pr[e] = jj <= i ? __expf(Gi - gg[e]) * d[8 * q + e] * qscale : 0.0f;
-                    }
-                    store_split8(&sm.ap[0][kmaj(i, cb + 8 * q, 64)], &sm.ap[1][kmaj(i, cb + 8 * q, 64)], pr);
+                    const float4 x = __ldg(src + q);
+                    d[4 * q] = x.x; d[4 * q + 1] = x.y; d[4 * q + 2] = x.z; d[4 * q + 3] = x.w;
                 }
             }
-        }
-        // A's writers (warps 0, 1, 4, 5) meet before the diagonal solve (warps 0, 1); the P warps
-        // join at the barrier after it
-        if (L < 64) asm volatile("bar.sync 1, 128;" ::: "memory");
+            __syncthreads();
+            umma::fence_after_sync();
+            const uint32_t tmem = sm.tmem_base;
+            const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
+            const uint32_t a_p[2] = {umma::smem_u32(sm.ap[0]), umma::smem_u32(sm.ap[1])};
+            const uint32_t b_t[2] = {umma::smem_u32(sm.u.bt[0]), umma::smem_u32(sm.u.bt[1])};
+            float* A = sm.u.A;
+            float* Tm = sm.T;
 
-        // T = (I + A)^-1 (A strictly lower), recursively by halves: T = [[T1, 0], [-T2 A21 T1, T2]].
-        // (1) the four 16x16 diagonal blocks by forward substitution (thread (b, c): column c;
-        //     col[r] = [r == c] - sum_{m<r} A[r][m] col[m], the entries above c come out zero);
-        // (2) the two 32x32 halves: T_(b,b-1) = -T_(b,b) A_(b,b-1) T_(b-1,b-1) for b = 1, 3;
-        // (3) the 32x32 off-diagonal block: T21 = -T2 (A21 T1).
-        // Only the block lower triangle of T is written; readers treat the rest as zero.
-        {
-            if (tid < 64) {
-                const int b = tid >> 4, c = tid & 15, o = 16 * b;
-                float col[16];
+            {
+                // A (fp32, rows L < 64) and P (split, rows L - 64 for L >= 64), columns of wg
+                {
+                    const int i = L & 63, cb = 32 * wg;
+                    const float Gi = sm.G[i];
+                    const float4* G4 = reinterpret_cast<const float4*>(sm.G + cb);
+                    // (a warp's 32 rows lie in one half, so for rows < 32 the columns of wg = 1 are all above
+                    // the diagonal: A's block there is never read, P's is zero)
+                    if (L < 64) {
+                        const float bi = sm.beta[i];
+                        if (cb <= i)
 #pragma unroll
-                for (int r = 0; r < 16; ++r) {
-                    float acc = (r == c) ? 1.0f : 0.0f;
+                        for (int q = 0; q < 8; ++q) {
+                            const float4 g = G4[q];
+                            const float gg[4] = {g.x, g.y, g.z, g.w};
+                            float a[4];
 #pragma unroll
-                    for (int m4 = 0; m4 < r; m4 += 4) {
-                        const float4 a4 = *reinterpret_cast<const float4*>(&A[(o + r) * ST + o + m4]);
-                        if (m4 + 0 < r) acc = fmaf(-a4.x, col[m4 + 0], acc);
-                        if (m4 + 1 < r) acc = fmaf(-a4.y, col[m4 + 1], acc);
-                        if (m4 + 2 < r) acc = fmaf(-a4.z, col[m4 + 2], acc);
-                        if (m4 + 3 < r) acc = fmaf(-a4.w, col[m4 + 3], acc);
+                            for (int e = 0; e < 4; ++e) {
+                                const int jj = cb + 4 * q + e;
+                                a[e] = jj < i ? bi * __expf(Gi - gg[e]) * d[4 * q + e] : 0.0f;
+                            }
+                            *reinterpret_cast<float4*>(&A[i * ST + cb + 4 * q]) = make_float4(a[0], a[1], a[2], a[3]);
+                        }
+                    } else if (cb > i) {
+#pragma unroll
+                        for (int q = 0; q < 4; ++q) {
+                            *reinterpret_cast<uint4*>(&sm.ap[0][kmaj(i, cb + 8 * q, 64)]) = make_uint4(0u, 0u, 0u, 0u);
+                            *reinterpret_cast<uint4*>(&sm.ap[1][kmaj(i, cb + 8 * q, 64)]) = make_uint4(0u, 0u, 0u, 0u);
+                        }
+                    } else {
+#pragma unroll
+                        for (int q = 0; q < 4; ++q) {
+                            const float4 ga = G4[2 * q], gb = G4[2 * q + 1];
+                            const float gg[8] = {ga.x, ga.y, ga.z, ga.w, gb.x, gb.y, gb.z, gb.w};
+                            float pr[8];
+#pragma unroll
+                            for (int e = 0; e < 8; ++e) {
+                                const int jj = cb + 8 * q + e;
+                                pr[e] = jj <= i ? __expf(Gi - gg[e]) * d[8 * q + e] * qscale : 0.0f;
+                            }
+                            store_split8(&sm.ap[0][kmaj(i, cb + 8 * q, 64)], &sm.ap[1][kmaj(i, cb + 8 * q, 64)], pr);
+                        }
                     }
-                    col[r] = acc;
                 }
-#pragma unroll
-                for (int r = 0; r < 16; ++r) Tm[(o + r) * ST + o + c] = col[r];
-            }
-            __syncthreads();
-            {   // (2) pairs b = 1 (rows 16-31 x cols 0-15) and b = 3 (rows 48-63 x cols 32-47)
-                const int pr = tid >> 7, r = (tid >> 3) & 15, c2 = 2 * (tid & 7);
-                const int ro = 32 * pr + 16, co = 32 * pr;  // block (b, b-1) origin
-                float w0 = 0.f, w1 = 0.f;
-#pragma unroll
-                for (int m = 0; m < 16; ++m) {
-                    const float a = A[(ro + r) * ST + co + m];
-                    const float2 t2 = *reinterpret_cast<const float2*>(&Tm[(co + m) * ST + co + c2]);
-                    w0 = fmaf(a, t2.x, w0);
-                    w1 = fmaf(a, t2.y, w1);
-                }
-                *reinterpret_cast<float2*>(&sm.W[pr * 256 + r * 16 + c2]) = make_float2(w0, w1);
-                __syncthreads();
-                float t0 = 0.f, t1 = 0.f;
-#pragma unroll
-                for (int m = 0; m < 16; ++m) {
-                    const float a = Tm[(ro + r) * ST + ro + m];
-                    const float2 w2 = *reinterpret_cast<const float2*>(&sm.W[pr * 256 + m * 16 + c2]);
-                    t0 = fmaf(a, w2.x, t0);
-                    t1 = fmaf(a, w2.y, t1);
-                }
-                *reinterpret_cast<float2*>(&Tm[(ro + r) * ST + co + c2]) = make_float2(-t0, -t1);
-            }
-            __syncthreads();
-            {   // (3) rows 32-63 x cols 0-31; T1 and T2 are block lower triangular.  Both loops are
-                // fully unrolled; the structurally zero 16-wide blocks (never written, so they may
-                // hold any bits) are selected away, not multiplied, so every load is in flight at once
-                const int r = tid >> 3, c4 = 4 * (tid & 7);
-                const bool hi_c = (c4 >> 4) != 0;  // T1[m][c] for m < 16 is zero when c >= 16
-                const float4 z4 = make_float4(0.f, 0.f, 0.f, 0.f);
-                float acc[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-                for (int m = 0; m < 32; ++m) {
-                    const float a = A[(32 + r) * ST + m];
-                    const float4 t4l = *reinterpret_cast<const float4*>(&Tm[m * ST + c4]);
-                    const float4 t4 = (m < 16 && hi_c) ? z4 : t4l;
-                    acc[0] = fmaf(a, t4.x, acc[0]); acc[1] = fmaf(a, t4.y, acc[1]);
-                    acc[2] = fmaf(a, t4.z, acc[2]); acc[3] = fmaf(a, t4.w, acc[3]);
-                }
-                *reinterpret_cast<float4*>(&sm.W[r * 32 + c4]) = make_float4(acc[0], acc[1], acc[2], acc[3]);
-                __syncthreads();
-                const bool lo_r = (r >> 4) == 0;  // T2[r][m] for m >= 16 is zero when r < 16
-                float t[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-                for (int m = 0; m < 32; ++m) {
-                    const float al = Tm[(32 + r) * ST + 32 + m];
-                    const float a = (m >= 16 && lo_r) ? 0.0f : al;
-                    const float4 w4 = *reinterpret_cast<const float4*>(&sm.W[m * 32 + c4]);
-                    t[0] = fmaf(a, w4.x, t[0]); t[1] = fmaf(a, w4.y, t[1]);
-                    t[2] = fmaf(a, w4.z, t[2]); t[3] = fmaf(a, w4.w, t[3]);
-                }
-                *reinterpret_cast<float4*>(&Tm[(32 + r) * ST + c4]) = make_float4(-t[0], -t[1], -t[2], -t[3]);
-            }
-            __syncthreads();
-            // T -> MN-major B tile (element (n = column, k = row)); row fastest across
-            // lanes; column groups right of the row's diagonal block are zero
-            for (int u = tid; u < 64 * 8; u += kPrepThreads) {
-                const int m = u & 63, g = u >> 6;
-                float tr[8];
-                if ((g >> 1) <= (m >> 4)) {
-                    const float4 x0 = *reinterpret_cast<const float4*>(&Tm[m * ST + g * 8]);
-                    const float4 x1 = *reinterpret_cast<const float4*>(&Tm[m * ST + g * 8 + 4]);
-                    tr[0] = x0.x; tr[1] = x0.y; tr[2] = x0.z; tr[3] = x0.w;
-                    tr[4] = x1.x; tr[5] = x1.y; tr[6] = x1.z; tr[7] = x1.w;
-                } else {
-#pragma unroll
-                    for (int e = 0; e < 8; ++e) tr[e] = 0.0f;
-                }
-                store_split8(&sm.u.bt[0][mnmaj(g * 8, m, 64)], &sm.u.bt[1][mnmaj(g * 8, m, 64)], tr);
-            }
-        }
-        umma::fence_proxy_async();
-        umma::fence_before_sync();
-        __syncthreads();
-        umma::fence_after_sync();
+                // A's writers (warps 0, 1, 4, 5) meet before the diagonal solve (warps 0, 1); the P warps
+                // join at the barrier after it
+                if (L < 64) asm volatile("bar.sync 1, 128;" ::: "memory");
 
-        // P T  (M = 128 descriptor over the 64-row P tile; rows 64-127 of the product unused)
+                // T = (I + A)^-1 (A strictly lower), recursively by halves: T = [[T1, 0], [-T2 A21 T1, T2]].
+                // (1) the four 16x16 diagonal blocks by forward substitution (thread (b, c): column c;
+                //     col[r] = [r == c] - sum_{m<r} A[r][m] col[m], the entries above c come out zero);
+                // (2) the two 32x32 halves: T_(b,b-1) = -T_(b,b) A_(b,b-1) T_(b-1,b-1) for b = 1, 3;
+                // (3) the 32x32 off-diagonal block: T21 = -T2 (A21 T1).
+                // Only the block lower triangle of T is written; readers treat the rest as zero.
+                {
+                    if (tid < 64) {
+                        const int b = tid >> 4, c = tid & 15, o = 16 * b;
+                        float col[16];
+#pragma unroll
+                        for (int r = 0; r < 16; ++r) {
+                            float acc = (r == c) ? 1.0f : 0.0f;
+#pragma unroll
+                            for (int m4 = 0; m4 < r; m4 += 4) {
+                                const float4 a4 = *reinterpret_cast<const float4*>(&A[(o + r) * ST + o + m4]);
+                                if (m4 + 0 < r) acc = fmaf(-a4.x, col[m4 + 0], acc);
+                                if (m4 + 1 < r) acc = fmaf(-a4.y, col[m4 + 1], acc);
+                                if (m4 + 2 < r) acc = fmaf(-a4.z, col[m4 + 2], acc);
+                                if (m4 + 3 < r) acc = fmaf(-a4.w, col[m4 + 3], acc);
+                            }
+                            col[r] = acc;
+                        }
+#pragma unroll
+                        for (int r = 0; r < 16; ++r) Tm[(o + r) * ST + o + c] = col[r];
+                    }
+                    __syncthreads();
+                    {   // (2) pairs b = 1 (rows 16-31 x cols 0-15) and b = 3 (rows 48-63 x cols 32-47)
+                        const int pr = tid >> 7, r = (tid >> 3) & 15, c2 = 2 * (tid & 7);
+                        const int ro = 32 * pr + 16, co = 32 * pr;  // block (b, b-1) origin
+                        float w0 = 0.f, w1 = 0.f;
+#pragma unroll
+                        for (int m = 0; m < 16; ++m) {
+                            const float a = A[(ro + r) * ST + co + m];
+                            const float2 t2 = *reinterpret_cast<const float2*>(&Tm[(co + m) * ST + co + c2]);
+                            w0 = fmaf(a, t2.x, w0);
+                            w1 = fmaf(a, t2.y, w1);
+                        }
+                        *reinterpret_cast<float2*>(&sm.W[pr * 256 + r * 16 + c2]) = make_float2(w0, w1);
+                        __syncthreads();
+                        float t0 = 0.f, t1 = 0.f;
+#pragma unroll
+                        for (int m = 0; m < 16; ++m) {
+                            const float a = Tm[(ro + r) * ST + ro + m];
+                            const float2 w2 = *reinterpret_cast<const float2*>(&sm.W[pr * 256 + m * 16 + c2]);
+                            t0 = fmaf(a, w2.x, t0);
+                            t1 = fmaf(a, w2.y, t1);
+                        }
+                        *reinterpret_cast<float2*>(&Tm[(ro + r) * ST + co + c2]) = make_float2(-t0, -t1);
+                    }
+                    __syncthreads();
+                    {   // (3) rows 32-63 x cols 0-31; T1 and T2 are block lower triangular.  Both loops are
+                        // fully unrolled; the structurally zero 16-wide blocks (never written, so they may
+                        // hold any bits) are selected away, not multiplied, so every load is in flight at once
+                        const int r = tid >> 3, c4 = 4 * (tid & 7);
+                        const bool hi_c = (c4 >> 4) != 0;  // T1[m][c] for m < 16 is zero when c >= 16
+                        const float4 z4 = make_float4(0.f, 0.f, 0.f, 0.f);
+                        float acc[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+                        for (int m = 0; m < 32; ++m) {
+                            const float a = A[(32 + r) * ST + m];
+                            const float4 t4l = *reinterpret_cast<const float4*>(&Tm[m * ST + c4]);
+                            const float4 t4 = (m < 16 && hi_c) ? z4 : t4l;
+                            acc[0] = fmaf(a, t4.x, acc[0]); acc[1] = fmaf(a, t4.y, acc[1]);
+                            acc[2] = fmaf(a, t4.z, acc[2]); acc[3] = fmaf(a, t4.w, acc[3]);
+                        }
+                        *reinterpret_cast<float4*>(&sm.W[r * 32 + c4]) = make_float4(acc[0], acc[1], acc[2], acc[3]);
+                        __syncthreads();
+                        const bool lo_r = (r >> 4) == 0;  // T2[r][m] for m >= 16 is zero when r < 16
+                        float t[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+                        for (int m = 0; m < 32; ++m) {
+                            const float al = Tm[(32 + r) * ST + 32 + m];
+                            const float a = (m >= 16 && lo_r) ? 0.0f : al;
+                            const float4 w4 = *reinterpret_cast<const float4*>(&sm.W[m * 32 + c4]);
+                            t[0] = fmaf(a, w4.x, t[0]); t[1] = fmaf(a, w4.y, t[1]);
+                            t[2] = fmaf(a, w4.z, t[2]); t[3] = fmaf(a, w4.w, t[3]);
+                        }
+                        *reinterpret_cast<float4*>(&Tm[(32 + r) * ST + c4]) = make_float4(-t[0], -t[1], -t[2], -t[3]);
+                    }
+                    __syncthreads();
+                    // T -> MN-major B tile (element (n = column, k = row)); row fastest across
+                    // lanes; column groups right of the row's diagonal block are zero
+                    for (int u = tid; u < 64 * 8; u += kPrepThreads) {
+                        const int m = u & 63, g = u >> 6;
+                        float tr[8];
+                        if ((g >> 1) <= (m >> 4)) {
+                            const float4 x0 = *reinterpret_cast<const float4*>(&Tm[m * ST + g * 8]);
+                            const float4 x1 = *reinterpret_cast<const float4*>(&Tm[m * ST + g * 8 + 4]);
+                            tr[0] = x0.x; tr[1] = x0.y; tr[2] = x0.z; tr[3] = x0.w;
+                            tr[4] = x1.x; tr[5] = x1.y; tr[6] = x1.z; tr[7] = x1.w;
+                        } else {
+#pragma unroll
+                            for (int e = 0; e < 8; ++e) tr[e] = 0.0f;
+                        }
+                        store_split8(&sm.u.bt[0][mnmaj(g * 8, m, 64)], &sm.u.bt[1][mnmaj(g * 8, m, 64)], tr);
+                    }
+                }
+                umma::fence_proxy_async();
+                umma::fence_before_sync();
+                __syncthreads();
+                umma::fence_after_sync();
+
+                // P T  (M = 128 descriptor over the 64-row P tile; rows 64-127 of the product unused)
+                if (tid == 0) {
+                    mma_split(tmem, a_p[0], a_p[1], 128, 1024, 256, b_t[0], b_t[1], 1024, 256, 4,
+                              umma::idesc_bf16(128, 64, false, true));
+                    umma::commit(&sm.mbar);
+                }
+                if (!umma::mbar_wait(&sm.mbar, phase)) { sm.abort_flag = 1; atomicOr(err, kErrTimeout); }
+                phase ^= 1u;
+                __syncthreads();
+                if (sm.abort_flag) break;
+                umma::fence_after_sync();
+
+                // [T; P T] image (K-major, split; [P T; T] for odd chunks): threads L >= 64 copy T row L - 64
+                // from the split T tile (its 8-column groups are contiguous there), threads L < 64 split and
+                // write P T row L from TMEM lane L; columns of wg
+                {
+                    unsigned char* img = am_image(p, slot, h);
+                    const int cb = 32 * wg;
+                    if (L < 64) {
+                        float x[32];
+                        umma::tmem_ld32(tmem + lane_off + cb, x);
+                        umma::tmem_wait_ld();
+#pragma unroll
+                        for (int q = 0; q < 4; ++q) {
+                            uint4 vh, vl;
+                            split8(x + 8 * q, vh, vl);
+                            const int off = kmaj(odd ? L : 64 + L, cb + 8 * q, 64);
+                            *reinterpret_cast<uint4*>(img + off * 2) = vh;
+                            *reinterpret_cast<uint4*>(img + kAmBytes / 2 + off * 2) = vl;
+                        }
+                    } else {
+                        const int m = L - 64;
+#pragma unroll
+                        for (int q = 0; q < 4; ++q) {
+                            const int e = mnmaj(cb + 8 * q, m, 64);
+                            const uint4 vh = *reinterpret_cast<const uint4*>(&sm.u.bt[0][e]);
+                            const uint4 vl = *reinterpret_cast<const uint4*>(&sm.u.bt[1][e]);
+                            const int off = kmaj(odd ? 64 + m : m, cb + 8 * q, 64);
+                            *reinterpret_cast<uint4*>(img + off * 2) = vh;
+                            *reinterpret_cast<uint4*>(img + kAmBytes / 2 + off * 2) = vl;
+                        }
+                    }
+                }
+                umma::fence_before_sync();
+                __syncthreads();
+                umma::fence_after_sync();
+            }
+
+            // everything this chunk's chain needs is written: publish it (release, GPU scope)
+            if (tid == 0) {
+                __threadfence();
+                flag_publish(ready_flag(p, slot, h), p.epoch);
+            }
+        }  // used slot
+        // after round one: the last CTA to finish it stays whatever its SM, so the remaining
+        // tasks always have a taker; thread 0 fetches the next task
         if (tid == 0) {
-            mma_split(tmem, a_p[0], a_p[1], 128, 1024, 256, b_t[0], b_t[1], 1024, 256, 4,
-                      umma::idesc_bf16(128, 64, false, true));
-            umma::commit(&sm.mbar);
+            if (first && atomicAdd(counter + 1, 1u) + 1u == gridDim.x) stays = true;
+            sm.next[nx] = stays ? gridDim.x + atomicAdd(counter, 1u) : n_tasks;
         }
-        if (!umma::mbar_wait(&sm.mbar, phase)) { sm.abort_flag = 1; atomicOr(err, kErrTimeout); }
-        phase ^= 1u;
+        first = false;
         __syncthreads();
-        if (sm.abort_flag) goto done;
-        umma::fence_after_sync();
-
-        // [T; P T] image (K-major, split; [P T; T] for odd chunks): threads L >= 64 copy T row L - 64
-        // from the split T tile (its 8-column groups are contiguous there), threads L < 64 split and
-        // write P T row L from TMEM lane L; columns of wg
-        {
-            unsigned char* img = am_image(p, slot, h);
-            const int cb = 32 * wg;
-            if (L < 64) {
-                float x[32];
-                umma::tmem_ld32(tmem + lane_off + cb, x);
-                umma::tmem_wait_ld();
-#pragma unroll
-                for (int q = 0; q < 4; ++q) {
-                    uint4 vh, vl;
-                    split8(x + 8 * q, vh, vl);
-                    const int off = kmaj(odd ? L : 64 + L, cb + 8 * q, 64);
-                    *reinterpret_cast<uint4*>(img + off * 2) = vh;
-                    *reinterpret_cast<uint4*>(img + kAmBytes / 2 + off * 2) = vl;
-                }
-            } else {
-                const int m = L - 64;
-#pragma unroll
-                for (int q = 0; q < 4; ++q) {
-                    const int e = mnmaj(cb + 8 * q, m, 64);
-                    const uint4 vh = *reinterpret_cast<const uint4*>(&sm.u.bt[0][e]);
-                    const uint4 vl = *reinterpret_cast<const uint4*>(&sm.u.bt[1][e]);
-                    const int off = kmaj(odd ? 64 + m : m, cb + 8 * q, 64);
-                    *reinterpret_cast<uint4*>(img + off * 2) = vh;
-                    *reinterpret_cast<uint4*>(img + kAmBytes / 2 + off * 2) = vl;
-                }
-            }
-        }
-        umma::fence_before_sync();
-        __syncthreads();
-        umma::fence_after_sync();
+        task = sm.next[nx];
+        nx ^= 1;
     }
 
-    // everything this chunk's chain needs is written: publish it (release, GPU scope)
-    if (tid == 0) {
-        __threadfence();
-        flag_publish(ready_flag(p, slot, h), p.epoch);
-    }
-
-done:
     umma::fence_before_sync();
     __syncthreads();
     if (warp == 0) umma::tmem_dealloc(sm.tmem_base, 64);
@@ -1251,10 +1293,39 @@ unsigned long long next_epoch()
     return counter.fetch_add(0x9E3779B97F4A7C15ull) | 1ull;
 }
 
+int sm_count()
+{
+    static int cached[64] = {};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
+    if (cached[dev] == 0) {
+        int v = 0;
+        if (cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+        cached[dev] = v;
+    }
+    return cached[dev];
+}
+
+// prep grid: four CTAs per SM (its occupancy), at most one per task; sets which SMs stay after
+// round one: those the chain's CTAs leave free (at least a quarter of the GPU); with more chain
+// CTAs than SMs the chain runs in waves anyway and every SM stays
+unsigned prep_grid(ScanParams& p, size_t slots)
+{
+    const long long sms = sm_count() > 0 ? sm_count() : 1;
+    const long long tasks = (long long)slots * p.hv;
+    const long long chain_ctas = (long long)p.hv * (kHeadDim / kDVS) * p.n_seq;
+    long long keep = chain_ctas < sms ? sms - chain_ctas : sms;
+    if (keep < (sms + 3) / 4) keep = (sms + 3) / 4;
+    p.prep_sms = (int)sms;
+    p.prep_keep = (int)keep;
+    return (unsigned)(tasks < 4 * sms ? tasks : 4 * sms);
+}
+
 cudaError_t launch_scan(const ScanParams& p_in, cudaStream_t stream)
 {
     ScanParams p = p_in;
     p.epoch = next_epoch();
+    p.prep_sms = p.prep_keep = 0;
     if (p.n_seq == 0) return cudaSuccess;
     const size_t gram_smem = sizeof(GramSmem), prep_smem = sizeof(PrepSmem), chain_smem = sizeof(ChainSmem<kDVS>);
     cudaError_t e = cudaFuncSetAttribute(scan_gram_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)gram_smem);
@@ -1269,11 +1340,11 @@ cudaError_t launch_scan(const ScanParams& p_in, cudaStream_t stream)
         if (e != cudaSuccess) return e;
     } else {
         // each kernel may start while its predecessor drains and waits for it before reading
+        const unsigned prep_ctas = prep_grid(p, slots);
         e = launch_k(scan_gram_kernel, dim3((unsigned)p.hk, (unsigned)((slots + 1) / 2)), dim3(kGramThreads), gram_smem,
                      stream, true, p);
         if (e != cudaSuccess) return e;
-        e = launch_k(scan_prep_kernel, dim3((unsigned)p.hv, (unsigned)slots), dim3(kPrepThreads), prep_smem, stream,
-                     true, p);
+        e = launch_k(scan_prep_kernel, dim3(prep_ctas), dim3(kPrepThreads), prep_smem, stream, true, p);
         if (e != cudaSuccess) return e;
     }
     return launch_k(scan_chain_kernel<kDVS>, dim3((unsigned)(p.hv * (kHeadDim / kDVS)), (unsigned)p.n_seq),
