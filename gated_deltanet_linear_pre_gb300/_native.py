@@ -83,6 +83,8 @@ def lib():
             L.gdn_layer_check.argtypes = [D, _i32, _i32, _p, _p]
             L.gdn_scan_selftest_timeout.restype = ctypes.c_int
             L.gdn_scan_selftest_timeout.argtypes = [D, _i32, _i32] + [_p] * 10 + [_sz, _p]
+            L.gdn_scan_selftest_one_taker.restype = ctypes.c_int
+            L.gdn_scan_selftest_one_taker.argtypes = [D, _i32, _i32] + [_p] * 10 + [_sz, _p]
             L.gdn_step.restype = ctypes.c_int
             L.gdn_step.argtypes = [D, _i32] + [_p] * 12 + [_i32, _p, _p]
             _lib = L
@@ -255,3 +257,19 @@ def gdn_scan_selftest_timeout(d: gdn_dims, cu_seqlens, total_tokens, qn, kn, vc,
         _ptr(workspace, "workspace", torch.uint8), workspace.numel() if workspace is not None else 0,
         _stream(stream))
     _check("gdn_scan_selftest_timeout", st)
+
+
+def gdn_scan_selftest_one_taker(d: gdn_dims, cu_seqlens, total_tokens, qn, kn, vc, glog, beta, S_in, S_out, o,
+                                workspace, stream=None):
+    """Test hook of prep's progress guarantee: gdn_scan with no SM kept for prep after its first round."""
+    n_seq, T = _batch(cu_seqlens, total_tokens)
+    hk, hv, dk, dv = d.hk, d.hv, d.dk, d.dv
+    f32 = torch.float32
+    st = lib().gdn_scan_selftest_one_taker(
+        ctypes.byref(d), n_seq, T, _ptr(cu_seqlens, "cu_seqlens", torch.int32), _ptr(qn, "qn", f32, (T, hk, dk)),
+        _ptr(kn, "kn", f32, (T, hk, dk)), _ptr(vc, "vc", f32, (T, hv, dv)), _ptr(glog, "glog", f32, (T, hv)),
+        _ptr(beta, "beta", f32, (T, hv)), _ptr(S_in, "S_in", f32, (n_seq, hv, dk, dv)),
+        _ptr(S_out, "S_out", f32, (n_seq, hv, dk, dv)), _ptr(o, "o", f32, (T, hv, dv)),
+        _ptr(workspace, "workspace", torch.uint8), workspace.numel() if workspace is not None else 0,
+        _stream(stream))
+    _check("gdn_scan_selftest_one_taker", st)

@@ -439,4 +439,17 @@ gdn_status gdn_scan_selftest_timeout(const gdn_dims* dims, int32_t n_seq, int32_
     return run_scan(p, stream);
 }
 
+gdn_status gdn_scan_selftest_one_taker(const gdn_dims* dims, int32_t n_seq, int32_t T, const int32_t* cu_seqlens,
+                                       const float* qn, const float* kn, const float* vc, const float* glog,
+                                       const float* beta, const float* S_in, float* S_out, float* o,
+                                       void* workspace, size_t workspace_bytes, struct CUstream_st* stream)
+{
+    gdn::ScanParams p;
+    gdn_status st = prep_scan(dims, n_seq, T, cu_seqlens, qn, kn, vc, glog, beta, S_in, S_out, o, workspace,
+                              workspace_bytes, p);
+    if (st != GDN_OK) return st;
+    p.prep_no_keepers = 1;
+    return run_scan(p, stream);
+}
+
 }  // extern "C"

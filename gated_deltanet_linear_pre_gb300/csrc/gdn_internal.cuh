@@ -44,6 +44,7 @@ struct ScanParams {
     void* workspace;
     size_t workspace_bytes;
     int withhold_first_copy;  // failure-report self-test only (gdn_scan_selftest_timeout)
+    int prep_no_keepers;      // prep fallback self-test only (gdn_scan_selftest_one_taker)
     unsigned long long epoch;  // this call's tag for the per-chunk ready flags (set by launch_scan)
     int prep_sms, prep_keep;  // SMs of the device; SMs whose prep CTAs stay after round one (set by launch_scan)
 };

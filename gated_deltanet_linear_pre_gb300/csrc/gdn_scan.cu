@@ -205,7 +205,8 @@ __device__ __forceinline__ bool flag_wait(const unsigned long long* f, unsigned 
     return true;
 }
 
-// prep's task counter and count of CTAs done with round one (header words 16 and 17), cleared by gram
+// prep's task counter, count of CTAs done with round one and count of CTAs that stay (header
+// words 16, 17 and 18), cleared by gram
 __device__ __forceinline__ unsigned int* prep_counter(const ScanParams& p)
 {
     return reinterpret_cast<unsigned int*>(static_cast<unsigned char*>(p.workspace) + 64);
@@ -349,6 +350,7 @@ __global__ void __launch_bounds__(kGramThreads, 2) scan_gram_kernel(ScanParams p
         *err = 0u;
         prep_counter(p)[0] = 0u;
         prep_counter(p)[1] = 0u;
+        prep_counter(p)[2] = 0u;
     }
     int c0[2], n[2];
     bool has_prev[2], odd[2], used[2];
@@ -500,6 +502,10 @@ __global__ void __launch_bounds__(kPrepThreads, 4) scan_prep_kernel(ScanParams p
     const unsigned n_tasks = (unsigned)(n_slots(p.T, p.n_seq) * (size_t)p.hv);
     bool stays = prep_sm_stays(p);
     unsigned int* counter = prep_counter(p);
+    if (stays && tid == 0) {  // CTAs that stay register before their round one
+        atomicAdd(counter + 2, 1u);
+        __threadfence();
+    }
     bool first = true;
     int nx = 0;
     for (unsigned task = blockIdx.x; task < n_tasks;) {
@@ -756,10 +762,14 @@ __global__ void __launch_bounds__(kPrepThreads, 4) scan_prep_kernel(ScanParams p
                 flag_publish(ready_flag(p, slot, h), p.epoch);
             }
         }  // used slot
-        // after round one: the last CTA to finish it stays whatever its SM, so the remaining
-        // tasks always have a taker; thread 0 fetches the next task
+        // after round one: if no CTA landed on an SM that stays, the last CTA to finish round one
+        // stays whatever its SM, so the remaining tasks always have a taker; thread 0 fetches the
+        // next task
         if (tid == 0) {
-            if (first && atomicAdd(counter + 1, 1u) + 1u == gridDim.x) stays = true;
+            if (first && atomicAdd(counter + 1, 1u) + 1u == gridDim.x) {
+                __threadfence();
+                if (atomicAdd(counter + 2, 0u) == 0u) stays = true;
+            }
             sm.next[nx] = stays ? gridDim.x + atomicAdd(counter, 1u) : n_tasks;
         }
         first = false;
@@ -1341,6 +1351,7 @@ cudaError_t launch_scan(const ScanParams& p_in, cudaStream_t stream)
     } else {
         // each kernel may start while its predecessor drains and waits for it before reading
         const unsigned prep_ctas = prep_grid(p, slots);
+        if (p.prep_no_keepers) p.prep_keep = 0;  // self-test: the round-one fallback takes every later task
         e = launch_k(scan_gram_kernel, dim3((unsigned)p.hk, (unsigned)((slots + 1) / 2)), dim3(kGramThreads), gram_smem,
                      stream, true, p);
         if (e != cudaSuccess) return e;

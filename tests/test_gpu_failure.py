@@ -74,3 +74,28 @@ def test_expired_wait_is_reported_and_the_context_stays_usable():
     gdn.gdn_scan_check(ws)
     assert u.max_rel(o.cpu().numpy(), ref["o"]) <= u.TOL_F32
     assert u.max_rel(S_out.cpu().numpy(), ref["S_out"]) <= u.TOL_F32
+
+
+@pytest.mark.parametrize("lens", [[2048], [1000, 700, 350]])
+def test_prep_fallback_alone_gives_the_same_scan(lens):
+    """With no SM kept for prep after its first round, the one CTA the fallback keeps takes every
+    remaining task; the scan must come out bit for bit as the normal one."""
+    import gpu_util as u
+    import gated_deltanet_linear_pre_gb300 as gdn
+    inp = gin.make_layer(92, lens, hist_nonzero=True, S0_std=0.02)
+    d = u.dims_of(inp)
+    T, n_seq = inp.total_tokens, inp.n_seq
+    x = u.device_inputs(inp)
+    f = dict(device="cuda", dtype=torch.float32)
+    q, k = torch.empty((T, d.hk, d.dk), **f), torch.empty((T, d.hk, d.dk), **f)
+    v, lam, beta = torch.empty((T, d.hv, d.dv), **f), torch.empty((T, d.hv), **f), torch.empty((T, d.hv), **f)
+    gdn.gdn_pre(d, x["cu"], T, x["qkv"], x["conv_w"], x["hist"], torch.empty_like(x["hist"]), x["a"], x["b"],
+                x["A_log"], x["dt_bias"], q, k, v, lam, beta)
+    ws = torch.empty(gdn.gdn_scan_workspace_bytes(d, n_seq, T), device="cuda", dtype=torch.uint8)
+    o1, o2 = torch.empty((T, d.hv, d.dv), **f), torch.empty((T, d.hv, d.dv), **f)
+    S1, S2 = torch.empty_like(x["S0"]), torch.empty_like(x["S0"])
+    gdn.gdn_scan(d, x["cu"], T, q, k, v, lam, beta, x["S0"], S1, o1, ws)
+    gdn.gdn_scan_check(ws)
+    gdn.gdn_scan_selftest_one_taker(d, x["cu"], T, q, k, v, lam, beta, x["S0"], S2, o2, ws)
+    gdn.gdn_scan_check(ws)
+    assert torch.equal(o1, o2) and torch.equal(S1, S2)
