@@ -217,3 +217,11 @@ def test_layer_other_head_counts(hk, hv):
     assert u.max_rel(got["y"], ref["y"]) <= u.TOL_F16
     assert u.max_rel(got["S_out"], ref["S_out"]) <= u.TOL_F32
     np.testing.assert_array_equal(got["hist_out"].view(np.uint16), inp_hist_bits(ref["hist_out"]))
+
+
+@pytest.mark.parametrize("layer", [0, 35])
+def test_layer_stack_workload_sampled_heads(layer):
+    # the timed workload itself: one T=2048 layer of the 36-layer stack (its own seeded weights and
+    # activations, zero history, S0 = 0, fp16 out) through gdn_layer as the bench calls it; every
+    # fifth value head's outputs and final state against the fp64 oracle, the history bit-exact
+    _check_layer(gin.stack_layer(layer), heads=list(range(layer % 5, 48, 5)))
