@@ -21,7 +21,7 @@ namespace gdn {
 namespace {
 
 constexpr int kTokBlk = 8;    // tokens per warp task
-constexpr int kWarps = 8;     // warps (heads) per block
+constexpr int kWarps = 4;     // warps (heads) per block (128-thread blocks schedule finer than 256)
 constexpr int kThreads = kWarps * 32;
 constexpr int kHistThreads = kThreads;  // one history channel per thread
 
@@ -99,7 +99,7 @@ __device__ __forceinline__ void conv_block(const uint2 (&cur)[kTokBlk], F4 win0,
     }
 }
 
-__global__ void __launch_bounds__(kThreads, 4)
+__global__ void __launch_bounds__(kThreads, 8)
 pre_kernel(PreParams p, int n_slots, int head_groups, int n_conv_blocks)
 {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
