@@ -54,7 +54,7 @@ __device__ __forceinline__ float conv_channel(const StepParams& p, int s, int ch
                            __half2float(x)));
 }
 
-__global__ void __launch_bounds__(kThreads, 2) step_kernel(StepParams p)
+__global__ void __launch_bounds__(kThreads, 3) step_kernel(StepParams p)
 {
     __shared__ float sq[kHeadDim], sk[kHeadDim], sv[kHeadDim];
     __shared__ float red[8][kHeadDim];  // per-row-group partial column sums
