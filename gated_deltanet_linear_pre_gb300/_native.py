@@ -67,16 +67,18 @@ def lib():
             L.gdn_pre.argtypes = [D, _i32, _i32] + [_p] * 15
             L.gdn_scan_workspace_bytes.restype = _sz
             L.gdn_scan_workspace_bytes.argtypes = [D, _i32, _i32]
-            L.gdn_scan.restype = ctypes.c_int
-            L.gdn_scan.argtypes = [D, _i32, _i32] + [_p] * 10 + [_sz, _p]
+            for name in ("gdn_scan", "gdn_scan_fast"):
+                getattr(L, name).restype = ctypes.c_int
+                getattr(L, name).argtypes = [D, _i32, _i32] + [_p] * 10 + [_sz, _p]
             L.gdn_scan_noalloc.restype = ctypes.c_int
             L.gdn_scan_noalloc.argtypes = [D, _i32, _i32] + [_p] * 9 + [_p]
             L.gdn_post.restype = ctypes.c_int
             L.gdn_post.argtypes = [D, _i32, _p, _p, _p, _i32, _p, _p]
             L.gdn_layer_workspace_bytes.restype = _sz
             L.gdn_layer_workspace_bytes.argtypes = [D, _i32, _i32]
-            L.gdn_layer.restype = ctypes.c_int
-            L.gdn_layer.argtypes = [D, _i32, _i32] + [_p] * 13 + [_i32, _p, _p, _sz, _p]
+            for name in ("gdn_layer", "gdn_layer_fast"):
+                getattr(L, name).restype = ctypes.c_int
+                getattr(L, name).argtypes = [D, _i32, _i32] + [_p] * 13 + [_i32, _p, _p, _sz, _p]
             L.gdn_scan_check.restype = ctypes.c_int
             L.gdn_scan_check.argtypes = [_p, _p]
             L.gdn_layer_check.restype = ctypes.c_int
@@ -152,19 +154,29 @@ def gdn_scan_workspace_bytes(d: gdn_dims, n_seq: int, total_tokens: int) -> int:
 
 def gdn_scan(d: gdn_dims, cu_seqlens, total_tokens, qn, kn, vc, glog, beta, S_in, S_out, o,
              workspace=None, stream=None):
+    _scan("gdn_scan", d, cu_seqlens, total_tokens, qn, kn, vc, glog, beta, S_in, S_out, o, workspace, stream)
+
+
+def gdn_scan_fast(d: gdn_dims, cu_seqlens, total_tokens, qn, kn, vc, glog, beta, S_in, S_out, o,
+                  workspace=None, stream=None):
+    """gdn_scan with one-pass bf16 tensor-core products (faster, less accurate)."""
+    _scan("gdn_scan_fast", d, cu_seqlens, total_tokens, qn, kn, vc, glog, beta, S_in, S_out, o, workspace, stream)
+
+
+def _scan(name, d, cu_seqlens, total_tokens, qn, kn, vc, glog, beta, S_in, S_out, o, workspace, stream):
     n_seq, T = _batch(cu_seqlens, total_tokens)
     hk, hv, dk, dv = d.hk, d.hv, d.dk, d.dv
     f32 = torch.float32
     ws_ptr, ws_bytes = None, 0
     if workspace is not None:
         ws_ptr, ws_bytes = _ptr(workspace, "workspace", torch.uint8), workspace.numel()
-    st = lib().gdn_scan(ctypes.byref(d), n_seq, T, _ptr(cu_seqlens, "cu_seqlens", torch.int32),
+    st = getattr(lib(), name)(ctypes.byref(d), n_seq, T, _ptr(cu_seqlens, "cu_seqlens", torch.int32),
                         _ptr(qn, "qn", f32, (T, hk, dk)), _ptr(kn, "kn", f32, (T, hk, dk)),
                         _ptr(vc, "vc", f32, (T, hv, dv)), _ptr(glog, "glog", f32, (T, hv)),
                         _ptr(beta, "beta", f32, (T, hv)), _ptr(S_in, "S_in", f32, (n_seq, hv, dk, dv)),
                         _ptr(S_out, "S_out", f32, (n_seq, hv, dk, dv)), _ptr(o, "o", f32, (T, hv, dv)),
                         ws_ptr, ws_bytes, _stream(stream))
-    _check("gdn_scan", st)
+    _check(name, st)
 
 
 def gdn_scan_noalloc(d: gdn_dims, cu_seqlens, total_tokens, qn, kn, vc, glog, beta, S_in, S_out, o, stream=None):
@@ -197,11 +209,24 @@ def gdn_layer_workspace_bytes(d: gdn_dims, n_seq: int, total_tokens: int) -> int
 
 def gdn_layer(d: gdn_dims, cu_seqlens, total_tokens, qkv, conv_w, hist_in, hist_out, a, b, z, A_log, dt_bias,
               gamma, S_in, S_out, out_f32: bool, y, workspace, stream=None):
+    _layer("gdn_layer", d, cu_seqlens, total_tokens, qkv, conv_w, hist_in, hist_out, a, b, z, A_log, dt_bias,
+           gamma, S_in, S_out, out_f32, y, workspace, stream)
+
+
+def gdn_layer_fast(d: gdn_dims, cu_seqlens, total_tokens, qkv, conv_w, hist_in, hist_out, a, b, z, A_log,
+                   dt_bias, gamma, S_in, S_out, out_f32: bool, y, workspace, stream=None):
+    """gdn_layer with one-pass bf16 tensor-core products in the scan (faster, less accurate)."""
+    _layer("gdn_layer_fast", d, cu_seqlens, total_tokens, qkv, conv_w, hist_in, hist_out, a, b, z, A_log, dt_bias,
+           gamma, S_in, S_out, out_f32, y, workspace, stream)
+
+
+def _layer(name, d, cu_seqlens, total_tokens, qkv, conv_w, hist_in, hist_out, a, b, z, A_log, dt_bias,
+           gamma, S_in, S_out, out_f32, y, workspace, stream):
     n_seq, T = _batch(cu_seqlens, total_tokens)
     C, hv, dk, dv = _C(d), d.hv, d.dk, d.dv
     f16, f32 = torch.float16, torch.float32
     ydt = f32 if out_f32 else f16
-    st = lib().gdn_layer(ctypes.byref(d), n_seq, T, _ptr(cu_seqlens, "cu_seqlens", torch.int32),
+    st = getattr(lib(), name)(ctypes.byref(d), n_seq, T, _ptr(cu_seqlens, "cu_seqlens", torch.int32),
                          _ptr(qkv, "qkv", f16, (T, C)), _ptr(conv_w, "conv_w", f32, (C, 4)),
                          _ptr(hist_in, "hist_in", f16, (n_seq, C, 3)),
                          _ptr(hist_out, "hist_out", f16, (n_seq, C, 3)),
@@ -211,7 +236,7 @@ def gdn_layer(d: gdn_dims, cu_seqlens, total_tokens, qkv, conv_w, hist_in, hist_
                          _ptr(S_out, "S_out", f32, (n_seq, hv, dk, dv)), 1 if out_f32 else 0,
                          _ptr(y, "y", ydt, (T, hv, dv)), _ptr(workspace, "workspace", torch.uint8),
                          workspace.numel() if workspace is not None else 0, _stream(stream))
-    _check("gdn_layer", st)
+    _check(name, st)
 
 
 def gdn_step(d: gdn_dims, n_seq: int, qkv, conv_w, hist_in, hist_out, a, b, z, A_log, dt_bias, gamma, S_in, S_out,

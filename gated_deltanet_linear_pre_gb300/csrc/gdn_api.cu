@@ -292,6 +292,19 @@ gdn_status gdn_scan(const gdn_dims* dims, int32_t n_seq, int32_t T, const int32_
     return st != GDN_OK ? st : run_scan(p, stream);
 }
 
+gdn_status gdn_scan_fast(const gdn_dims* dims, int32_t n_seq, int32_t T, const int32_t* cu_seqlens,
+                         const float* qn, const float* kn, const float* vc, const float* glog, const float* beta,
+                         const float* S_in, float* S_out, float* o, void* workspace, size_t workspace_bytes,
+                         struct CUstream_st* stream)
+{
+    gdn::ScanParams p;
+    gdn_status st = prep_scan(dims, n_seq, T, cu_seqlens, qn, kn, vc, glog, beta, S_in, S_out, o, workspace,
+                              workspace_bytes, p);
+    if (st != GDN_OK) return st;
+    p.fast = 1;
+    return run_scan(p, stream);
+}
+
 gdn_status gdn_post(const gdn_dims* dims, int32_t T, const float* o, const uint16_t* z, const float* gamma,
                     int32_t out_f32, void* y, struct CUstream_st* stream)
 {
@@ -312,12 +325,12 @@ size_t gdn_layer_workspace_bytes(const gdn_dims* dims, int32_t n_seq, int32_t T)
     return total;
 }
 
-gdn_status gdn_layer(const gdn_dims* dims, int32_t n_seq, int32_t T, const int32_t* cu_seqlens,
-                     const uint16_t* qkv, const float* conv_w, const uint16_t* hist_in, uint16_t* hist_out,
-                     const uint16_t* a, const uint16_t* b, const uint16_t* z, const float* A_log,
-                     const float* dt_bias, const float* gamma, const float* S_in, float* S_out,
-                     int32_t out_f32, void* y, void* workspace, size_t workspace_bytes,
-                     struct CUstream_st* stream)
+static gdn_status layer_impl(const gdn_dims* dims, int32_t n_seq, int32_t T, const int32_t* cu_seqlens,
+                             const uint16_t* qkv, const float* conv_w, const uint16_t* hist_in, uint16_t* hist_out,
+                             const uint16_t* a, const uint16_t* b, const uint16_t* z, const float* A_log,
+                             const float* dt_bias, const float* gamma, const float* S_in, float* S_out,
+                             int32_t out_f32, void* y, void* workspace, size_t workspace_bytes,
+                             struct CUstream_st* stream, int fast)
 {
     gdn_status st;
     if ((st = check_dims(dims)) != GDN_OK) return st;
@@ -354,9 +367,32 @@ gdn_status gdn_layer(const gdn_dims* dims, int32_t n_seq, int32_t T, const int32
                         sp)) != GDN_OK)
         return st;
     if ((st = prep_post(dims, T, o, z, gamma, out_f32, y, op)) != GDN_OK) return st;
+    sp.fast = fast;
     if ((st = run_pre(pp, stream)) != GDN_OK) return st;
     if ((st = run_scan(sp, stream)) != GDN_OK) return st;
     return run_post(op, stream);
+}
+
+gdn_status gdn_layer(const gdn_dims* dims, int32_t n_seq, int32_t T, const int32_t* cu_seqlens,
+                     const uint16_t* qkv, const float* conv_w, const uint16_t* hist_in, uint16_t* hist_out,
+                     const uint16_t* a, const uint16_t* b, const uint16_t* z, const float* A_log,
+                     const float* dt_bias, const float* gamma, const float* S_in, float* S_out,
+                     int32_t out_f32, void* y, void* workspace, size_t workspace_bytes,
+                     struct CUstream_st* stream)
+{
+    return layer_impl(dims, n_seq, T, cu_seqlens, qkv, conv_w, hist_in, hist_out, a, b, z, A_log, dt_bias, gamma,
+                      S_in, S_out, out_f32, y, workspace, workspace_bytes, stream, 0);
+}
+
+gdn_status gdn_layer_fast(const gdn_dims* dims, int32_t n_seq, int32_t T, const int32_t* cu_seqlens,
+                          const uint16_t* qkv, const float* conv_w, const uint16_t* hist_in, uint16_t* hist_out,
+                          const uint16_t* a, const uint16_t* b, const uint16_t* z, const float* A_log,
+                          const float* dt_bias, const float* gamma, const float* S_in, float* S_out,
+                          int32_t out_f32, void* y, void* workspace, size_t workspace_bytes,
+                          struct CUstream_st* stream)
+{
+    return layer_impl(dims, n_seq, T, cu_seqlens, qkv, conv_w, hist_in, hist_out, a, b, z, A_log, dt_bias, gamma,
+                      S_in, S_out, out_f32, y, workspace, workspace_bytes, stream, 1);
 }
 
 }  // extern "C"

@@ -96,6 +96,22 @@ __device__ __forceinline__ void store_split8(uint16_t* hi, uint16_t* lo, const f
     *reinterpret_cast<uint4*>(lo) = vl;
 }
 
+// 8 fp32 values -> bf16 (round to nearest even), the hi plane only (fast mode)
+__device__ __forceinline__ void store_hi8(uint16_t* hi, const float* x)
+{
+    uint32_t h[4];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) h[q] = bf2_bits(__floats2bfloat162_rn(x[2 * q], x[2 * q + 1]));
+    *reinterpret_cast<uint4*>(hi) = make_uint4(h[0], h[1], h[2], h[3]);
+}
+
+template <bool FAST>
+__device__ __forceinline__ void store_op8(uint16_t* hi, uint16_t* lo, const float* x)
+{
+    if constexpr (FAST) store_hi8(hi, x);
+    else store_split8(hi, lo, x);
+}
+
 // Three-pass split product D = A * B over `ksteps` 16-wide K steps; a_kstep /
 // b_kstep are the byte advances of one K step in each tile.  Descriptors are
 // built once per operand and advanced by adding to their start-address field.
@@ -111,6 +127,15 @@ __device__ __forceinline__ void mma_split(uint32_t d, uint32_t a_hi, uint32_t a_
     for (int ks = 0; ks < ksteps; ++ks) umma::mma_bf16(d, dal + ks * sa, dbh + ks * sb, idesc, 1u);
 }
 
+// One-pass product D = A_hi * B_hi (fast mode: bf16 operands, fp32 accumulation)
+__device__ __forceinline__ void mma_one(uint32_t d, uint32_t a_hi, uint32_t a_lbo, uint32_t a_sbo, uint32_t a_kstep,
+                                        uint32_t b_hi, uint32_t b_sbo, uint32_t b_kstep, int ksteps, uint32_t idesc)
+{
+    const uint64_t dah = umma::desc(a_hi, a_lbo, a_sbo), dbh = umma::desc(b_hi, 128, b_sbo);
+    const uint64_t sa = a_kstep >> 4, sb = b_kstep >> 4;
+    for (int ks = 0; ks < ksteps; ++ks) umma::mma_bf16(d, dah + ks * sa, dbh + ks * sb, idesc, ks != 0);
+}
+
 // Split product in two instruction groups: D[:, 0:2N] = A_hi [B_hi | B_lo], then
 // D[:, 0:N] += A_lo B_hi, so D[:, 0:N] + D[:, N:2N] = A B to ~16 bits.  Needs B_lo
 // to follow B_hi directly along N in shared memory (b_hilo is the start of
@@ -118,12 +143,18 @@ __device__ __forceinline__ void mma_split(uint32_t d, uint32_t a_hi, uint32_t a_
 // The K-step count and every stride are compile-time constants so that the
 // issuing thread spends as few instructions as possible per MMA.
 template <int KSTEPS, int N, uint32_t A_LBO, uint32_t A_SBO, uint32_t A_KSTEP, uint32_t B_SBO, uint32_t B_KSTEP,
-          bool A_MN, bool B_MN, bool ACC = false>
+          bool A_MN, bool B_MN, bool ACC = false, bool FAST = false>
 __device__ __forceinline__ void mma_split2(uint32_t d, uint32_t a_hi, uint32_t a_lo, uint32_t b_hilo)
 {
     const uint64_t dah = umma::desc(a_hi, A_LBO, A_SBO), dal = umma::desc(a_lo, A_LBO, A_SBO);
     const uint64_t db = umma::desc(b_hilo, 128, B_SBO);
     constexpr uint32_t wide = umma::idesc_bf16(128, 2 * N, A_MN, B_MN), narrow = umma::idesc_bf16(128, N, A_MN, B_MN);
+    if constexpr (FAST) {  // one pass, A_hi * B_hi into D[:, 0:N]
+#pragma unroll
+        for (int ks = 0; ks < KSTEPS; ++ks)
+            umma::mma_bf16(d, dah + ks * (A_KSTEP >> 4), db + ks * (B_KSTEP >> 4), narrow, (ACC || ks != 0) ? 1u : 0u);
+        return;
+    }
 #pragma unroll
     for (int ks = 0; ks < KSTEPS; ++ks)
         umma::mma_bf16(d, dah + ks * (A_KSTEP >> 4), db + ks * (B_KSTEP >> 4), wide, (ACC || ks != 0) ? 1u : 0u);
@@ -406,11 +437,16 @@ __global__ void __launch_bounds__(kGramThreads, 2) scan_gram_kernel(ScanParams p
         // (K K^T ; Q K^T) = [K; Q] K^T  (B = the K rows of the same tile);  M = [K; Q] K_prev^T
         if (tid == 0) {
             const uint32_t a_hi = umma::smem_u32(sm.akq[0]), a_lo = umma::smem_u32(sm.akq[1]);
-            mma_split(tmem, a_hi, a_lo, 128, 2048, 256, a_hi, a_lo, 2048, 256, 8,
-                      umma::idesc_bf16(128, 64, false, false));
-            if (has_prev[t])
-                mma_split(tmem + 64, a_hi, a_lo, 128, 2048, 256, umma::smem_u32(sm.bkp[0]), umma::smem_u32(sm.bkp[1]),
-                          2048, 256, 8, umma::idesc_bf16(128, 64, false, false));
+            constexpr uint32_t id = umma::idesc_bf16(128, 64, false, false);
+            if (p.fast) {
+                mma_one(tmem, a_hi, 128, 2048, 256, a_hi, 2048, 256, 8, id);
+                if (has_prev[t]) mma_one(tmem + 64, a_hi, 128, 2048, 256, umma::smem_u32(sm.bkp[0]), 2048, 256, 8, id);
+            } else {
+                mma_split(tmem, a_hi, a_lo, 128, 2048, 256, a_hi, a_lo, 2048, 256, 8, id);
+                if (has_prev[t])
+                    mma_split(tmem + 64, a_hi, a_lo, 128, 2048, 256, umma::smem_u32(sm.bkp[0]), umma::smem_u32(sm.bkp[1]),
+                              2048, 256, 8, id);
+            }
             umma::commit(&sm.mbar);
         }
         // the second chunk's K and Q loads fly while this chunk's products and epilogue run
@@ -710,8 +746,11 @@ __global__ void __launch_bounds__(kPrepThreads, 4) scan_prep_kernel(ScanParams p
 
                 // P T  (M = 128 descriptor over the 64-row P tile; rows 64-127 of the product unused)
                 if (tid == 0) {
-                    mma_split(tmem, a_p[0], a_p[1], 128, 1024, 256, b_t[0], b_t[1], 1024, 256, 4,
-                              umma::idesc_bf16(128, 64, false, true));
+                    if (p.fast)
+                        mma_one(tmem, a_p[0], 128, 1024, 256, b_t[0], 1024, 256, 4, umma::idesc_bf16(128, 64, false, true));
+                    else
+                        mma_split(tmem, a_p[0], a_p[1], 128, 1024, 256, b_t[0], b_t[1], 1024, 256, 4,
+                                  umma::idesc_bf16(128, 64, false, true));
                     umma::commit(&sm.mbar);
                 }
                 if (!umma::mbar_wait(&sm.mbar, phase)) { sm.abort_flag = 1; atomicOr(err, kErrTimeout); }
@@ -861,7 +900,14 @@ __device__ __forceinline__ bool chain_wait(uint64_t* mbar, uint32_t parity, cons
     return __all_sync(0xffffffffu, ok);
 }
 
-template <int DVS>
+template <int COLS>
+__device__ __forceinline__ void zero_cols(float (&d)[COLS])
+{
+#pragma unroll
+    for (int e = 0; e < COLS; ++e) d[e] = 0.0f;
+}
+
+template <int DVS, bool FAST>
 __global__ void __launch_bounds__(kChainThreads, 1) scan_chain_kernel(ScanParams p)
 {
     extern __shared__ __align__(1024) unsigned char smem_raw[];
@@ -1015,7 +1061,7 @@ __global__ void __launch_bounds__(kChainThreads, 1) scan_chain_kernel(ScanParams
             GDN_WAIT(&sm.mb_kq, 0);
             umma::fence_after_sync();
             if (leader) {
-                mma_split2<8, DVS, 128, 4096, 256, 2048, 256, false, true>(tmem + cD2, kh0, kh0 + 2048, b_s);
+                mma_split2<8, DVS, 128, 4096, 256, 2048, 256, false, true, false, FAST>(tmem + cD2, kh0, kh0 + 2048, b_s);
                 umma::commit(&sm.mb_f);
             }
             __syncwarp();
@@ -1027,7 +1073,7 @@ __global__ void __launch_bounds__(kChainThreads, 1) scan_chain_kernel(ScanParams
             GDN_WAIT(&sm.mb_am, c & 1);
             umma::fence_after_sync();
             if (leader) {
-                mma_split2<4, DVS, 128, 1024, 256, 1024, 256, false, true>(tmem + cD3, a_t_hi, a_t_lo, b_x);
+                mma_split2<4, DVS, 128, 1024, 256, 1024, 256, false, true, false, FAST>(tmem + cD3, a_t_hi, a_t_lo, b_x);
                 umma::commit(&sm.mb_d3);
             }
             __syncwarp();
@@ -1038,7 +1084,7 @@ __global__ void __launch_bounds__(kChainThreads, 1) scan_chain_kernel(ScanParams
                 umma::fence_after_sync();
                 const uint32_t a = kh0 + ((c + 1) & 1) * kSlotBytes;  // stacked from R1 (odd) or R0 (even)
                 if (leader)
-                    mma_split2<8, DVS, 128, 4096, 256, 2048, 256, false, true>(tmem + cD2, a, a + 2048, b_s);
+                    mma_split2<8, DVS, 128, 4096, 256, 2048, 256, false, true, false, FAST>(tmem + cD2, a, a + 2048, b_s);
                 __syncwarp();
             }
             // U'_c published: M_{c+1} U'_c on top (the chunk-to-chunk path), then K_c^T U'_c
@@ -1047,12 +1093,12 @@ __global__ void __launch_bounds__(kChainThreads, 1) scan_chain_kernel(ScanParams
             umma::fence_after_sync();
             if (leader) {
                 if (more) {
-                    mma_split2<4, DVS, 128, 1024, 256, 1024, 256, false, true, true>(tmem + cD2, a_m_hi, a_m_lo, b_u);
+                    mma_split2<4, DVS, 128, 1024, 256, 1024, 256, false, true, true, FAST>(tmem + cD2, a_m_hi, a_m_lo, b_u);
                     umma::commit(&sm.mb_f);
                 }
                 // K_c^T: MN-major view of the K half (token groups 4 KB apart, key groups 128 B)
                 const uint32_t kb = kh0 + kslot(c) * kSlotBytes;
-                mma_split2<4, DVS, 4096, 128, 8192, 1024, 256, true, true>(tmem + cD4, kb, kb + 2048, b_u);
+                mma_split2<4, DVS, 4096, 128, 8192, 1024, 256, true, true, false, FAST>(tmem + cD4, kb, kb + 2048, b_u);
                 umma::commit(&sm.mb_d4);
             }
             __syncwarp();
@@ -1103,7 +1149,7 @@ __global__ void __launch_bounds__(kChainThreads, 1) scan_chain_kernel(ScanParams
         if (n_chunks > 0) {
 #pragma unroll
             for (int e = 0; e < COLS; e += 8)
-                store_split8(&sm.bs[0][mnmaj(cb + e, L, 128)], &sm.bs[1][mnmaj(cb + e, L, 128)], S + e);
+                store_op8<FAST>(&sm.bs[0][mnmaj(cb + e, L, 128)], &sm.bs[1][mnmaj(cb + e, L, 128)], S + e);
             umma::fence_proxy_async();
             umma::mbar_arrive(&sm.mb_s);
             if (grp == 0) {  // V of chunk 0, by the row group that owns its K side
@@ -1129,7 +1175,7 @@ __global__ void __launch_bounds__(kChainThreads, 1) scan_chain_kernel(ScanParams
             {
                 float d[COLS], d2[COLS];
                 tmem_ld_cols<COLS>(tmem + lane_off + cD2 + cb, d);
-                tmem_ld_cols<COLS>(tmem + lane_off + cD2 + DVS + cb, d2);
+                if constexpr (!FAST) tmem_ld_cols<COLS>(tmem + lane_off + cD2 + DVS + cb, d2); else zero_cols(d2);
                 umma::tmem_wait_ld();
 #pragma unroll
                 for (int e = 0; e < COLS; ++e) d[e] += d2[e];
@@ -1148,7 +1194,7 @@ __global__ void __launch_bounds__(kChainThreads, 1) scan_chain_kernel(ScanParams
                     GDN_GROUP_SYNC();  // every V read done before X overwrites the tile
 #pragma unroll
                     for (int e = 0; e < COLS; e += 8)
-                        store_split8(&sm.bx[0][mnmaj(cb + e, t, 64)], &sm.bx[1][mnmaj(cb + e, t, 64)], d + e);
+                        store_op8<FAST>(&sm.bx[0][mnmaj(cb + e, t, 64)], &sm.bx[1][mnmaj(cb + e, t, 64)], d + e);
                     umma::fence_proxy_async();
                 } else {
                     const float f = g_eG * qscale;
@@ -1173,7 +1219,7 @@ __global__ void __launch_bounds__(kChainThreads, 1) scan_chain_kernel(ScanParams
                 umma::fence_after_sync();
                 float d[COLS], d2[COLS];
                 tmem_ld_cols<COLS>(tmem + lane_off + cD4 + cb, d);
-                tmem_ld_cols<COLS>(tmem + lane_off + cD4 + DVS + cb, d2);
+                if constexpr (!FAST) tmem_ld_cols<COLS>(tmem + lane_off + cD4 + DVS + cb, d2); else zero_cols(d2);
                 umma::tmem_wait_ld();
 #pragma unroll
                 for (int e = 0; e < COLS; ++e) S[e] = fmaf(gl_prev, S[e], d[e] + d2[e]);
@@ -1184,7 +1230,7 @@ __global__ void __launch_bounds__(kChainThreads, 1) scan_chain_kernel(ScanParams
                     float x[8];
 #pragma unroll
                     for (int q = 0; q < 8; ++q) x[q] = gl * S[e + q];
-                    store_split8(&sm.bs[0][mnmaj(cb + e, L, 128)], &sm.bs[1][mnmaj(cb + e, L, 128)], x);
+                    store_op8<FAST>(&sm.bs[0][mnmaj(cb + e, L, 128)], &sm.bs[1][mnmaj(cb + e, L, 128)], x);
                 }
                 umma::fence_proxy_async();
                 umma::fence_before_sync();
@@ -1198,7 +1244,7 @@ __global__ void __launch_bounds__(kChainThreads, 1) scan_chain_kernel(ScanParams
             {
                 float d[COLS], d2[COLS];
                 tmem_ld_cols<COLS>(tmem + lane_off + cD3 + cb, d);
-                tmem_ld_cols<COLS>(tmem + lane_off + cD3 + DVS + cb, d2);
+                if constexpr (!FAST) tmem_ld_cols<COLS>(tmem + lane_off + cD3 + DVS + cb, d2); else zero_cols(d2);
                 umma::tmem_wait_ld();
 #pragma unroll
                 for (int e = 0; e < COLS; ++e) d[e] += d2[e];
@@ -1209,7 +1255,7 @@ __global__ void __launch_bounds__(kChainThreads, 1) scan_chain_kernel(ScanParams
                         float x[8];
 #pragma unroll
                         for (int q = 0; q < 8; ++q) x[q] = kd * d[e + q];
-                        store_split8(&sm.bu[0][mnmaj(cb + e, t, 64)], &sm.bu[1][mnmaj(cb + e, t, 64)], x);
+                        store_op8<FAST>(&sm.bu[0][mnmaj(cb + e, t, 64)], &sm.bu[1][mnmaj(cb + e, t, 64)], x);
                     }
                     umma::fence_proxy_async();
                 } else {
@@ -1246,7 +1292,7 @@ __global__ void __launch_bounds__(kChainThreads, 1) scan_chain_kernel(ScanParams
             umma::fence_after_sync();
             float d[COLS], d2[COLS];
             tmem_ld_cols<COLS>(tmem + lane_off + cD4 + cb, d);
-            tmem_ld_cols<COLS>(tmem + lane_off + cD4 + DVS + cb, d2);
+            if constexpr (!FAST) tmem_ld_cols<COLS>(tmem + lane_off + cD4 + DVS + cb, d2); else zero_cols(d2);
             umma::tmem_wait_ld();
 #pragma unroll
             for (int e = 0; e < COLS; ++e) S[e] = fmaf(gl_prev, S[e], d[e] + d2[e]);
@@ -1342,7 +1388,8 @@ cudaError_t launch_scan(const ScanParams& p_in, cudaStream_t stream)
     if (e != cudaSuccess) return e;
     e = cudaFuncSetAttribute(scan_prep_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)prep_smem);
     if (e != cudaSuccess) return e;
-    e = cudaFuncSetAttribute(scan_chain_kernel<kDVS>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)chain_smem);
+    auto chain = p.fast ? scan_chain_kernel<kDVS, true> : scan_chain_kernel<kDVS, false>;
+    e = cudaFuncSetAttribute(chain, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)chain_smem);
     if (e != cudaSuccess) return e;
     const size_t slots = n_slots(p.T, p.n_seq);
     if (p.T == 0) {  // no gram launch to clear the failure record (rare: every sequence empty)
@@ -1358,7 +1405,7 @@ cudaError_t launch_scan(const ScanParams& p_in, cudaStream_t stream)
         e = launch_k(scan_prep_kernel, dim3(prep_ctas), dim3(kPrepThreads), prep_smem, stream, true, p);
         if (e != cudaSuccess) return e;
     }
-    return launch_k(scan_chain_kernel<kDVS>, dim3((unsigned)(p.hv * (kHeadDim / kDVS)), (unsigned)p.n_seq),
+    return launch_k(chain, dim3((unsigned)(p.hv * (kHeadDim / kDVS)), (unsigned)p.n_seq),
                     dim3(kChainThreads), chain_smem, stream, p.T > 0, p);
 }
 

@@ -214,6 +214,29 @@ GDN_API gdn_status gdn_layer(const gdn_dims* dims, int32_t n_seq, int32_t total_
                      struct CUstream_st* stream);
 
 /*
+ * gdn_scan_fast / gdn_layer_fast -- the same computations with every
+ * tensor-core product of the scan taken in one pass on bf16 operands (fp32
+ * accumulation, fp32 state) instead of the split hi/lo passes: a third of
+ * the MMA instructions, traded for accuracy.  Arguments, workspaces, layouts
+ * and errors exactly as gdn_scan / gdn_layer.  The error against the fp64
+ * reference is bounded by bf16 rounding of K, Q, the state and the chunk
+ * intermediates rather than by the 1e-4 of the split path; the tests state the
+ * bound they check.
+ */
+GDN_API gdn_status gdn_scan_fast(const gdn_dims* dims, int32_t n_seq, int32_t total_tokens,
+                                 const int32_t* cu_seqlens, const float* qn, const float* kn,
+                                 const float* vc, const float* glog, const float* beta,
+                                 const float* S_in, float* S_out, float* o, void* workspace,
+                                 size_t workspace_bytes, struct CUstream_st* stream);
+GDN_API gdn_status gdn_layer_fast(const gdn_dims* dims, int32_t n_seq, int32_t total_tokens,
+                                  const int32_t* cu_seqlens, const uint16_t* qkv, const float* conv_w,
+                                  const uint16_t* hist_in, uint16_t* hist_out, const uint16_t* a,
+                                  const uint16_t* b, const uint16_t* z, const float* A_log,
+                                  const float* dt_bias, const float* gamma, const float* S_in,
+                                  float* S_out, int32_t out_f32, void* y, void* workspace,
+                                  size_t workspace_bytes, struct CUstream_st* stream);
+
+/*
  * Failure reports of the scan.  Every wait inside the scan kernels is
  * bounded (about two seconds); one that expires makes its CTA record an
  * error in the scan workspace, release what it holds and stop, so the CUDA

@@ -225,3 +225,70 @@ def test_layer_stack_workload_sampled_heads(layer):
     # activations, zero history, S0 = 0, fp16 out) through gdn_layer as the bench calls it; every
     # fifth value head's outputs and final state against the fp64 oracle, the history bit-exact
     _check_layer(gin.stack_layer(layer), heads=list(range(layer % 5, 48, 5)))
+
+
+# ---- fast mode: one-pass bf16 tensor-core products in the scan ---------------------------
+# bf16 keeps 8 significant bits (unit roundoff u = 2^-9 ~ 1.95e-3); every product of the scan
+# rounds both operands once, and the errors of the chunk intermediates, the gS operand and the
+# look-ahead correction add.  Measured on GB300: outputs 4.6e-3 .. 9.2e-3, final state 2.6e-3 ..
+# 4.5e-3 over the cases below; the bars are ~10 u and ~5 u.
+TOL_FAST_Y, TOL_FAST_S = 2e-2, 1e-2
+
+
+def _run_layer_fast(inp):
+    import gated_deltanet_linear_pre_gb300 as gdn
+    u = U()
+    d = u.dims_of(inp)
+    x = u.device_inputs(inp)
+    T, n_seq = inp.total_tokens, inp.n_seq
+    y = torch.empty((T, d.hv, d.dv), device="cuda", dtype=torch.float32 if inp.out_f32 else torch.float16)
+    S_out, hist_out = torch.empty_like(x["S0"]), torch.empty_like(x["hist"])
+    ws = torch.empty(gdn.gdn_layer_workspace_bytes(d, n_seq, T), device="cuda", dtype=torch.uint8)
+    gdn.gdn_layer_fast(d, x["cu"], T, x["qkv"], x["conv_w"], x["hist"], hist_out, x["a"], x["b"], x["z"],
+                       x["A_log"], x["dt_bias"], x["gamma"], x["S0"], S_out, bool(inp.out_f32), y, ws)
+    return y.float().cpu().numpy(), S_out.cpu().numpy(), hist_out.cpu().numpy()
+
+
+FAST_CASES = {
+    "t300_fp16": (lambda: gin.single_layer_boundary(300, False), None),
+    "t512_fp32": (lambda: gin.single_layer_boundary(512, True), None),
+    "varlen": (lambda: gin.varlen_batch(), None),
+    "stack_layer": (lambda: gin.stack_layer(3), list(range(1, 48, 6))),
+}
+
+
+@pytest.mark.parametrize("case", list(FAST_CASES))
+def test_layer_fast_within_bf16_bound(case):
+    u = U()
+    make, heads = FAST_CASES[case]
+    inp = make()
+    ref = oracle.layer(inp, heads=heads)
+    y, S, hist = _run_layer_fast(inp)
+    hs = slice(None) if heads is None else heads
+    assert u.max_rel(y[:, hs], ref["y"][:, hs]) <= TOL_FAST_Y
+    assert u.max_rel(S[:, hs], ref["S_out"][:, hs]) <= TOL_FAST_S
+    np.testing.assert_array_equal(hist.view(np.uint16), inp_hist_bits(ref["hist_out"]))
+
+
+def test_scan_fast_differs_from_precise_only_within_the_bound():
+    # the fast entry point really takes the one-pass path (its result is not the split one's),
+    # and stays within the bound of the precise result
+    import gated_deltanet_linear_pre_gb300 as gdn
+    u = U()
+    inp = gin.single_layer_boundary(300, True)
+    ref = oracle.layer(inp, heads=[0])
+    f32 = lambda a: torch.from_numpy(np.ascontiguousarray(np.asarray(a, np.float32))).cuda()
+    q, k, v, lam, beta = (f32(ref[x]) for x in ("q", "k", "v", "lam", "beta"))
+    d = u.dims_of(inp)
+    T = inp.total_tokens
+    cu = torch.from_numpy(inp.cu_seqlens).cuda()
+    S0 = f32(inp.S0)
+    ws = torch.empty(gdn.gdn_scan_workspace_bytes(d, 1, T), device="cuda", dtype=torch.uint8)
+    outs = []
+    for fn in (gdn.gdn_scan, gdn.gdn_scan_fast):
+        o, S = torch.empty((T, d.hv, d.dv), device="cuda"), torch.empty_like(S0)
+        fn(d, cu, T, q, k, v, lam, beta, S0, S, o, ws)
+        outs.append((o.cpu().numpy(), S.cpu().numpy()))
+    (o1, S1), (o2, S2) = outs
+    assert not np.array_equal(o1, o2)
+    assert u.max_rel(o2, o1) <= TOL_FAST_Y and u.max_rel(S2, S1) <= TOL_FAST_S
