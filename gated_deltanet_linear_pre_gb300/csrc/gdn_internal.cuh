@@ -46,7 +46,6 @@ struct ScanParams {
     int withhold_first_copy;  // failure-report self-test only (gdn_scan_selftest_timeout)
     int prep_no_keepers;      // prep fallback self-test only (gdn_scan_selftest_one_taker)
     int fast;                 // one-pass bf16 products (gdn_scan_fast / gdn_layer_fast)
-    unsigned long long epoch;  // this call's tag for the per-chunk ready flags (set by launch_scan)
     int prep_sms, prep_keep;  // SMs of the device; SMs whose prep CTAs stay after round one (set by launch_scan)
 };
 

@@ -42,8 +42,6 @@
 // Every MMA is issued by one thread and completes on an mbarrier; every wait
 // is bounded and, on expiry, the CTA records an error code in the workspace,
 // drains its own copies in flight (bounded), frees its TMEM and stops.
-#include <atomic>
-#include <chrono>
 
 #include "gdn_internal.cuh"
 #include "umma.cuh"
@@ -203,7 +201,7 @@ struct ChainGates {
 };
 static_assert(sizeof(ChainGates) % 16 == 0 && sizeof(ChainGates) <= kGateBytes, "gate row");
 
-// per (chunk slot, value head): the call's epoch once prep has written that chunk's [T; P T]
+// per (chunk slot, value head): zeroed by gram, 1 once prep has written that chunk's [T; P T]
 // image and gate row (and, through its wait on gram, everything before it is complete)
 __device__ __forceinline__ unsigned long long* ready_flag(const ScanParams& p, size_t slot, int h)
 {
@@ -372,16 +370,27 @@ __global__ void __launch_bounds__(kGramThreads, 2) scan_gram_kernel(ScanParams p
     // two consecutive chunk slots of key head j; key head fastest, so the slots complete in order
     const int j = blockIdx.x, slot0 = 2 * (int)blockIdx.y;
     uint32_t* err = reinterpret_cast<uint32_t*>(p.workspace);
-    pdl_launch_dependents();
+    // no early trigger: prep (and through it the chain) launches once gram has completed, so both
+    // see the state this kernel leaves in the workspace header and the ready flags
     pdl_wait();
-    // the failure record and prep's task counter start clean: the first CTA clears them before
-    // anything could use them (an expired wait takes seconds; the later kernels of the scan
-    // start only after this one ends)
+    // the failure record and prep's counters start clean: the first CTA clears them before
+    // anything could use them (the later kernels of the scan start only after this one ends)
     if (slot0 == 0 && j == 0 && tid == 0) {
         *err = 0u;
         prep_counter(p)[0] = 0u;
         prep_counter(p)[1] = 0u;
         prep_counter(p)[2] = 0u;
+    }
+    // this CTA's two slots' ready flags, for the value heads of key head j, start at zero.  Clearing
+    // them here, rather than tagging flags with a per-call value, keeps whatever the workspace held
+    // irrelevant and needs nothing from the host per call, so a scan replayed from a captured CUDA
+    // graph is correct too
+    {
+        const int per = p.hv / p.hk;
+        for (int i = tid; i < 2 * per; i += kGramThreads) {
+            const int s = slot0 + i / per, h = j * per + i % per;
+            if ((size_t)s < n_slots(p.T, p.n_seq)) *ready_flag(p, (size_t)s, h) = 0ull;
+        }
     }
     int c0[2], n[2];
     bool has_prev[2], odd[2], used[2];
@@ -798,7 +807,7 @@ __global__ void __launch_bounds__(kPrepThreads, 4) scan_prep_kernel(ScanParams p
             // everything this chunk's chain needs is written: publish it (release, GPU scope)
             if (tid == 0) {
                 __threadfence();
-                flag_publish(ready_flag(p, slot, h), p.epoch);
+                flag_publish(ready_flag(p, slot, h), 1ull);
             }
         }  // used slot
         // after round one: if no CTA landed on an SM that stays, the last CTA to finish round one
@@ -916,6 +925,7 @@ __global__ void __launch_bounds__(kChainThreads, 1) scan_chain_kernel(ScanParams
     // (which implies every earlier kernel of the call has completed) and the copy warp for each
     // later chunk's flag, so the recurrence starts while prep's last CTAs still run
     pdl_launch_dependents();
+    // this scan's call count: gram advanced it and completed before prep, hence this grid, launched
     constexpr int SLICES = kHeadDim / DVS;
     constexpr int COLS = DVS / kChainWG;  // columns per compute thread
     constexpr uint32_t kTmemCols = 512;
@@ -953,7 +963,7 @@ __global__ void __launch_bounds__(kChainThreads, 1) scan_chain_kernel(ScanParams
         umma::mbar_init(&sm.mb_grp[0], kChainCompute / 2);
         umma::mbar_init(&sm.mb_grp[1], kChainCompute / 2);
         sm.abort_flag = 0;
-        if (n_chunks > 0 && !flag_wait(ready_flag(p, base, h), p.epoch)) {
+        if (n_chunks > 0 && !flag_wait(ready_flag(p, base, h), 1ull)) {
             sm.abort_flag = 1;
             atomicOr(err, kErrTimeout);
         }
@@ -1014,7 +1024,7 @@ __global__ void __launch_bounds__(kChainThreads, 1) scan_chain_kernel(ScanParams
             prefetch_l2(c + 2);
             {   // chunk c+1's operands are written (bounded wait for its ready flag)
                 bool ok = true;
-                if (leader) ok = flag_wait(ready_flag(p, base + c + 1, h), p.epoch);
+                if (leader) ok = flag_wait(ready_flag(p, base + c + 1, h), 1ull);
                 if (!__shfl_sync(0xffffffffu, ok ? 1 : 0, 0)) {
                     if (leader) {
                         sm.abort_flag = 1;
@@ -1340,15 +1350,6 @@ size_t scan_workspace_bytes(int hk, int hv, int n_seq, int T)
     return kWsHeader + n_slots(T, n_seq) * ((size_t)hv * (kAmBlock + 8) + (size_t)hk * (kKqBytes + kGramBytes + kMBytes));
 }
 
-// a fresh 64-bit tag per scan call for the ready flags: a workspace's stale flags (from an
-// earlier call, or uninitialised memory) never equal the current call's tag in practice
-unsigned long long next_epoch()
-{
-    static std::atomic<unsigned long long> counter{
-        (unsigned long long)std::chrono::steady_clock::now().time_since_epoch().count() * 0x9E3779B97F4A7C15ull};
-    return counter.fetch_add(0x9E3779B97F4A7C15ull) | 1ull;
-}
-
 int sm_count()
 {
     static int cached[64] = {};
@@ -1380,7 +1381,6 @@ unsigned prep_grid(ScanParams& p, size_t slots)
 cudaError_t launch_scan(const ScanParams& p_in, cudaStream_t stream)
 {
     ScanParams p = p_in;
-    p.epoch = next_epoch();
     p.prep_sms = p.prep_keep = 0;
     if (p.n_seq == 0) return cudaSuccess;
     const size_t gram_smem = sizeof(GramSmem), prep_smem = sizeof(PrepSmem), chain_smem = sizeof(ChainSmem<kDVS>);

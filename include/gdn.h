@@ -142,6 +142,10 @@ GDN_API size_t gdn_scan_workspace_bytes(const gdn_dims* dims, int32_t n_seq, int
  *      o        fp32 [T][hv][dv]        S^T q / sqrt(dk) after each token
  * workspace: device scratch of at least gdn_scan_workspace_bytes() bytes
  *            (may be NULL when that is 0); contents on entry are ignored.
+ * Stream capture: a call may be captured into a CUDA graph.  Nothing it
+ * enqueues depends on host state that changes from call to call, so each
+ * replay of the graph is a complete scan of what the captured buffers then
+ * hold.  Calls sharing one workspace must not overlap on the GPU.
  */
 GDN_API gdn_status gdn_scan(const gdn_dims* dims, int32_t n_seq, int32_t total_tokens,
                     const int32_t* cu_seqlens, const float* qn, const float* kn,
@@ -203,7 +207,8 @@ GDN_API size_t gdn_layer_workspace_bytes(const gdn_dims* dims, int32_t n_seq, in
  * `stream`, the stage tensors kept in `workspace` (the pages time the three
  * stages back to back as one pre+scan+post total, "Round 30 Track C Audit",
  * section 2).  Arguments as in the three stage calls.  S_out may equal S_in;
- * hist_out must not overlap hist_in.
+ * hist_out must not overlap hist_in.  May be captured into a CUDA graph, as
+ * gdn_scan.
  */
 GDN_API gdn_status gdn_layer(const gdn_dims* dims, int32_t n_seq, int32_t total_tokens,
                      const int32_t* cu_seqlens, const uint16_t* qkv, const float* conv_w,
