@@ -925,7 +925,6 @@ __global__ void __launch_bounds__(kChainThreads, 1) scan_chain_kernel(ScanParams
     // (which implies every earlier kernel of the call has completed) and the copy warp for each
     // later chunk's flag, so the recurrence starts while prep's last CTAs still run
     pdl_launch_dependents();
-    // this scan's call count: gram advanced it and completed before prep, hence this grid, launched
     constexpr int SLICES = kHeadDim / DVS;
     constexpr int COLS = DVS / kChainWG;  // columns per compute thread
     constexpr uint32_t kTmemCols = 512;
