@@ -368,6 +368,12 @@ static gdn_status layer_impl(const gdn_dims* dims, int32_t n_seq, int32_t T, con
         return st;
     if ((st = prep_post(dims, T, o, z, gamma, out_f32, y, op)) != GDN_OK) return st;
     sp.fast = fast;
+    // q and k go from the pre kernel straight into the scan's [K; Q] operand images (bf16 hi / lo,
+    // split exactly as the scan splits fp32 inputs), so the scan's gram kernel only copies them in
+    if (T > 0) {
+        pp.kq_images = static_cast<unsigned char*>(sws) + gdn::scan_kq_images_offset(dims->hk, dims->hv, n_seq, T);
+        sp.kq_written = 1;
+    }
     if ((st = run_pre(pp, stream)) != GDN_OK) return st;
     if ((st = run_scan(sp, stream)) != GDN_OK) return st;
     return run_post(op, stream);

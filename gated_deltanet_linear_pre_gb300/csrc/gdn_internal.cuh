@@ -11,6 +11,18 @@ namespace gdn {
 constexpr int kHeadDim = 128;  // dk == dv == 128: one head is 32 lanes x 4 channels
 constexpr int kChunk = 64;     // tokens per scan chunk
 
+// The scan's [K; Q] operand image of one (chunk slot, key head): 128 rows (the chunk's 64 k rows and
+// 64 q rows, k first for chunks at an even index within their sequence, q first for odd ones) x 128
+// columns, bf16 split into hi and lo planes, in 16 groups of 8 rows, each group its hi plane (2 KB,
+// 16 no-swizzle core matrices along the columns) then its lo plane.  Byte offset of (row r, column k)
+// in the hi plane; the lo plane is 2048 bytes behind.  Chunk slots: sequence s owns slots from
+// cu[s] / 64 + s on.
+constexpr size_t kKqImageBytes = 128 * 128 * 2 * 2;
+__host__ __device__ __forceinline__ int kq_off(int r, int k)
+{
+    return (r >> 3) * 4096 + (k >> 3) * 128 + (r & 7) * 16 + (k & 7) * 2;
+}
+
 struct PreParams {
     int hk, hv, C, T, n_seq;
     float eps;
@@ -28,6 +40,9 @@ struct PreParams {
     float* vc;
     float* glog;
     float* beta;
+    // inside gdn_layer: q and k go straight into the scan's [K; Q] images (qn and kn unused); the
+    // images of slot `slot`, key head j start at kq_images + (slot * hk + j) * kKqImageBytes
+    unsigned char* kq_images;
 };
 
 struct ScanParams {
@@ -47,6 +62,7 @@ struct ScanParams {
     int prep_no_keepers;      // prep fallback self-test only (gdn_scan_selftest_one_taker)
     int fast;                 // one-pass bf16 products (gdn_scan_fast / gdn_layer_fast)
     int prep_sms, prep_keep;  // SMs of the device; SMs whose prep CTAs stay after round one (set by launch_scan)
+    int kq_written;           // the pre kernel wrote the [K; Q] images (qn and kn unused; gdn_layer)
 };
 
 struct PostParams {
@@ -82,6 +98,7 @@ struct StepParams {
 cudaError_t launch_pre(const PreParams& p, cudaStream_t stream);
 cudaError_t launch_step(const StepParams& p, cudaStream_t stream);
 size_t scan_workspace_bytes(int hk, int hv, int n_seq, int T);
+size_t scan_kq_images_offset(int hk, int hv, int n_seq, int T);  // byte offset of the [K; Q] images in the workspace
 cudaError_t launch_scan(const ScanParams& p, cudaStream_t stream);
 cudaError_t launch_post(const PostParams& p, cudaStream_t stream);
 

@@ -15,6 +15,8 @@
 // slides the 3-token window in registers and writes 16-byte fp32 stores.
 // The q/k norms are warp reductions.  A separate row of blocks writes the
 // carried history of every sequence.
+#include <cuda_bf16.h>
+
 #include "gdn_internal.cuh"
 
 namespace gdn {
@@ -73,6 +75,31 @@ __device__ __forceinline__ float conv4(float w0, float w1, float w2, float w3, f
     return acc;
 }
 
+// One token's normalised q or k head (4 channels per lane) into the scan's [K; Q] image:
+// bf16 hi / lo split (hi = bf16(x), lo = bf16(x - hi), as the scan splits its fp32
+// inputs), then lanes 2m and 2m+1, which hold columns 8m..8m+7, trade halves so
+// that the even lane stores the 16-byte hi piece and the odd lane the lo piece.
+// pos: the token's position in its sequence; slot0: the sequence's first slot.
+__device__ __forceinline__ void store_kq(unsigned char* img_j, size_t slot_stride, int slot0, int pos, bool is_k,
+                                         int lane, float y0, float y1, float y2, float y3)
+{
+    const int ci = pos >> 6, r = pos & 63;
+    const bool odd = (ci & 1) != 0;
+    const int row = ((is_k == odd) ? 64 : 0) + r;  // k first in even chunks, q first in odd ones
+    const __nv_bfloat162 h01 = __floats2bfloat162_rn(y0, y1), h23 = __floats2bfloat162_rn(y2, y3);
+    const float2 f01 = __bfloat1622float2(h01), f23 = __bfloat1622float2(h23);
+    const __nv_bfloat162 l01 = __floats2bfloat162_rn(y0 - f01.x, y1 - f01.y);
+    const __nv_bfloat162 l23 = __floats2bfloat162_rn(y2 - f23.x, y3 - f23.y);
+    const uint32_t uh01 = *reinterpret_cast<const uint32_t*>(&h01), uh23 = *reinterpret_cast<const uint32_t*>(&h23);
+    const uint32_t ul01 = *reinterpret_cast<const uint32_t*>(&l01), ul23 = *reinterpret_cast<const uint32_t*>(&l23);
+    const bool ev = (lane & 1) == 0;
+    const uint32_t g0 = __shfl_xor_sync(0xffffffffu, ev ? ul01 : uh01, 1);
+    const uint32_t g1 = __shfl_xor_sync(0xffffffffu, ev ? ul23 : uh23, 1);
+    const uint4 out = ev ? make_uint4(uh01, uh23, g0, g1) : make_uint4(g0, g1, ul01, ul23);
+    unsigned char* dst = img_j + (size_t)(slot0 + ci) * slot_stride + kq_off(row, 8 * (lane >> 1)) + (ev ? 0 : 2048);
+    *reinterpret_cast<uint4*>(dst) = out;
+}
+
 // A whole block inside one sequence: no per-token checks, the output pointer
 // advances by a fixed row stride.  kNorm: a q/k head (L2-normalised).
 template <bool kNorm>
@@ -99,6 +126,8 @@ __device__ __forceinline__ void conv_block(const uint2 (&cur)[kTokBlk], F4 win0,
     }
 }
 
+// kImg: q and k go to the scan's [K; Q] images (inside gdn_layer) instead of qn / kn
+template <bool kImg>
 __global__ void __launch_bounds__(kThreads, 8)
 pre_kernel(PreParams p, int n_slots, int head_groups, int n_conv_blocks)
 {
@@ -163,7 +192,60 @@ pre_kernel(PreParams p, int n_slots, int head_groups, int n_conv_blocks)
         win2 = tap4(p, seq, seq_start, pos - 1, c);
     }
 
-    if (t_end - t_begin == kTokBlk && t_end <= seq_end) {  // the common case
+    // inside gdn_layer, q and k go to the scan's images
+    const size_t slot_stride = (size_t)hk * kKqImageBytes;
+    unsigned char* img_j = kImg ? p.kq_images + (size_t)(is_q ? slot : slot - hk) * kKqImageBytes : nullptr;
+
+    if (kImg && t_end - t_begin == kTokBlk && t_end <= seq_end && vh < 0) {  // the common case, image output
+        // When the 8 tokens are one 8-row group of one chunk's image (the sequence starts at a multiple
+        // of 8), that group is 4 contiguous KB (hi plane, lo plane): stage the split rows in shared
+        // memory (row-major, 272-byte rows so that neither side's accesses conflict) and write the
+        // 4 KB with 512 contiguous bytes per warp store.  Otherwise each token goes out on its own.
+        constexpr int kRow = 272, kPlane = kTokBlk * kRow;
+        __shared__ __align__(16) unsigned char kq_stage[kWarps][2 * kPlane];
+        unsigned char* stg = kq_stage[warp];
+        const int pos0 = t_begin - seq_start, slot0 = seq_start / kChunk + seq;
+        const bool grouped = (pos0 & 7) == 0;
+#pragma unroll
+        for (int i = 0; i < kTokBlk; ++i) {
+            const F4 x = unpack_half4(cur[i]);
+            float y0 = silu_fast(conv4(w0.x, w0.y, w0.z, w0.w, win0.x, win1.x, win2.x, x.x));
+            float y1 = silu_fast(conv4(w1.x, w1.y, w1.z, w1.w, win0.y, win1.y, win2.y, x.y));
+            float y2 = silu_fast(conv4(w2.x, w2.y, w2.z, w2.w, win0.z, win1.z, win2.z, x.z));
+            float y3 = silu_fast(conv4(w3.x, w3.y, w3.z, w3.w, win0.w, win1.w, win2.w, x.w));
+            win0 = win1;
+            win1 = win2;
+            win2 = x;
+            const float inv = rsqrtf(warp_sum(y0 * y0 + y1 * y1 + y2 * y2 + y3 * y3) + p.eps);
+            y0 *= inv; y1 *= inv; y2 *= inv; y3 *= inv;
+            if (grouped) {
+                const __nv_bfloat162 h01 = __floats2bfloat162_rn(y0, y1), h23 = __floats2bfloat162_rn(y2, y3);
+                const float2 f01 = __bfloat1622float2(h01), f23 = __bfloat1622float2(h23);
+                const __nv_bfloat162 l01 = __floats2bfloat162_rn(y0 - f01.x, y1 - f01.y);
+                const __nv_bfloat162 l23 = __floats2bfloat162_rn(y2 - f23.x, y3 - f23.y);
+                *reinterpret_cast<uint2*>(stg + i * kRow + lane * 8) =
+                    make_uint2(*reinterpret_cast<const uint32_t*>(&h01), *reinterpret_cast<const uint32_t*>(&h23));
+                *reinterpret_cast<uint2*>(stg + kPlane + i * kRow + lane * 8) =
+                    make_uint2(*reinterpret_cast<const uint32_t*>(&l01), *reinterpret_cast<const uint32_t*>(&l23));
+            } else {
+                store_kq(img_j, slot_stride, slot0, pos0 + i, is_k, lane, y0, y1, y2, y3);
+            }
+        }
+        if (grouped) {
+            __syncwarp();
+            const int ci = pos0 >> 6;
+            const int row0 = ((is_k == ((ci & 1) != 0)) ? 64 : 0) + (pos0 & 63);
+            unsigned char* dst = img_j + (size_t)(slot0 + ci) * slot_stride + (row0 >> 3) * 4096;
+            // 16-byte piece `lane` of each 512-byte run: plane k / 4, core matrix 4 (k % 4) + lane / 8
+            // (columns 8 m .. 8 m + 7), row lane % 8
+#pragma unroll
+            for (int k = 0; k < 8; ++k) {
+                const int m = (k & 3) * 4 + (lane >> 3), i = lane & 7;
+                *reinterpret_cast<uint4*>(dst + k * 512 + lane * 16) =
+                    *reinterpret_cast<const uint4*>(stg + (k >> 2) * kPlane + i * kRow + m * 16);
+            }
+        }
+    } else if (t_end - t_begin == kTokBlk && t_end <= seq_end) {  // the common case
         if (vh >= 0)
             conv_block<false>(cur, win0, win1, win2, w0, w1, w2, w3,
                               p.vc + ((size_t)t_begin * p.hv + vh) * kHeadDim + lane * 4, (size_t)p.hv * kHeadDim,
@@ -206,6 +288,10 @@ pre_kernel(PreParams p, int n_slots, int head_groups, int n_conv_blocks)
             ss = warp_sum(ss);
             const float inv = rsqrtf(ss + p.eps);
             y0 *= inv; y1 *= inv; y2 *= inv; y3 *= inv;
+            if constexpr (kImg) {
+                store_kq(img_j, slot_stride, seq_start / kChunk + seq, t - seq_start, is_k, lane, y0, y1, y2, y3);
+                continue;
+            }
             const int j = is_q ? slot : slot - hk;
             dst = (is_k ? p.kn : p.qn) + ((size_t)t * hk + j) * kHeadDim + lane * 4;
         }
@@ -236,8 +322,10 @@ cudaError_t launch_pre(const PreParams& p, cudaStream_t stream)
     const long long blocks = n_conv_blocks + n_hist_blocks;
     if (blocks == 0) return cudaSuccess;
     if (blocks > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
-    return launch_k(pre_kernel, dim3((unsigned)blocks), dim3(kThreads), 0, stream, true, p, n_slots, head_groups,
-                    (int)n_conv_blocks);
+    return p.kq_images ? launch_k(pre_kernel<true>, dim3((unsigned)blocks), dim3(kThreads), 0, stream, true, p, n_slots,
+                                  head_groups, (int)n_conv_blocks)
+                       : launch_k(pre_kernel<false>, dim3((unsigned)blocks), dim3(kThreads), 0, stream, true, p, n_slots,
+                                  head_groups, (int)n_conv_blocks);
 }
 
 }  // namespace gdn

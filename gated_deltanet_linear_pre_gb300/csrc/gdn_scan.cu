@@ -60,10 +60,9 @@ constexpr size_t kAmBlock = kAmBytes + kGateBytes; // [T; P T] image followed by
 constexpr size_t kWsHeader = 4096;                // error words
 constexpr int kDVS = 64;                          // value columns per chain CTA
 
-// [K; Q] image of a chunk (bytes): 16 groups of 8 rows, each group its hi plane
-// (2 KB, 16 core matrices along K) then its lo plane, so that any run of row
-// groups, e.g. one 64-row half, is one contiguous block
-__device__ __forceinline__ int kq_off(int r, int k) { return (r >> 3) * 4096 + (k >> 3) * 128 + (r & 7) * 16 + (k & 7) * 2; }
+// [K; Q] image of a chunk: kq_off (the shared header); any run of row groups, e.g. one 64-row
+// half, is one contiguous block
+static_assert(kKqBytes == kKqImageBytes, "[K; Q] image size");
 
 // element offsets inside no-swizzle core-matrix tiles (bf16, 64 elements per core matrix)
 __device__ __forceinline__ int kmaj(int r, int k, int Kd) { return ((r >> 3) * (Kd >> 3) + (k >> 3)) * 64 + (r & 7) * 8 + (k & 7); }
@@ -178,6 +177,12 @@ __device__ __forceinline__ unsigned char* kq_image(const ScanParams& p, size_t s
     return static_cast<unsigned char*>(p.workspace) + kWsHeader + n_slots(p.T, p.n_seq) * p.hv * kAmBlock +
            (slot * p.hk + j) * kKqBytes;
 }
+
+// (K K^T ; Q K^T) of a (chunk slot, key head): 128 rows x 64 fp32, stored by 4-column groups,
+// the float4 of (row r, columns [4 g, 4 g + 4)) at index g * 128 + r, so that the gram kernels,
+// which write a row per thread, and prep, which reads one the same way, both move 512 contiguous
+// bytes per warp access
+__device__ __forceinline__ int gram_f4(int r, int g) { return g * 128 + r; }
 
 __device__ __forceinline__ float* gram_rows(const ScanParams& p, size_t slot, int j)
 {
@@ -301,11 +306,12 @@ __device__ __forceinline__ float warp_chunk_cumsum(float (&lam)[2], int lane)
 constexpr int kGramThreads = 256;
 
 struct __align__(1024) GramSmem {
-    uint16_t akq[2][128 * 128];  // split [K; Q] (K-major)
-    uint16_t bkp[2][64 * 128];   // split K of the previous chunk (K-major B, 64 rows)
+    uint16_t akq[2][128 * 128];  // split [K; Q] (K-major); the image-input kernel: the [K; Q] image
+    uint16_t bkp[2][64 * 128];   // split K of the previous chunk (K-major B, 64 rows); image input: its image half
     uint32_t tmem_base;
     int abort_flag;
     uint64_t mbar;
+    uint64_t mb_load;  // image input: the bulk copies
 };
 
 // 64 token rows x 128 fp32 of one key head, 32 values per thread: unit u = tid + kThreads q
@@ -473,9 +479,10 @@ __global__ void __launch_bounds__(kGramThreads, 2) scan_gram_kernel(ScanParams p
             float d[32];
             umma::tmem_ld32(tmem + lane_off + 32 * wg, d);
             umma::tmem_wait_ld();
-            float4* dst = reinterpret_cast<float4*>(gram_rows(p, slot, j) + L * 64 + 32 * wg);
+            float4* dst = reinterpret_cast<float4*>(gram_rows(p, slot, j));
 #pragma unroll
-            for (int q = 0; q < 8; ++q) dst[q] = make_float4(d[4 * q], d[4 * q + 1], d[4 * q + 2], d[4 * q + 3]);
+            for (int q = 0; q < 8; ++q)
+                dst[gram_f4(L, 8 * wg + q)] = make_float4(d[4 * q], d[4 * q + 1], d[4 * q + 2], d[4 * q + 3]);
             if (has_prev[t]) {  // M rows -> split K-major image (K = 64 tokens of the previous chunk), Q rows first for odd chunks
                 const int mrow = odd[t] ? (L ^ 64) : L;
                 umma::tmem_ld32(tmem + lane_off + 64 + 32 * wg, d);
@@ -495,6 +502,116 @@ __global__ void __launch_bounds__(kGramThreads, 2) scan_gram_kernel(ScanParams p
         umma::fence_before_sync();
         __syncthreads();
         umma::fence_after_sync();
+    }
+    umma::fence_before_sync();
+    __syncthreads();
+    if (warp == 0) umma::tmem_dealloc(sm.tmem_base, 128);
+}
+
+// gram with the [K; Q] images already written (by the pre kernel, inside gdn_layer): one CTA
+// per (chunk slot, key head) bulk-copies the slot's image and the previous chunk's k half,
+// zeroes the rows past a ragged last chunk (in shared memory for its products and in the
+// image for the chain) and forms the same products as scan_gram_kernel.  The image rows are in
+// the chunk's stacking order, so the products' rows are too: (K K^T ; Q K^T) rows are swapped
+// back for odd chunks, the M image keeps them.
+constexpr uint32_t kHalfBytes = 64 * 128 * 2 * 2;  // one 64-row half of an image, hi + lo
+
+__global__ void __launch_bounds__(kGramThreads, 2) scan_gram_img_kernel(ScanParams p)
+{
+    extern __shared__ __align__(1024) unsigned char smem_raw[];
+    GramSmem& sm = *reinterpret_cast<GramSmem*>(smem_raw);
+    const int tid = threadIdx.x, warp = tid >> 5;
+    const int L = tid & 127, wg = tid >> 7;
+    const int j = blockIdx.x, slot = (int)blockIdx.y;
+    uint32_t* err = reinterpret_cast<uint32_t*>(p.workspace);
+    // no early trigger (as scan_gram_kernel): prep and the chain start after this kernel completes
+    pdl_wait();
+    if (slot == 0 && j == 0 && tid == 0) {
+        *err = 0u;
+        prep_counter(p)[0] = 0u;
+        prep_counter(p)[1] = 0u;
+        prep_counter(p)[2] = 0u;
+    }
+    {   // this slot's ready flags, for the value heads of key head j, start at zero
+        const int per = p.hv / p.hk;
+        for (int i = tid; i < per; i += kGramThreads) *ready_flag(p, (size_t)slot, j * per + i) = 0ull;
+    }
+    int c0, n;
+    bool has_prev, odd;
+    if (!slot_chunk(p, slot, c0, n, &has_prev, &odd)) return;  // a slot no sequence uses
+
+    unsigned char* img_s = reinterpret_cast<unsigned char*>(sm.akq);
+    unsigned char* kp_s = reinterpret_cast<unsigned char*>(sm.bkp);
+    unsigned char* img = kq_image(p, (size_t)slot, j);
+    if (warp == 0) umma::tmem_alloc(&sm.tmem_base, 128);
+    if (tid == 0) {
+        umma::mbar_init(&sm.mbar, 1);
+        umma::mbar_init(&sm.mb_load, 1);
+        sm.abort_flag = 0;
+        // the previous chunk's k half: its first half if that chunk is even (k first), else its second
+        umma::mbar_arrive_expect_tx(&sm.mb_load, (uint32_t)kKqBytes + (has_prev ? kHalfBytes : 0u));
+        umma::bulk_g2s(img_s, img, (uint32_t)kKqBytes, &sm.mb_load);
+        if (has_prev) umma::bulk_g2s(kp_s, kq_image(p, (size_t)slot - 1, j) + (odd ? 0u : kHalfBytes), kHalfBytes, &sm.mb_load);
+    }
+    umma::fence_before_sync();
+    __syncthreads();
+    umma::fence_after_sync();
+    if (!umma::mbar_wait(&sm.mb_load, 0)) { sm.abort_flag = 1; atomicOr(err, kErrTimeout); }
+    if (n < kChunk) {  // rows past the chunk's end (both halves): zero here and in the image
+        for (int i = tid; i < 128 * 32; i += kGramThreads) {
+            const int row = i >> 5, pc = i & 31;
+            if ((row & 63) < n) continue;
+            const int off = (row >> 3) * 4096 + (pc & 15) * 128 + (row & 7) * 16 + (pc >> 4) * 2048;
+            *reinterpret_cast<uint4*>(img_s + off) = make_uint4(0u, 0u, 0u, 0u);
+            *reinterpret_cast<uint4*>(img + off) = make_uint4(0u, 0u, 0u, 0u);
+        }
+    }
+    umma::fence_proxy_async();
+    umma::fence_before_sync();
+    __syncthreads();
+    umma::fence_after_sync();
+    if (!sm.abort_flag) {
+        const uint32_t tmem = sm.tmem_base;
+        if (tid == 0) {
+            const uint32_t a_hi = umma::smem_u32(img_s), b_hi = a_hi + (odd ? kHalfBytes : 0u), kp = umma::smem_u32(kp_s);
+            constexpr uint32_t id = umma::idesc_bf16(128, 64, false, false);
+            if (p.fast) {
+                mma_one(tmem, a_hi, 128, 4096, 256, b_hi, 4096, 256, 8, id);
+                if (has_prev) mma_one(tmem + 64, a_hi, 128, 4096, 256, kp, 4096, 256, 8, id);
+            } else {
+                mma_split(tmem, a_hi, a_hi + 2048, 128, 4096, 256, b_hi, b_hi + 2048, 4096, 256, 8, id);
+                if (has_prev) mma_split(tmem + 64, a_hi, a_hi + 2048, 128, 4096, 256, kp, kp + 2048, 4096, 256, 8, id);
+            }
+            umma::commit(&sm.mbar);
+        }
+        if (!umma::mbar_wait(&sm.mbar, 0)) { sm.abort_flag = 1; atomicOr(err, kErrTimeout); }
+        __syncthreads();
+        umma::fence_after_sync();
+        if (!sm.abort_flag) {
+            const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
+            float d[32];
+            umma::tmem_ld32(tmem + lane_off + 32 * wg, d);
+            umma::tmem_wait_ld();
+            // gram rows in (K K^T ; Q K^T) order: image row L of an odd chunk is row L ^ 64 there
+            float4* dst = reinterpret_cast<float4*>(gram_rows(p, (size_t)slot, j));
+            const int grow = odd ? (L ^ 64) : L;
+#pragma unroll
+            for (int q = 0; q < 8; ++q)
+                dst[gram_f4(grow, 8 * wg + q)] = make_float4(d[4 * q], d[4 * q + 1], d[4 * q + 2], d[4 * q + 3]);
+            if (has_prev) {  // M rows, already in stacking order -> split K-major image (K = 64 previous tokens)
+                umma::tmem_ld32(tmem + lane_off + 64 + 32 * wg, d);
+                umma::tmem_wait_ld();
+                unsigned char* mimg = m_image(p, (size_t)slot, j);
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    uint4 vh, vl;
+                    split8(d + 8 * q, vh, vl);
+                    const int off = kmaj(L, 32 * wg + 8 * q, 64);
+                    *reinterpret_cast<uint4*>(mimg + off * 2) = vh;
+                    *reinterpret_cast<uint4*>(mimg + kMBytes / 2 + off * 2) = vl;
+                }
+            }
+        }
     }
     umma::fence_before_sync();
     __syncthreads();
@@ -586,10 +703,10 @@ __global__ void __launch_bounds__(kPrepThreads, 4) scan_prep_kernel(ScanParams p
             // L < 64, Q K^T for L >= 64), columns [32 wg, 32 wg + 32)
             float d[32];
             {
-                const float4* src = reinterpret_cast<const float4*>(gram_rows(p, slot, j) + L * 64 + 32 * wg);
+                const float4* src = reinterpret_cast<const float4*>(gram_rows(p, slot, j));
 #pragma unroll
                 for (int q = 0; q < 8; ++q) {
-                    const float4 x = __ldg(src + q);
+                    const float4 x = __ldg(src + gram_f4(L, 8 * wg + q));
                     d[4 * q] = x.x; d[4 * q + 1] = x.y; d[4 * q + 2] = x.z; d[4 * q + 3] = x.w;
                 }
             }
@@ -1344,6 +1461,12 @@ done:
 
 }  // namespace
 
+size_t scan_kq_images_offset(int hk, int hv, int n_seq, int T)
+{
+    (void)hk;
+    return kWsHeader + n_slots(T, n_seq) * (size_t)hv * kAmBlock;
+}
+
 size_t scan_workspace_bytes(int hk, int hv, int n_seq, int T)
 {
     return kWsHeader + n_slots(T, n_seq) * ((size_t)hv * (kAmBlock + 8) + (size_t)hk * (kKqBytes + kGramBytes + kMBytes));
@@ -1383,7 +1506,8 @@ cudaError_t launch_scan(const ScanParams& p_in, cudaStream_t stream)
     p.prep_sms = p.prep_keep = 0;
     if (p.n_seq == 0) return cudaSuccess;
     const size_t gram_smem = sizeof(GramSmem), prep_smem = sizeof(PrepSmem), chain_smem = sizeof(ChainSmem<kDVS>);
-    cudaError_t e = cudaFuncSetAttribute(scan_gram_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)gram_smem);
+    cudaError_t e = cudaFuncSetAttribute(p.kq_written ? scan_gram_img_kernel : scan_gram_kernel,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)gram_smem);
     if (e != cudaSuccess) return e;
     e = cudaFuncSetAttribute(scan_prep_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)prep_smem);
     if (e != cudaSuccess) return e;
@@ -1398,8 +1522,10 @@ cudaError_t launch_scan(const ScanParams& p_in, cudaStream_t stream)
         // each kernel may start while its predecessor drains and waits for it before reading
         const unsigned prep_ctas = prep_grid(p, slots);
         if (p.prep_no_keepers) p.prep_keep = 0;  // self-test: the round-one fallback takes every later task
-        e = launch_k(scan_gram_kernel, dim3((unsigned)p.hk, (unsigned)((slots + 1) / 2)), dim3(kGramThreads), gram_smem,
-                     stream, true, p);
+        e = p.kq_written ? launch_k(scan_gram_img_kernel, dim3((unsigned)p.hk, (unsigned)slots), dim3(kGramThreads),
+                                    gram_smem, stream, true, p)
+                         : launch_k(scan_gram_kernel, dim3((unsigned)p.hk, (unsigned)((slots + 1) / 2)),
+                                    dim3(kGramThreads), gram_smem, stream, true, p);
         if (e != cudaSuccess) return e;
         e = launch_k(scan_prep_kernel, dim3(prep_ctas), dim3(kPrepThreads), prep_smem, stream, true, p);
         if (e != cudaSuccess) return e;

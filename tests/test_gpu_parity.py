@@ -292,3 +292,59 @@ def test_scan_fast_differs_from_precise_only_within_the_bound():
     (o1, S1), (o2, S2) = outs
     assert not np.array_equal(o1, o2)
     assert u.max_rel(o2, o1) <= TOL_FAST_Y and u.max_rel(S2, S1) <= TOL_FAST_S
+
+
+def _stages_then_layer(inp, fast=False):
+    """The same layer through gdn_pre + gdn_scan(_fast) + gdn_post and through gdn_layer(_fast),
+    on the same device inputs; returns both (y, S_out, hist_out) triples."""
+    import gpu_util as u
+    import gated_deltanet_linear_pre_gb300 as gdn
+    torch = pytest.importorskip("torch")
+    d = u.dims_of(inp)
+    x = u.device_inputs(inp)
+    T, n_seq = inp.total_tokens, inp.n_seq
+    f = dict(device="cuda", dtype=torch.float32)
+    ydt = torch.float32 if inp.out_f32 else torch.float16
+    qn, kn = torch.empty((T, d.hk, d.dk), **f), torch.empty((T, d.hk, d.dk), **f)
+    vc, o = torch.empty((T, d.hv, d.dv), **f), torch.empty((T, d.hv, d.dv), **f)
+    glog, beta = torch.empty((T, d.hv), **f), torch.empty((T, d.hv), **f)
+    outs = []
+    for staged in (True, False):
+        y = torch.full((T, d.hv, d.dv), float("nan"), device="cuda", dtype=ydt)
+        S, hist = torch.empty_like(x["S0"]), torch.empty_like(x["hist"])
+        if staged:
+            ws = torch.empty(gdn.gdn_scan_workspace_bytes(d, n_seq, T), device="cuda", dtype=torch.uint8)
+            gdn.gdn_pre(d, x["cu"], T, x["qkv"], x["conv_w"], x["hist"], hist, x["a"], x["b"], x["A_log"],
+                        x["dt_bias"], qn, kn, vc, glog, beta)
+            (gdn.gdn_scan_fast if fast else gdn.gdn_scan)(d, x["cu"], T, qn, kn, vc, glog, beta, x["S0"], S, o, ws)
+            gdn.gdn_post(d, T, o, x["z"], x["gamma"], bool(inp.out_f32), y)
+        else:
+            # a workspace full of set bits: whatever it held must not matter
+            ws = torch.full((gdn.gdn_layer_workspace_bytes(d, n_seq, T),), 0xFF, device="cuda", dtype=torch.uint8)
+            (gdn.gdn_layer_fast if fast else gdn.gdn_layer)(
+                d, x["cu"], T, x["qkv"], x["conv_w"], x["hist"], hist, x["a"], x["b"], x["z"], x["A_log"],
+                x["dt_bias"], x["gamma"], x["S0"], S, bool(inp.out_f32), y, ws)
+        torch.cuda.synchronize()
+        outs.append((y, S, hist))
+    return outs
+
+
+LAYER_EQ_CASES = {
+    "T=300 ragged last chunk": lambda: gin.single_layer_boundary(300, False),
+    "T=512 fp32 out": lambda: gin.single_layer_boundary(512, True),
+    "T=1": lambda: gin.single_layer_boundary(1, False),
+    "varlen with a one-token and an empty sequence": lambda: gin.make_layer(
+        41, [130, 1, 0, 64, 259], hist_nonzero=True, S0_std=0.02),
+    "varlen batch": lambda: gin.varlen_batch(),
+}
+
+
+@pytest.mark.parametrize("fast", [False, True], ids=["precise", "fast"])
+@pytest.mark.parametrize("case", list(LAYER_EQ_CASES))
+def test_layer_equals_the_three_stage_calls_bitwise(case, fast):
+    """gdn_layer writes q and k straight into the scan's operand images; the images hold the same
+    bits the scan makes from gdn_pre's fp32 outputs, so every output matches the stage calls exactly."""
+    torch = pytest.importorskip("torch")
+    staged, layer = _stages_then_layer(LAYER_EQ_CASES[case](), fast)
+    for name, a, b in zip(("y", "S_out", "hist_out"), staged, layer):
+        assert torch.equal(a, b), name
