@@ -1456,6 +1456,11 @@ done:
     umma::fence_before_sync();
     __syncthreads();
     if (warp == 0) umma::tmem_dealloc(sm.tmem_base, kTmemCols);
+    // This grid completes only after prep's has: the next call's kernels wait on this grid alone,
+    // and a prep CTA may still be taking its last (empty) ticket from the task counter that the next
+    // call's gram clears.  By now prep has published every flag this CTA consumed, so the wait is
+    // short (no measurable cost).
+    pdl_wait();
 #undef GDN_WAIT
 }
 
