@@ -140,3 +140,37 @@ def test_scan_ignores_what_the_workspace_held():
         outs.append((o, S))
     assert torch.equal(outs[0][0], outs[1][0]) and torch.equal(outs[0][1], outs[1][1])
     assert np.isfinite(outs[1][0].cpu().numpy()).all()
+
+
+def test_back_to_back_batches_of_different_shapes_share_one_workspace():
+    """Calls queued back to back on one workspace (sized for the largest) with different batch shapes:
+    every call's counters, flags and images start from what the previous call left, and each result
+    must equal the same call on a fresh workspace."""
+    import gpu_util as u
+    import gated_deltanet_linear_pre_gb300 as gdn
+    batches = [gin.make_layer(36, [1500, 40, 700], hist_nonzero=True, S0_std=0.02),
+               gin.stack_layer(5),
+               gin.make_layer(37, [64] * 9 + [3], hist_nonzero=True, S0_std=0.02),
+               gin.make_layer(38, [2047], hist_nonzero=True, S0_std=0.02)]
+    dims = [u.dims_of(b) for b in batches]
+    shared = torch.empty(max(gdn.gdn_layer_workspace_bytes(d, b.n_seq, b.total_tokens) for d, b in zip(dims, batches)),
+                         device="cuda", dtype=torch.uint8)
+    xs = [u.device_inputs(b) for b in batches]
+
+    def run(i, ws):
+        b, d, x = batches[i], dims[i], xs[i]
+        y = torch.empty((b.total_tokens, d.hv, d.dv), device="cuda", dtype=torch.float16)
+        S, hist = torch.empty_like(x["S0"]), torch.empty_like(x["hist"])
+        gdn.gdn_layer(d, x["cu"], b.total_tokens, x["qkv"], x["conv_w"], x["hist"], hist, x["a"], x["b"], x["z"],
+                      x["A_log"], x["dt_bias"], x["gamma"], x["S0"], S, False, y, ws)
+        return y, S, hist
+
+    queued = [run(i, shared) for i in range(len(batches))]  # no synchronisation between the calls
+    torch.cuda.synchronize()
+    for i in range(len(batches)):
+        b, d = batches[i], dims[i]
+        fresh = run(i, torch.empty(gdn.gdn_layer_workspace_bytes(d, b.n_seq, b.total_tokens), device="cuda",
+                                   dtype=torch.uint8))
+        torch.cuda.synchronize()
+        for got, want in zip(queued[i], fresh):
+            assert torch.equal(got, want), i
