@@ -468,12 +468,47 @@ def main():
     # buffer's writer behind its previous reader across steps.
     e2e = None
     if not args.no_e2e:
-        y_host = [torch.empty((T, HV, DV), dtype=torch.float16).pin_memory() for _ in range(LAYERS)]
-        S_host = [torch.empty_like(h["S0"]).pin_memory() for h in host]
-        hist_host = [torch.empty_like(h["hist"]).pin_memory() for h in host]
+        # Each layer's activations (qkv, a, b, z, hist, S0) sit in one pinned host buffer and one device
+        # buffer of the same layout, 256-byte aligned pieces, so that a step moves them in one copy per
+        # layer; likewise its outputs (y, S_out, hist_out).  Weights stay resident, as in the metric.
         acts = ("qkv", "a", "b", "z", "hist", "S0")
-        h2d = sum(host[l][k].numel() * host[l][k].element_size() for l in range(LAYERS) for k in acts)
-        d2h = sum(t.numel() * t.element_size() for ts in (y_host, S_host, hist_host) for t in ts)
+        in_specs = [(k, host[0][k].dtype, tuple(host[0][k].shape)) for k in acts]
+        out_specs = [("y", torch.float16, (T, HV, DV)), ("S_out", host[0]["S0"].dtype, tuple(host[0]["S0"].shape)),
+                     ("hist_out", host[0]["hist"].dtype, tuple(host[0]["hist"].shape))]
+
+        def packed(specs):
+            off, pos = {}, 0
+            for name, dt, shape in specs:
+                off[name] = pos
+                n = 1
+                for e in shape:
+                    n *= e
+                pos += (n * torch.empty((), dtype=dt).element_size() + 255) // 256 * 256
+            return off, pos
+
+        def views(buf, specs, off):
+            out = {}
+            for name, dt, shape in specs:
+                n = 1
+                for e in shape:
+                    n *= e
+                nbytes = n * torch.empty((), dtype=dt).element_size()
+                out[name] = buf[off[name]:off[name] + nbytes].view(dt).view(shape)
+            return out
+
+        in_off, in_bytes = packed(in_specs)
+        out_off, out_bytes = packed(out_specs)
+        in_host = [torch.empty(in_bytes, dtype=torch.uint8).pin_memory() for _ in range(LAYERS)]
+        in_dev = [torch.empty(in_bytes, dtype=torch.uint8, device=dev) for _ in range(LAYERS)]
+        out_host = [torch.empty(out_bytes, dtype=torch.uint8).pin_memory() for _ in range(LAYERS)]
+        out_dev = [torch.empty(out_bytes, dtype=torch.uint8, device=dev) for _ in range(LAYERS)]
+        for l in range(LAYERS):
+            hv = views(in_host[l], in_specs, in_off)
+            for k in acts:
+                hv[k].copy_(host[l][k])
+        xin = [views(b, in_specs, in_off) for b in in_dev]
+        xout = [views(b, out_specs, out_off) for b in out_dev]
+        h2d, d2h = in_bytes * LAYERS, out_bytes * LAYERS
         s_in, s_out = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
         ev_in = [torch.cuda.Event() for _ in range(LAYERS)]
         ev_comp = [torch.cuda.Event() for _ in range(LAYERS)]
@@ -484,23 +519,20 @@ def main():
 
         def e2e_step():
             for l in range(LAYERS):
-                x = devl[l]
+                w, x, o = devl[l], xin[l], xout[l]
                 with torch.cuda.stream(s_in):
                     s_in.wait_event(ev_comp[l])  # the previous step's compute has read these inputs
-                    for k in acts:
-                        x[k].copy_(host[l][k], non_blocking=True)
+                    in_dev[l].copy_(in_host[l], non_blocking=True)
                     ev_in[l].record(s_in)
                 stream.wait_event(ev_in[l])
-                stream.wait_event(ev_out[l])  # the previous step's read-back of y/S/hist is done
-                layer_fn(d, cu, T, x["qkv"], x["conv_w"], x["hist"], hist_out[l], x["a"], x["b"], x["z"],
-                              x["A_log"], x["dt_bias"], x["gamma"], x["S0"], S_out[l], False, y[l], layer_ws,
-                              stream=stream)
+                stream.wait_event(ev_out[l])  # the previous step's read-back of the outputs is done
+                layer_fn(d, cu, T, x["qkv"], w["conv_w"], x["hist"], o["hist_out"], x["a"], x["b"], x["z"],
+                         w["A_log"], w["dt_bias"], w["gamma"], x["S0"], o["S_out"], False, o["y"], layer_ws,
+                         stream=stream)
                 ev_comp[l].record(stream)
                 with torch.cuda.stream(s_out):
                     s_out.wait_event(ev_comp[l])
-                    y_host[l].copy_(y[l], non_blocking=True)
-                    S_host[l].copy_(S_out[l], non_blocking=True)
-                    hist_host[l].copy_(hist_out[l], non_blocking=True)
+                    out_host[l].copy_(out_dev[l], non_blocking=True)
                     ev_out[l].record(s_out)
 
         for _ in range(max(1, args.warmup)):
