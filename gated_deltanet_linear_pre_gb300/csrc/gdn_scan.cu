@@ -246,6 +246,13 @@ __device__ __forceinline__ unsigned int* prep_counter(const ScanParams& p)
     return reinterpret_cast<unsigned int*>(static_cast<unsigned char*>(p.workspace) + 64);
 }
 
+// per SM id (header bytes 1024..2047): prep CTAs that have arrived on that SM, cleared by gram
+constexpr int kSmSlots = 256;
+__device__ __forceinline__ unsigned int* prep_sm_arrivals(const ScanParams& p)
+{
+    return reinterpret_cast<unsigned int*>(static_cast<unsigned char*>(p.workspace) + 1024);
+}
+
 // whether this CTA's SM keeps taking prep tasks after round one: the SMs in the first
 // prep_keep / prep_sms of the SM-id range (ids may leave gaps up to %nsmid)
 __device__ __forceinline__ bool prep_sm_stays(const ScanParams& p)
@@ -304,6 +311,7 @@ __device__ __forceinline__ float warp_chunk_cumsum(float (&lam)[2], int lane)
 // still in shared memory.
 // =======================================================================================
 constexpr int kGramThreads = 256;
+static_assert(kGramThreads == kSmSlots, "gram's first CTA clears one SM slot per thread");
 
 struct __align__(1024) GramSmem {
     uint16_t akq[2][128 * 128];  // split [K; Q] (K-major); the image-input kernel: the [K; Q] image
@@ -387,6 +395,7 @@ __global__ void __launch_bounds__(kGramThreads, 2) scan_gram_kernel(ScanParams p
         prep_counter(p)[1] = 0u;
         prep_counter(p)[2] = 0u;
     }
+    if (slot0 == 0 && j == 0) prep_sm_arrivals(p)[tid] = 0u;  // kGramThreads == kSmSlots
     // this CTA's two slots' ready flags, for the value heads of key head j, start at zero.  Clearing
     // them here, rather than tagging flags with a per-call value, keeps whatever the workspace held
     // irrelevant and needs nothing from the host per call, so a scan replayed from a captured CUDA
@@ -532,6 +541,7 @@ __global__ void __launch_bounds__(kGramThreads, 2) scan_gram_img_kernel(ScanPara
         prep_counter(p)[1] = 0u;
         prep_counter(p)[2] = 0u;
     }
+    if (slot == 0 && j == 0) prep_sm_arrivals(p)[tid] = 0u;  // kGramThreads == kSmSlots
     {   // this slot's ready flags, for the value heads of key head j, start at zero
         const int per = p.hv / p.hk;
         for (int i = tid; i < per; i += kGramThreads) *ready_flag(p, (size_t)slot, j * per + i) = 0ull;
@@ -622,6 +632,13 @@ __global__ void __launch_bounds__(kGramThreads, 2) scan_gram_img_kernel(ScanPara
 // prep: one CTA per (chunk slot, value head)
 // =======================================================================================
 constexpr int kPrepThreads = 256;  // two warpgroups: each covers all 128 TMEM lanes, half the columns
+// round-one CTAs per SM the chain takes (of the four resident): the fewer, the sooner those SMs
+// are free, but the smaller the lead the staying CTAs start with over a chain that consumes
+// tasks faster than they produce them (T=2048: split-product scan 136.7 us with 1, 138.8 with 2,
+// 141.7 with 4; one-pass products, whose chain consumes faster, layer 162.0 us with 2, 159.9 with
+// 3, 162.4 with 4)
+constexpr int kRound1PerSm = 1;
+constexpr int kRound1PerSmFast = 3;
 
 struct __align__(1024) PrepSmem {
     uint16_t ap[2][64 * 64];   // P (K-major, 64 rows); an M = 128 descriptor reads its rows 64-127 from
@@ -657,20 +674,47 @@ __global__ void __launch_bounds__(kPrepThreads, 4) scan_prep_kernel(ScanParams p
     }
     uint32_t phase = 0;
     // Tasks (chunk slot, value head) in slot order, the value head fastest, so the chunk slots
-    // complete in order across all heads.  Round one: CTA b takes task b.  After it only the CTAs
-    // on the SMs chosen to stay take further tasks, in order, from the counter that gram cleared;
-    // the others exit, and their SMs take the chain's CTAs, which start on the first round's
-    // chunks while the remaining prep CTAs keep ahead of them.
+    // complete in order across all heads; every task index comes, in order, from the counter that
+    // gram cleared.  The CTAs on the SMs chosen to stay take tasks until none is left.  On the
+    // other SMs, which the chain's CTAs take as soon as they are free, only the first
+    // kRound1PerSm CTAs (kRound1PerSmFast with one-pass products) to arrive take one task (round
+    // one) and the rest leave at once, so that
+    // those SMs free up sooner while round one still puts the stayers ahead of the chain.
     const unsigned n_tasks = (unsigned)(n_slots(p.T, p.n_seq) * (size_t)p.hv);
     bool stays = prep_sm_stays(p);
     unsigned int* counter = prep_counter(p);
-    if (stays && tid == 0) {  // CTAs that stay register before their round one
-        atomicAdd(counter + 2, 1u);
-        __threadfence();
+    // no CTA stays: the last CTA to finish round one (or to skip it) stays whatever its SM, so the
+    // remaining tasks always have a taker
+    auto round_one_done = [&]() {
+        if (atomicAdd(counter + 1, 1u) + 1u == gridDim.x) {
+            __threadfence();
+            if (atomicAdd(counter + 2, 0u) == 0u) stays = true;
+        }
+    };
+    bool first = false;  // thread 0: this CTA's round-one task is yet to be counted
+    if (tid == 0) {
+        unsigned t = n_tasks;
+        if (stays) {  // CTAs that stay register before their round one
+            atomicAdd(counter + 2, 1u);
+            __threadfence();
+            t = atomicAdd(counter, 1u);
+            first = true;
+        } else {
+            uint32_t smid;
+            asm volatile("mov.u32 %0, %%smid;" : "=r"(smid));
+            if (atomicAdd(prep_sm_arrivals(p) + (smid % kSmSlots), 1u) < (unsigned)(p.fast ? kRound1PerSmFast : kRound1PerSm)) {
+                t = atomicAdd(counter, 1u);
+                first = true;
+            } else {  // skips round one, counted now
+                round_one_done();
+                if (stays) t = atomicAdd(counter, 1u);
+            }
+        }
+        sm.next[1] = t;
     }
-    bool first = true;
+    __syncthreads();
     int nx = 0;
-    for (unsigned task = blockIdx.x; task < n_tasks;) {
+    for (unsigned task = sm.next[1]; task < n_tasks;) {
         const int h = (int)(task % (unsigned)p.hv), slot = (int)(task / (unsigned)p.hv), j = h / (p.hv / p.hk);
         int c0, n;
         bool odd;
@@ -927,15 +971,10 @@ __global__ void __launch_bounds__(kPrepThreads, 4) scan_prep_kernel(ScanParams p
                 flag_publish(ready_flag(p, slot, h), 1ull);
             }
         }  // used slot
-        // after round one: if no CTA landed on an SM that stays, the last CTA to finish round one
-        // stays whatever its SM, so the remaining tasks always have a taker; thread 0 fetches the
-        // next task
+        // thread 0 fetches the next task (after round one, counted for the fallback above)
         if (tid == 0) {
-            if (first && atomicAdd(counter + 1, 1u) + 1u == gridDim.x) {
-                __threadfence();
-                if (atomicAdd(counter + 2, 0u) == 0u) stays = true;
-            }
-            sm.next[nx] = stays ? gridDim.x + atomicAdd(counter, 1u) : n_tasks;
+            if (first) round_one_done();
+            sm.next[nx] = stays ? atomicAdd(counter, 1u) : n_tasks;
         }
         first = false;
         __syncthreads();
