@@ -129,7 +129,7 @@ namespace {
 gdn_status prep_pre(const gdn_dims* dims, int32_t n_seq, int32_t T, const int32_t* cu_seqlens,
                     const uint16_t* qkv, const float* conv_w, const uint16_t* hist_in, uint16_t* hist_out,
                     const uint16_t* a, const uint16_t* b, const float* A_log, const float* dt_bias, float* qn,
-                    float* kn, float* vc, float* glog, float* beta, gdn::PreParams& p)
+                    float* kn, float* vc, float* glog, float* beta, gdn::PreParams& p, bool kq_images = false)
 {
     gdn_status st;
     if ((st = check_dims(dims)) != GDN_OK) return st;
@@ -140,7 +140,8 @@ gdn_status prep_pre(const gdn_dims* dims, int32_t n_seq, int32_t T, const int32_
         {hist_in, n_seq * C * 6, "hist_in"}, {hist_out, n_seq * C * 6, "hist_out"},
         {a, tt * hv * 2, "a"},           {b, tt * hv * 2, "b"},
         {A_log, hv * 4, "A_log"},        {dt_bias, hv * 4, "dt_bias"},
-        {qn, tt * hk * d * 4, "qn"},     {kn, tt * hk * d * 4, "kn"},
+        // inside gdn_layer q and k go to the scan's images instead (no qn / kn buffers)
+        {qn, kq_images ? 0 : tt * hk * d * 4, "qn"}, {kn, kq_images ? 0 : tt * hk * d * 4, "kn"},
         {vc, tt * hv * d * 4, "vc"},     {glog, tt * hv * 4, "glog"},
         {beta, tt * hv * 4, "beta"},
     };
@@ -172,14 +173,15 @@ gdn_status run_pre(const gdn::PreParams& p, struct CUstream_st* stream)
 gdn_status prep_scan(const gdn_dims* dims, int32_t n_seq, int32_t T, const int32_t* cu_seqlens,
                      const float* qn, const float* kn, const float* vc, const float* glog, const float* beta,
                      const float* S_in, float* S_out, float* o, void* workspace, size_t workspace_bytes,
-                     gdn::ScanParams& p)
+                     gdn::ScanParams& p, bool kq_images = false)
 {
     gdn_status st;
     if ((st = check_dims(dims)) != GDN_OK) return st;
     if ((st = check_batch(n_seq, T, cu_seqlens)) != GDN_OK) return st;
     const size_t hk = dims->hk, hv = dims->hv, d = dims->dk, tt = (size_t)T;
     const Buf bufs[] = {
-        {qn, tt * hk * d * 4, "qn"},   {kn, tt * hk * d * 4, "kn"},   {vc, tt * hv * d * 4, "vc"},
+        {qn, kq_images ? 0 : tt * hk * d * 4, "qn"}, {kn, kq_images ? 0 : tt * hk * d * 4, "kn"},
+        {vc, tt * hv * d * 4, "vc"},
         {glog, tt * hv * 4, "glog"},   {beta, tt * hv * 4, "beta"},
         {S_in, n_seq * hv * d * d * 4, "S_in"}, {S_out, n_seq * hv * d * d * 4, "S_out"},
         {o, tt * hv * d * 4, "o"},
@@ -226,11 +228,12 @@ gdn_status read_failure_word(const void* word, struct CUstream_st* stream)
     return GDN_OK;
 }
 
-// offset of the scan workspace inside a gdn_layer workspace (the stage tensors come first)
+// offset of the scan workspace inside a gdn_layer workspace (the stage tensors vc, o, glog and beta
+// come first; q and k live only in the scan workspace's images)
 size_t layer_scan_offset(const gdn_dims* dims, int32_t T)
 {
-    const size_t hk = dims->hk, hv = dims->hv, d = dims->dk, tt = (size_t)T;
-    return align256(tt * hk * d * 4) * 2 + align256(tt * hv * d * 4) * 2 + align256(tt * hv * 4) * 2;
+    const size_t hv = dims->hv, d = dims->dk, tt = (size_t)T;
+    return align256(tt * hv * d * 4) * 2 + align256(tt * hv * 4) * 2;
 }
 
 gdn_status prep_post(const gdn_dims* dims, int32_t T, const float* o, const uint16_t* z, const float* gamma,
@@ -316,9 +319,8 @@ gdn_status gdn_post(const gdn_dims* dims, int32_t T, const float* o, const uint1
 size_t gdn_layer_workspace_bytes(const gdn_dims* dims, int32_t n_seq, int32_t T)
 {
     if (!dims || n_seq < 0 || T < 0) return 0;
-    const size_t hk = dims->hk, hv = dims->hv, d = dims->dk, tt = (size_t)T;
-    size_t total = 0;
-    total += align256(tt * hk * d * 4) * 2;  // qn, kn
+    const size_t hv = dims->hv, d = dims->dk, tt = (size_t)T;
+    size_t total = 0;                         // no qn, kn: q and k go straight into the scan's images
     total += align256(tt * hv * d * 4) * 2;  // vc, o
     total += align256(tt * hv * 4) * 2;      // glog, beta
     total += align256(gdn::scan_workspace_bytes(dims->hk, dims->hv, n_seq, T));
@@ -339,11 +341,12 @@ static gdn_status layer_impl(const gdn_dims* dims, int32_t n_seq, int32_t T, con
     if (workspace_bytes < need || (need && !workspace))
         return fail(GDN_ERR_WORKSPACE, "layer workspace %zu bytes, need %zu", workspace_bytes, need);
     if (need && !aligned16(workspace)) return fail(GDN_ERR_ALIGNMENT, "workspace is not 16-byte aligned");
-    const size_t hk = dims->hk, hv = dims->hv, d = dims->dk, tt = (size_t)T;
+    const size_t hv = dims->hv, d = dims->dk, tt = (size_t)T;
     char* w = static_cast<char*>(workspace);
     auto carve = [&](size_t bytes) { char* r = w; w += align256(bytes); return r; };
-    float* qn = reinterpret_cast<float*>(carve(tt * hk * d * 4));
-    float* kn = reinterpret_cast<float*>(carve(tt * hk * d * 4));
+    // (no qn / kn: q and k go from the pre kernel straight into the scan's [K; Q] operand images,
+    // bf16 hi / lo split exactly as the scan splits fp32 inputs, and the scan's gram kernel only
+    // copies them in)
     float* vc = reinterpret_cast<float*>(carve(tt * hv * d * 4));
     float* o = reinterpret_cast<float*>(carve(tt * hv * d * 4));
     float* glog = reinterpret_cast<float*>(carve(tt * hv * 4));
@@ -360,16 +363,14 @@ static gdn_status layer_impl(const gdn_dims* dims, int32_t n_seq, int32_t T, con
     gdn::PreParams pp;
     gdn::ScanParams sp;
     gdn::PostParams op;
-    if ((st = prep_pre(dims, n_seq, T, cu_seqlens, qkv, conv_w, hist_in, hist_out, a, b, A_log, dt_bias, qn,
-                       kn, vc, glog, beta, pp)) != GDN_OK)
+    if ((st = prep_pre(dims, n_seq, T, cu_seqlens, qkv, conv_w, hist_in, hist_out, a, b, A_log, dt_bias, nullptr,
+                       nullptr, vc, glog, beta, pp, true)) != GDN_OK)
         return st;
-    if ((st = prep_scan(dims, n_seq, T, cu_seqlens, qn, kn, vc, glog, beta, S_in, S_out, o, sws, scan_ws,
-                        sp)) != GDN_OK)
+    if ((st = prep_scan(dims, n_seq, T, cu_seqlens, nullptr, nullptr, vc, glog, beta, S_in, S_out, o, sws, scan_ws,
+                        sp, true)) != GDN_OK)
         return st;
     if ((st = prep_post(dims, T, o, z, gamma, out_f32, y, op)) != GDN_OK) return st;
     sp.fast = fast;
-    // q and k go from the pre kernel straight into the scan's [K; Q] operand images (bf16 hi / lo,
-    // split exactly as the scan splits fp32 inputs), so the scan's gram kernel only copies them in
     if (T > 0) {
         pp.kq_images = static_cast<unsigned char*>(sws) + gdn::scan_kq_images_offset(dims->hk, dims->hv, n_seq, T);
         sp.kq_written = 1;

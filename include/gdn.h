@@ -198,8 +198,9 @@ GDN_API gdn_status gdn_scan_noalloc(const gdn_dims* dims, int32_t n_seq, int32_t
                                     const float* S_in, float* S_out, float* o,
                                     struct CUstream_st* stream);
 
-/* Workspace bytes gdn_layer needs: the stage tensors qn, kn, vc, glog, beta,
- * o plus the scan's own workspace, each 256-byte aligned. */
+/* Workspace bytes gdn_layer needs: the stage tensors vc, glog, beta, o plus
+ * the scan's own workspace, each 256-byte aligned (q and k go from the pre
+ * stage straight into the scan's operand images there: no qn / kn). */
 GDN_API size_t gdn_layer_workspace_bytes(const gdn_dims* dims, int32_t n_seq, int32_t total_tokens);
 
 /*
