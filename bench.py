@@ -160,11 +160,17 @@ STAGE_SOURCES = {"pre": ["gdn_pre.cu"], "scan": ["gdn_scan.cu", "umma.cuh"], "po
 
 
 def source_digest(stage: str) -> str:
+    """SHA-256 of the stage's CUDA sources with comments and blank space removed, so that a capture
+    stays valid across comment edits and goes stale at any change of code."""
     import hashlib
+    import re
     h = hashlib.sha256()
     for name in STAGE_SOURCES[stage] + ["gdn_internal.cuh"]:
-        with open(os.path.join(ROOT, "gated_deltanet_linear_pre_gb300", "csrc", name), "rb") as f:
-            h.update(f.read())
+        with open(os.path.join(ROOT, "gated_deltanet_linear_pre_gb300", "csrc", name)) as f:
+            text = f.read()
+        text = re.sub(r"/\*.*?\*/", " ", text, flags=re.S)  # block comments
+        text = re.sub(r"//[^\n]*", " ", text)                # line comments
+        h.update(" ".join(text.split()).encode())
     return h.hexdigest()
 
 

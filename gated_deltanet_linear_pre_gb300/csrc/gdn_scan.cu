@@ -26,8 +26,11 @@
 //  * scan_gram_kernel, one CTA per (two chunks, key head), fully parallel: splits
 //    [K; Q] into the tensor-core layout (the chain's [K; Q] image), forms
 //    (K K^T ; Q K^T) in fp32, and M = [K; Q] K_prev^T against the previous
-//    chunk's keys (the chain's look-ahead operand).
-//  * scan_prep_kernel, one CTA per (chunk, value head), fully parallel: A and
+//    chunk's keys (the chain's look-ahead operand).  Inside gdn_layer the pre
+//    kernel writes the images itself and scan_gram_img_kernel (one CTA per
+//    (chunk, key head)) copies them in and forms the same products.
+//  * scan_prep_kernel, persistent CTAs taking (chunk, value head) tasks in
+//    order, beside the chain once it runs: A and
 //    P from the key head's gram rows and the head's gates, the inverse of
 //    I + A (recursive halving with 16x16 diagonal blocks by forward
 //    substitution, on CUDA cores) and P T on the tensor core; writes the
@@ -387,8 +390,9 @@ __global__ void __launch_bounds__(kGramThreads, 2) scan_gram_kernel(ScanParams p
     // no early trigger: prep (and through it the chain) launches once gram has completed, so both
     // see the state this kernel leaves in the workspace header and the ready flags
     pdl_wait();
-    // the failure record and prep's counters start clean: the first CTA clears them before
-    // anything could use them (the later kernels of the scan start only after this one ends)
+    // the failure record, prep's counters and its per-SM arrival counts start clean: the first CTA
+    // clears them before anything could use them (the later kernels of the scan start only after
+    // this one ends)
     if (slot0 == 0 && j == 0 && tid == 0) {
         *err = 0u;
         prep_counter(p)[0] = 0u;
@@ -629,7 +633,7 @@ __global__ void __launch_bounds__(kGramThreads, 2) scan_gram_img_kernel(ScanPara
 }
 
 // =======================================================================================
-// prep: one CTA per (chunk slot, value head)
+// prep: persistent CTAs, one (chunk slot, value head) task at a time
 // =======================================================================================
 constexpr int kPrepThreads = 256;  // two warpgroups: each covers all 128 TMEM lanes, half the columns
 // round-one CTAs per SM the chain takes (of the four resident): the fewer, the sooner those SMs
@@ -678,8 +682,8 @@ __global__ void __launch_bounds__(kPrepThreads, 4) scan_prep_kernel(ScanParams p
     // gram cleared.  The CTAs on the SMs chosen to stay take tasks until none is left.  On the
     // other SMs, which the chain's CTAs take as soon as they are free, only the first
     // kRound1PerSm CTAs (kRound1PerSmFast with one-pass products) to arrive take one task (round
-    // one) and the rest leave at once, so that
-    // those SMs free up sooner while round one still puts the stayers ahead of the chain.
+    // one) and the rest leave at once, so that those SMs free up sooner while round one still puts
+    // the stayers ahead of the chain.
     const unsigned n_tasks = (unsigned)(n_slots(p.T, p.n_seq) * (size_t)p.hv);
     bool stays = prep_sm_stays(p);
     unsigned int* counter = prep_counter(p);
