@@ -46,6 +46,8 @@
 // is bounded and, on expiry, the CTA records an error code in the workspace,
 // drains its own copies in flight (bounded), frees its TMEM and stops.
 
+#include <cstddef>
+
 #include "gdn_internal.cuh"
 #include "umma.cuh"
 
@@ -324,6 +326,10 @@ struct __align__(1024) GramSmem {
     uint64_t mbar;
     uint64_t mb_load;  // image input: the bulk copies
 };
+// bulk-copy destinations and operand tiles on 16-byte boundaries
+static_assert(offsetof(GramSmem, akq) % 16 == 0 && offsetof(GramSmem, bkp) % 16 == 0 &&
+                  offsetof(GramSmem, mbar) % 8 == 0 && offsetof(GramSmem, mb_load) % 8 == 0,
+              "gram shared-memory alignment");
 
 // 64 token rows x 128 fp32 of one key head, 32 values per thread: unit u = tid + kThreads q
 // covers row t (8 rows per group of 8 core-matrix rows) and columns [8 g, 8 g + 8)
@@ -658,6 +664,10 @@ struct __align__(1024) PrepSmem {
     uint32_t next[2];  // the next task, broadcast from thread 0 (alternating slots)
     uint64_t mbar;
 };
+// operand tiles (tensor-core descriptors, 16-byte vector accesses) on 16-byte boundaries
+static_assert(offsetof(PrepSmem, ap) % 16 == 0 && offsetof(PrepSmem, u) % 16 == 0 && offsetof(PrepSmem, T) % 16 == 0 &&
+                  offsetof(PrepSmem, W) % 16 == 0 && offsetof(PrepSmem, mbar) % 8 == 0,
+              "prep shared-memory alignment");
 
 __global__ void __launch_bounds__(kPrepThreads, 4) scan_prep_kernel(ScanParams p)
 {
@@ -1040,6 +1050,14 @@ struct __align__(1024) ChainSmem {
     uint64_t mb_x, mb_s, mb_u;            // compute -> producer (all compute threads arrive)
     uint64_t mb_grp[2];                   // row groups of the compute threads (lanes 0-63 / 64-127)
 };
+// bulk-copy destinations, operand tiles and the fp32 staging tile (read as float4) on 16-byte
+// boundaries; the struct fits the 227 KB a CTA may have
+static_assert(offsetof(ChainSmem<64>, kh) % 16 == 0 && offsetof(ChainSmem<64>, mm) % 16 == 0 &&
+                  offsetof(ChainSmem<64>, am) % 16 == 0 && offsetof(ChainSmem<64>, gb) % 16 == 0 &&
+                  offsetof(ChainSmem<64>, bs) % 16 == 0 && offsetof(ChainSmem<64>, bx) % 16 == 0 &&
+                  offsetof(ChainSmem<64>, bu) % 16 == 0 && offsetof(ChainSmem<64>, mb_kq) % 8 == 0,
+              "chain shared-memory alignment");
+static_assert(sizeof(ChainSmem<64>) <= 232448, "chain shared memory");
 
 // fp32 64 x 64 staging tile over bx: row r, 16-byte column chunk k at chunk
 // (k ^ (r & 15)) of the row, so that a warp's 32 rows hit distinct banks
