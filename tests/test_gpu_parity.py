@@ -336,6 +336,9 @@ LAYER_EQ_CASES = {
     "varlen with a one-token and an empty sequence": lambda: gin.make_layer(
         41, [130, 1, 0, 64, 259], hist_nonzero=True, S0_std=0.02),
     "varlen batch": lambda: gin.varlen_batch(),
+    # many short sequences: more chain CTAs than SMs (every SM keeps prep tasks) and sequence starts
+    # off the 8-token grid (pre's per-token image stores)
+    "300 short sequences": lambda: gin.make_layer(42, n_seq_random=300, max_len=100, hist_nonzero=True, S0_std=0.02),
 }
 
 
