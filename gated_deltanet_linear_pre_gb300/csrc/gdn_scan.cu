@@ -648,6 +648,10 @@ constexpr int kPrepThreads = 256;  // two warpgroups: each covers all 128 TMEM l
 // 141.7 with 4; one-pass products, whose chain consumes faster, layer 162.0 us with 2, 159.9 with
 // 3, 162.4 with 4)
 constexpr int kRound1PerSm = 1;
+// chunk slots above which prep defers each task's ready flag into its next task (T=32768: layer
+// 2459-2489 -> 2400-2454 us, the 8-sequence varlen batch 1213 -> 1200 us; one T=2048 prompt, 33
+// slots, would lose 1.4 us)
+constexpr int kDeferFlagsAbove = 64;
 constexpr int kRound1PerSmFast = 3;
 
 struct __align__(1024) PrepSmem {
@@ -706,6 +710,12 @@ __global__ void __launch_bounds__(kPrepThreads, 4) scan_prep_kernel(ScanParams p
         }
     };
     bool first = false;  // thread 0: this CTA's round-one task is yet to be counted
+    // With many chunk slots prep is the scan's bottleneck: a task's ready flag is then published early in
+    // the CTA's next task, where the fence before it (waiting for the image writes) runs under that
+    // task's loads.  With few (one T=2048 prompt: 33) the chain is the bottleneck and consumes each
+    // flag soon after it is set, so it is published at once.
+    const bool defer_flags = n_slots(p.T, p.n_seq) > (size_t)kDeferFlagsAbove;
+    int pend_slot = -1, pend_h = 0;  // the ready flag waiting to be published (deferred mode)
     if (tid == 0) {
         unsigned t = n_tasks;
         if (stays) {  // CTAs that stay register before their round one
@@ -768,6 +778,13 @@ __global__ void __launch_bounds__(kPrepThreads, 4) scan_prep_kernel(ScanParams p
                     d[4 * q] = x.x; d[4 * q + 1] = x.y; d[4 * q + 2] = x.z; d[4 * q + 3] = x.w;
                 }
             }
+            // the previous task's flag: its fence (which waits for that task's image writes) runs under
+            // this task's loads, in a warp that only loads here
+            if (tid == kPrepThreads - 32 && pend_slot >= 0) {
+                __threadfence();
+                flag_publish(ready_flag(p, (size_t)pend_slot, pend_h), 1ull);
+            }
+            pend_slot = -1;
             __syncthreads();
             umma::fence_after_sync();
             const uint32_t tmem = sm.tmem_base;
@@ -980,7 +997,10 @@ __global__ void __launch_bounds__(kPrepThreads, 4) scan_prep_kernel(ScanParams p
             }
 
             // everything this chunk's chain needs is written: publish it (release, GPU scope)
-            if (tid == 0) {
+            if (defer_flags) {
+                pend_slot = slot;
+                pend_h = h;
+            } else if (tid == 0) {
                 __threadfence();
                 flag_publish(ready_flag(p, slot, h), 1ull);
             }
@@ -996,6 +1016,10 @@ __global__ void __launch_bounds__(kPrepThreads, 4) scan_prep_kernel(ScanParams p
         nx ^= 1;
     }
 
+    if (tid == kPrepThreads - 32 && pend_slot >= 0) {  // the last task's flag
+        __threadfence();
+        flag_publish(ready_flag(p, (size_t)pend_slot, pend_h), 1ull);
+    }
     umma::fence_before_sync();
     __syncthreads();
     if (warp == 0) umma::tmem_dealloc(sm.tmem_base, 64);
