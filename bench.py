@@ -68,6 +68,8 @@ def parse():
     ap.add_argument("--fast", action="store_true",
                     help="prefill through gdn_scan_fast / gdn_layer_fast (one-pass bf16 scan products)")
     ap.add_argument("--batch", type=int, default=256, help="sequences per decode step (--mode decode)")
+    ap.add_argument("--out-f32", action="store_true",
+                    help="prefill with fp32 output (the pages' second output mode; no published total to compare)")
     return ap.parse_args()
 
 
@@ -394,7 +396,9 @@ def main():
     cu = torch.tensor([0, T_PROMPT], dtype=torch.int32, device=dev)
     T = T_PROMPT
     f32 = dict(device=dev, dtype=torch.float32)
-    y = [torch.empty((T, HV, DV), device=dev, dtype=torch.float16) for _ in range(LAYERS)]
+    out_f32 = bool(args.out_f32)
+    ydt = torch.float32 if out_f32 else torch.float16
+    y = [torch.empty((T, HV, DV), device=dev, dtype=ydt) for _ in range(LAYERS)]
     hist_out = [torch.empty_like(x["hist"]) for x in devl]
     S_out = [torch.empty_like(x["S0"]) for x in devl]
     # stage tensors shared by all layers (the layers run in stream order)
@@ -411,7 +415,7 @@ def main():
     def step():
         for l, x in enumerate(devl):
             layer_fn(d, cu, T, x["qkv"], x["conv_w"], x["hist"], hist_out[l], x["a"], x["b"], x["z"], x["A_log"],
-                     x["dt_bias"], x["gamma"], x["S0"], S_out[l], False, y[l], layer_ws, stream=stream)
+                     x["dt_bias"], x["gamma"], x["S0"], S_out[l], out_f32, y[l], layer_ws, stream=stream)
 
     # per-stage pass: each stage's launches for all layers back to back (per-layer stage tensors),
     # so that every stage is timed in the steady state it runs in inside the stack
@@ -423,7 +427,7 @@ def main():
                                           x["A_log"], x["dt_bias"], t["qn"], t["kn"], t["vc"], t["glog"], t["beta"]),
         "scan": lambda l, x, t: scan_fn(d, cu, T, t["qn"], t["kn"], t["vc"], t["glog"], t["beta"], x["S0"],
                                             S_out[l], t["o"], scan_ws),
-        "post": lambda l, x, t: gdn.gdn_post(d, T, t["o"], x["z"], x["gamma"], False, y[l]),
+        "post": lambda l, x, t: gdn.gdn_post(d, T, t["o"], x["z"], x["gamma"], out_f32, y[l]),
     }
 
     def stage_group(name):
@@ -479,7 +483,7 @@ def main():
         # layer; likewise its outputs (y, S_out, hist_out).  Weights stay resident, as in the metric.
         acts = ("qkv", "a", "b", "z", "hist", "S0")
         in_specs = [(k, host[0][k].dtype, tuple(host[0][k].shape)) for k in acts]
-        out_specs = [("y", torch.float16, (T, HV, DV)), ("S_out", host[0]["S0"].dtype, tuple(host[0]["S0"].shape)),
+        out_specs = [("y", ydt, (T, HV, DV)), ("S_out", host[0]["S0"].dtype, tuple(host[0]["S0"].shape)),
                      ("hist_out", host[0]["hist"].dtype, tuple(host[0]["hist"].shape))]
 
         def packed(specs):
@@ -533,7 +537,7 @@ def main():
                 stream.wait_event(ev_in[l])
                 stream.wait_event(ev_out[l])  # the previous step's read-back of the outputs is done
                 layer_fn(d, cu, T, x["qkv"], w["conv_w"], x["hist"], o["hist_out"], x["a"], x["b"], x["z"],
-                         w["A_log"], w["dt_bias"], w["gamma"], x["S0"], o["S_out"], False, o["y"], layer_ws,
+                         w["A_log"], w["dt_bias"], w["gamma"], x["S0"], o["S_out"], out_f32, o["y"], layer_ws,
                          stream=stream)
                 ev_comp[l].record(stream)
                 with torch.cuda.stream(s_out):
@@ -561,7 +565,7 @@ def main():
 
     hbm_peak, tf_peak, peak_src = load_peaks()
     stage_bytes = {"pre": PRE_BYTES_TOK * T + PRE_BYTES_SEQ, "scan": SCAN_BYTES_TOK * T + SCAN_BYTES_SEQ,
-                   "post": POST_BYTES_TOK * T + DV * 4}
+                   "post": (POST_BYTES_TOK + (HV * DV * 2 if out_f32 else 0)) * T + DV * 4}
     stages = {}
     for k in ("pre", "scan", "post"):
         gbs = stage_bytes[k] / (per_launch_ms[k] * 1e-3) / 1e9
@@ -578,11 +582,14 @@ def main():
         cpu = cpu_baseline(layers_np, T, min(18, LAYERS))
 
     if rank == 0:
-        line = {"metric": METRIC + (" [fast: one-pass bf16 scan products]" if args.fast else ""),
+        line = {"metric": METRIC + (" [fast: one-pass bf16 scan products]" if args.fast else "")
+                          + (" [fp32 output]" if out_f32 else ""),
                 "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
                 "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
-                "vs_baseline": value / PAGES_TOKENS_PER_S, "dtype": "bf16" if args.fast else "f32", "data": "synthetic",
-                "config": {"workload": WORKLOAD, "layers": LAYERS, "seq_len": T, "global_batch": world,
+                "vs_baseline": None if out_f32 else value / PAGES_TOKENS_PER_S, "dtype": "bf16" if args.fast else "f32",
+                "data": "synthetic",
+                "config": {"workload": WORKLOAD.replace("fp16 output", "fp32 output") if out_f32 else WORKLOAD,
+                           "layers": LAYERS, "seq_len": T, "global_batch": world,
                            "parallelism": f"replicas{world}", "l2": "inputs larger than L2 (36-layer set ~2.3 GB)"},
                 "roofline": roofline, "stages": stages,
                 "timed_call": layer_fn.__name__,
