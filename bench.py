@@ -200,6 +200,28 @@ def load_peaks():
 
 
 # ---- CPU baseline (the fp64 oracle, as it stands) ----------------------------------------
+def host_cpu() -> dict:
+    """The host cores the oracle runs on: its OpenMP threads, the cores this process may use and the
+    CPU model (lscpu's, else /proc/cpuinfo's, else the machine type)."""
+    import platform
+    import subprocess
+    model = None
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.lower().startswith("model name"):
+                model = line.split(":", 1)[1].strip()
+                break
+    except (OSError, subprocess.SubprocessError):
+        pass
+    if not model and os.path.exists("/proc/cpuinfo"):
+        for line in open("/proc/cpuinfo"):
+            if line.lower().startswith(("model name", "cpu part")):
+                model = line.split(":", 1)[1].strip()
+                break
+    return {"affinity_cores": len(os.sched_getaffinity(0)), "cpu_model": model or platform.machine()}
+
+
 def cpu_baseline(layers_np, tokens: int, n_layers: int):
     """Time the oracle on `n_layers` layers x the first `tokens` tokens; returns the
     stack's prompt tokens/s it implies and a description of the sample."""
@@ -216,7 +238,7 @@ def cpu_baseline(layers_np, tokens: int, n_layers: int):
     value = tokens * n_layers / dt / METRIC_LAYERS
     return {"value": value, "unit": "tokens/s", "cores": oracle.threads(), "kind": "oracle",
             "sample": f"{n_layers} of the 36 layers x first {tokens} tokens, all 48 heads, fp64 token-sequential "
-                      f"oracle ({dt:.1f} s wall), scaled to the 36-layer stack"}
+                      f"oracle ({dt:.1f} s wall), scaled to the 36-layer stack", **host_cpu()}
 
 
 def run_reference(args, rank, world):
@@ -246,7 +268,7 @@ def run_reference(args, rank, world):
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
             "data": "synthetic", "config": {"workload": WORKLOAD, "layers": LAYERS, "seq_len": T_PROMPT},
             "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": oracle.threads(), "kind": "oracle",
-                             "sample": sample},
+                             "sample": sample, **host_cpu()},
             "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
     return 0
@@ -335,7 +357,7 @@ def run_decode(args, rank, world, local):
         dt = time.perf_counter() - t0
         cpu = {"value": B * n_cpu / dt / METRIC_LAYERS, "unit": "tokens/s", "cores": oracle.threads(),
                "kind": "oracle", "sample": f"{n_cpu} of the 36 layers x {B} one-token sequences, fp64 oracle "
-                                           f"({dt:.1f} s wall), scaled to the 36-layer stack"}
+                                           f"({dt:.1f} s wall), scaled to the 36-layer stack", **host_cpu()}
     if rank == 0:
         line = {"metric": DECODE_METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
                 "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
@@ -586,7 +608,7 @@ def main():
                           + (" [fp32 output]" if out_f32 else ""),
                 "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
                 "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
-                "vs_baseline": None if out_f32 else value / PAGES_TOKENS_PER_S, "dtype": "bf16" if args.fast else "f32",
+                "vs_baseline": None if out_f32 else value / PAGES_TOKENS_PER_S, "dtype": "bf16/f32-accum" if args.fast else "bf16x3-split/f32-accum",
                 "data": "synthetic",
                 "config": {"workload": WORKLOAD.replace("fp16 output", "fp32 output") if out_f32 else WORKLOAD,
                            "layers": LAYERS, "seq_len": T, "global_batch": world,

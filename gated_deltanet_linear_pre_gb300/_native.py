@@ -72,6 +72,10 @@ def lib():
                 getattr(L, name).argtypes = [D, _i32, _i32] + [_p] * 10 + [_sz, _p]
             L.gdn_scan_noalloc.restype = ctypes.c_int
             L.gdn_scan_noalloc.argtypes = [D, _i32, _i32] + [_p] * 9 + [_p]
+            L.gdn_scan_noalloc_check.restype = ctypes.c_int
+            L.gdn_scan_noalloc_check.argtypes = [_p]
+            L.gdn_last_async_error.restype = ctypes.c_int
+            L.gdn_last_async_error.argtypes = []
             L.gdn_post.restype = ctypes.c_int
             L.gdn_post.argtypes = [D, _i32, _p, _p, _p, _i32, _p, _p]
             L.gdn_layer_workspace_bytes.restype = _sz
@@ -260,6 +264,17 @@ def gdn_scan_check(workspace, stream=None):
     """Raise GdnError (GDN_ERR_TIMEOUT) if the last scan on this workspace reported an expired wait;
     synchronises the stream."""
     _check("gdn_scan_check", lib().gdn_scan_check(_ptr(workspace, "workspace", torch.uint8), _stream(stream)))
+
+
+def gdn_scan_noalloc_check(stream=None):
+    """As gdn_scan_check for the last gdn_scan_noalloc on the current device; synchronises the stream."""
+    _check("gdn_scan_noalloc_check", lib().gdn_scan_noalloc_check(_stream(stream)))
+
+
+def gdn_last_async_error():
+    """Raise GdnError (GDN_ERR_CUDA) if the library has seen a fault that left the CUDA context
+    unusable; never synchronises."""
+    _check("gdn_last_async_error", lib().gdn_last_async_error())
 
 
 def gdn_layer_check(d: gdn_dims, n_seq: int, total_tokens: int, workspace, stream=None):

@@ -1,6 +1,7 @@
 // gdn_api.cu -- the C ABI declared in include/gdn.h: host-side argument
 // validation, workspace carving and kernel launches.  No allocation, no
 // synchronisation.
+#include <atomic>
 #include <cmath>
 #include <cstdarg>
 #include <cstdio>
@@ -26,8 +27,40 @@ gdn_status fail(gdn_status s, const char* fmt, ...)
     return s;
 }
 
+// First CUDA error the library has seen that leaves the context unusable (a fault of an earlier
+// kernel, which every later launch and copy reports), kept for gdn_last_async_error; 0 = none yet.
+std::atomic<int> g_sticky_error{0};
+
+// the error codes CUDA documents as corrupting the context: once one is seen, every later call in
+// the process returns it, so it is kept rather than reported once
+bool context_fatal(cudaError_t e)
+{
+    switch (e) {
+    case cudaErrorIllegalAddress:
+    case cudaErrorLaunchFailure:
+    case cudaErrorIllegalInstruction:
+    case cudaErrorMisalignedAddress:
+    case cudaErrorInvalidAddressSpace:
+    case cudaErrorInvalidPc:
+    case cudaErrorHardwareStackError:
+    case cudaErrorLaunchTimeout:
+    case cudaErrorAssert:
+    case cudaErrorECCUncorrectable:
+        return true;
+    default:
+        return false;
+    }
+}
+
+void note_cuda_error(cudaError_t e)
+{
+    int none = 0;
+    if (context_fatal(e)) g_sticky_error.compare_exchange_strong(none, (int)e);
+}
+
 gdn_status cuda_fail(cudaError_t e, const char* what)
 {
+    note_cuda_error(e);
     return fail(GDN_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
 }
 
@@ -122,6 +155,16 @@ const char* gdn_status_string(gdn_status s)
 
 const char* gdn_last_error_string(void) { return g_last_error.c_str(); }
 
+gdn_status gdn_last_async_error(void)
+{
+    // what the runtime has already observed (peek: no synchronisation, nothing cleared)
+    note_cuda_error(cudaPeekAtLastError());
+    const int e = g_sticky_error.load();
+    if (e == 0) return GDN_OK;
+    return fail(GDN_ERR_CUDA, "an earlier kernel faulted and the CUDA context is unusable: %s",
+                cudaGetErrorString((cudaError_t)e));
+}
+
 }  // extern "C"
 
 namespace {
@@ -146,10 +189,21 @@ gdn_status prep_pre(const gdn_dims* dims, int32_t n_seq, int32_t T, const int32_
         {beta, tt * hv * 4, "beta"},
     };
     if ((st = check_bufs(bufs, sizeof bufs / sizeof bufs[0])) != GDN_OK) return st;
+    // hist_out may be hist_in itself (the history is then written by a trailing launch, after every
+    // read of the old history); any other overlap is rejected
+    const bool hist_in_place = hist_out == hist_in && bufs[3].bytes > 0;
     const Buf ins[] = {bufs[0], bufs[1], bufs[2], bufs[4], bufs[5], bufs[6], bufs[7]};
     const Buf outs[] = {bufs[3], bufs[8], bufs[9], bufs[10], bufs[11], bufs[12]};
-    if ((st = check_disjoint(outs, 6, ins, 7)) != GDN_OK) return st;
+    if (hist_in_place) {
+        const Buf ins_x[] = {bufs[0], bufs[1], bufs[4], bufs[5], bufs[6], bufs[7]};
+        if ((st = check_disjoint(outs, 6, ins_x, 6)) != GDN_OK) return st;
+        for (int i = 1; i < 6; ++i)
+            if (overlap(outs[i], bufs[2])) return fail(GDN_ERR_INVALID_ARG, "%s overlaps hist_in", outs[i].name);
+    } else if ((st = check_disjoint(outs, 6, ins, 7)) != GDN_OK) {
+        return st;
+    }
     p = gdn::PreParams{};
+    p.hist_in_place = hist_in_place ? 1 : 0;
     p.hk = dims->hk; p.hv = dims->hv; p.C = (int)C; p.T = T; p.n_seq = n_seq; p.eps = dims->eps;
     p.cu_seqlens = cu_seqlens;
     p.qkv = reinterpret_cast<const __half*>(qkv);

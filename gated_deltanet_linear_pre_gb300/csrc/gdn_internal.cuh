@@ -43,6 +43,7 @@ struct PreParams {
     // inside gdn_layer: q and k go straight into the scan's [K; Q] images (qn and kn unused); the
     // images of slot `slot`, key head j start at kq_images + (slot * hk + j) * kKqImageBytes
     unsigned char* kq_images;
+    int hist_in_place;  // hist_out == hist_in: the history is written by a second launch after the conv
 };
 
 struct ScanParams {

@@ -18,23 +18,42 @@ constexpr int kMaxDevices = 64;
 std::mutex g_setup_mutex;
 void* g_scratch_ptr[kMaxDevices] = {};
 
-// Device address of this device's scratch array, looked up once per device
-// with that device current.  In host code the array's name is only a
-// host-side handle; kernels must be given this address.
-gdn_status scratch_for_current_device(void** out)
+int current_device(gdn_status* st)
 {
     int dev = -1;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) {
         gdn::set_last_error(cudaGetErrorString(e));
-        return GDN_ERR_CUDA;
+        *st = GDN_ERR_CUDA;
+        return -1;
     }
     if (dev < 0 || dev >= kMaxDevices) {
         gdn::set_last_error("gdn_scan_noalloc: device ordinal beyond the supported 64");
-        return GDN_ERR_UNSUPPORTED;
+        *st = GDN_ERR_UNSUPPORTED;
+        return -1;
+    }
+    *st = GDN_OK;
+    return dev;
+}
+
+// Device address of this device's scratch array, with that device current.  In host code the
+// array's name is only a host-side handle; kernels must be given this address.  Looked up on
+// every call outside stream capture (after a device reset the module, and with it the array, is
+// loaded afresh); under capture the address of the last call outside capture is used, so the
+// first call on a device must come before any capture.
+gdn_status scratch_for_current_device(cudaStream_t stream, void** out)
+{
+    gdn_status st;
+    const int dev = current_device(&st);
+    if (st != GDN_OK) return st;
+    cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+    cudaError_t e = cudaStreamIsCapturing(stream, &cs);
+    if (e != cudaSuccess) {
+        gdn::set_last_error(cudaGetErrorString(e));
+        return GDN_ERR_CUDA;
     }
     std::lock_guard<std::mutex> lock(g_setup_mutex);
-    if (!g_scratch_ptr[dev]) {
+    if (cs == cudaStreamCaptureStatusNone) {
         void* ptr = nullptr;
         e = cudaGetSymbolAddress(&ptr, g_scan_scratch);
         if (e != cudaSuccess || !ptr) {
@@ -43,6 +62,9 @@ gdn_status scratch_for_current_device(void** out)
             return GDN_ERR_CUDA;
         }
         g_scratch_ptr[dev] = ptr;
+    } else if (!g_scratch_ptr[dev]) {
+        gdn::set_last_error("gdn_scan_noalloc: the first call on a device must come before any stream capture");
+        return GDN_ERR_INVALID_ARG;
     }
     *out = g_scratch_ptr[dev];
     return GDN_OK;
@@ -70,10 +92,27 @@ extern "C" gdn_status gdn_scan_noalloc(const gdn_dims* dims, int32_t n_seq, int3
         return GDN_ERR_UNSUPPORTED;
     }
     void* scratch = nullptr;
-    gdn_status st = scratch_for_current_device(&scratch);
+    gdn_status st = scratch_for_current_device(reinterpret_cast<cudaStream_t>(stream), &scratch);
     if (st != GDN_OK) return st;
     // the same validation and launches as gdn_scan; the scan clears the part of
     // its scratch that must start at zero on every call
     return gdn_scan(dims, n_seq, total_tokens, cu_seqlens, qn, kn, vc, glog, beta, S_in, S_out, o, scratch,
                     GDN_SCAN_NOALLOC_MAX_BYTES, stream);
+}
+
+extern "C" gdn_status gdn_scan_noalloc_check(struct CUstream_st* stream)
+{
+    gdn_status st;
+    const int dev = current_device(&st);
+    if (st != GDN_OK) return st;
+    void* scratch = nullptr;
+    {
+        std::lock_guard<std::mutex> lock(g_setup_mutex);
+        scratch = g_scratch_ptr[dev];
+    }
+    if (!scratch) {
+        gdn::set_last_error("gdn_scan_noalloc_check: gdn_scan_noalloc has not run on this device");
+        return GDN_ERR_INVALID_ARG;
+    }
+    return gdn_scan_check(scratch, stream);
 }

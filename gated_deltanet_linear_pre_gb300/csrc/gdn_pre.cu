@@ -304,7 +304,9 @@ pre_kernel(PreParams p, int n_slots, int head_groups, int n_conv_blocks)
         const int t = t_begin + lane;
         const float av = __half2float(p.a[(size_t)t * p.hv + vh]) + __ldg(p.dt_bias + vh);
         const float bv = __half2float(p.b[(size_t)t * p.hv + vh]);
-        const float sp = fmaxf(av, 0.0f) + __logf(1.0f + __expf(-fabsf(av)));  // softplus
+        // softplus as max(x, 0) + log1p(e^-|x|): for strongly negative x the sum 1 + e^-|x| would round
+        // most of e^-|x| away, and log1p keeps it (relative error of lam stays at the fp32 level)
+        const float sp = fmaxf(av, 0.0f) + log1pf(__expf(-fabsf(av)));
         p.glog[(size_t)t * p.hv + vh] = -__expf(__ldg(p.A_log + vh)) * sp;
         p.beta[(size_t)t * p.hv + vh] = __fdividef(1.0f, 1.0f + __expf(-bv));
     }
@@ -319,13 +321,19 @@ cudaError_t launch_pre(const PreParams& p, cudaStream_t stream)
     const int head_groups = (n_slots + kWarps - 1) / kWarps;
     const long long n_conv_blocks = n_tblocks * head_groups;
     const long long n_hist_blocks = ((long long)p.n_seq * p.C + kHistThreads - 1) / kHistThreads;
-    const long long blocks = n_conv_blocks + n_hist_blocks;
-    if (blocks == 0) return cudaSuccess;
-    if (blocks > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
-    return p.kq_images ? launch_k(pre_kernel<true>, dim3((unsigned)blocks), dim3(kThreads), 0, stream, true, p, n_slots,
-                                  head_groups, (int)n_conv_blocks)
-                       : launch_k(pre_kernel<false>, dim3((unsigned)blocks), dim3(kThreads), 0, stream, true, p, n_slots,
-                                  head_groups, (int)n_conv_blocks);
+    if (n_conv_blocks + n_hist_blocks > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
+    auto launch = [&](long long blocks, int conv_blocks) {
+        if (blocks == 0) return cudaSuccess;
+        return p.kq_images ? launch_k(pre_kernel<true>, dim3((unsigned)blocks), dim3(kThreads), 0, stream, true, p,
+                                      n_slots, head_groups, conv_blocks)
+                           : launch_k(pre_kernel<false>, dim3((unsigned)blocks), dim3(kThreads), 0, stream, true, p,
+                                      n_slots, head_groups, conv_blocks);
+    };
+    if (!p.hist_in_place) return launch(n_conv_blocks + n_hist_blocks, (int)n_conv_blocks);
+    // history in place: the conv blocks (the readers of the old history) first; the history blocks in a
+    // second launch, whose grid-dependency wait returns only once the first grid has completed
+    cudaError_t e = launch(n_conv_blocks, (int)n_conv_blocks);
+    return e != cudaSuccess ? e : launch(n_hist_blocks, 0);
 }
 
 }  // namespace gdn

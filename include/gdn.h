@@ -42,7 +42,8 @@
  *    launched and return a status with nothing enqueued.  A failed launch
  *    returns GDN_ERR_CUDA (the CUDA error string is kept for
  *    gdn_last_error_string).  Asynchronous faults surface at the caller's
- *    next synchronisation, as with any CUDA library.
+ *    next synchronisation, as with any CUDA library, and, without one, through
+ *    gdn_last_async_error once any CUDA call of the process has observed them.
  *  - Thread safety: calls may be made from several host threads on
  *    different streams; they share no mutable state except the last-error
  *    string, which is per host thread.
@@ -94,6 +95,19 @@ GDN_API const char* gdn_status_string(gdn_status s);
 GDN_API const char* gdn_last_error_string(void);
 
 /*
+ * gdn_last_async_error -- the sticky CUDA error: GDN_ERR_CUDA once the library
+ * has seen an error that leaves the CUDA context unusable (a kernel that
+ * faulted: illegal address or instruction, misaligned address, launch
+ * failure or timeout, device assert, uncorrectable ECC), else GDN_OK.  The
+ * error is seen either by one of the library's own calls (every later launch
+ * or copy in a faulted context returns it) or, at this call, through the
+ * CUDA runtime's last-error state.  Does not synchronise, enqueues nothing and
+ * clears nothing: once set it stays set for the life of the process, as the
+ * context's fault does.  The detail goes to gdn_last_error_string.
+ */
+GDN_API gdn_status gdn_last_async_error(void);
+
+/*
  * gdn_pre -- stage 1 ("Round 30 Track C Audit", section 1, gdn_pre: the
  * 4-tap conv loop, the history write at the last token, the per-key-head
  * q/k sum-of-squares reductions; "round 10 track b", variants: each conv
@@ -110,8 +124,11 @@ GDN_API const char* gdn_last_error_string(void);
  * Out: hist_out fp16 [n_seq][C][3]      last 3 inputs of each sequence
  *                                       (old history shifted in when the
  *                                       sequence is shorter than 3); bit
- *                                       copies, never rounded.  Must not
- *                                       overlap hist_in.
+ *                                       copies, never rounded.  May be the
+ *                                       same buffer as hist_in: the new
+ *                                       history is then written by a second
+ *                                       launch, after every read of the old
+ *                                       one.  Any other overlap is rejected.
  *      qn, kn   fp32 [T][hk][dk]        SiLU(conv) / sqrt(|.|^2 + eps)
  *      vc       fp32 [T][hv][dv]        SiLU(conv) of the v channels
  *      glog     fp32 [T][hv]            lam = log g (<= 0)
@@ -190,6 +207,10 @@ GDN_API gdn_status gdn_post(const gdn_dims* dims, int32_t total_tokens, const fl
  *   contents (the part that must start at zero is cleared by every call):
  *   calls whose work overlaps on the GPU -- different streams, or several
  *   host threads -- race on it.  Serialise them, e.g. on one stream.
+ * - The array's device address is looked up again on every call made outside
+ *   stream capture (so a device reset, after which the library's module is
+ *   loaded afresh, is picked up); under capture the address from the last
+ *   call outside capture is used.
  */
 #define GDN_SCAN_NOALLOC_MAX_BYTES ((size_t)64 << 20)
 GDN_API gdn_status gdn_scan_noalloc(const gdn_dims* dims, int32_t n_seq, int32_t total_tokens,
@@ -197,6 +218,16 @@ GDN_API gdn_status gdn_scan_noalloc(const gdn_dims* dims, int32_t n_seq, int32_t
                                     const float* vc, const float* glog, const float* beta,
                                     const float* S_in, float* S_out, float* o,
                                     struct CUstream_st* stream);
+
+/*
+ * gdn_scan_noalloc_check -- the failure report of the last gdn_scan_noalloc on
+ * the current device (as gdn_scan_check for an ordinary workspace: its
+ * record is the first word of the library's own scratch array, whose address
+ * the caller never holds).  Enqueues a 4-byte device-to-host copy on `stream`,
+ * SYNCHRONISES it and returns GDN_OK or GDN_ERR_TIMEOUT; GDN_ERR_INVALID_ARG
+ * if gdn_scan_noalloc has not run on this device yet.
+ */
+GDN_API gdn_status gdn_scan_noalloc_check(struct CUstream_st* stream);
 
 /* Workspace bytes gdn_layer needs: the stage tensors vc, glog, beta, o plus
  * the scan's own workspace, each 256-byte aligned (q and k go from the pre
@@ -207,9 +238,9 @@ GDN_API size_t gdn_layer_workspace_bytes(const gdn_dims* dims, int32_t n_seq, in
  * gdn_layer -- the whole prefill layer: gdn_pre, gdn_scan and gdn_post on
  * `stream`, the stage tensors kept in `workspace` (the pages time the three
  * stages back to back as one pre+scan+post total, "Round 30 Track C Audit",
- * section 2).  Arguments as in the three stage calls.  S_out may equal S_in;
- * hist_out must not overlap hist_in.  May be captured into a CUDA graph, as
- * gdn_scan.
+ * section 2).  Arguments as in the three stage calls.  S_out may equal S_in
+ * and hist_out may equal hist_in (partial overlaps are rejected).  May be
+ * captured into a CUDA graph, as gdn_scan.
  */
 GDN_API gdn_status gdn_layer(const gdn_dims* dims, int32_t n_seq, int32_t total_tokens,
                      const int32_t* cu_seqlens, const uint16_t* qkv, const float* conv_w,

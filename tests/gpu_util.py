@@ -25,6 +25,28 @@ def max_rel(x, ref) -> float:
     return float(err / den) if den > 0 else float(err)
 
 
+def max_rel_slices(x, ref, cu_seqlens=None, token_axis=0, head_axis=1):
+    """The same metric per (sequence, head) slice, the worst slice returned: each slice is held to its
+    own max |ref|, so a head or sequence with a small output or state is not judged against the
+    tensor's largest value.  With cu_seqlens the token axis is cut into sequences; without it the
+    token axis indexes sequences already (a state tensor [n_seq, hv, ...])."""
+    x = np.asarray(x, dtype=np.float64)
+    ref = np.asarray(ref, dtype=np.float64)
+    assert x.shape == ref.shape, (x.shape, ref.shape)
+    n = ref.shape[token_axis]
+    bounds = [(int(cu_seqlens[s]), int(cu_seqlens[s + 1])) for s in range(len(cu_seqlens) - 1)] \
+        if cu_seqlens is not None else [(i, i + 1) for i in range(n)]
+    worst = 0.0
+    for lo, hi in bounds:
+        if hi <= lo:
+            continue
+        xs = np.take(x, range(lo, hi), axis=token_axis)
+        rs = np.take(ref, range(lo, hi), axis=token_axis)
+        for h in range(ref.shape[head_axis]):
+            worst = max(worst, max_rel(np.take(xs, h, axis=head_axis), np.take(rs, h, axis=head_axis)))
+    return worst
+
+
 def dev(a, dtype=None):
     t = torch.from_numpy(np.ascontiguousarray(a)).cuda()
     return t if dtype is None else t.to(dtype)

@@ -28,7 +28,8 @@ def declared_symbols():
 def test_header_declares_the_boundary():
     syms = declared_symbols()
     for name in ("gdn_pre", "gdn_scan", "gdn_post", "gdn_layer", "gdn_step", "gdn_scan_workspace_bytes",
-                 "gdn_layer_workspace_bytes", "gdn_status_string", "gdn_last_error_string"):
+                 "gdn_layer_workspace_bytes", "gdn_status_string", "gdn_last_error_string",
+                 "gdn_last_async_error", "gdn_scan_noalloc_check"):
         assert name in syms
 
 
@@ -92,8 +93,10 @@ def test_pre_rejects_bad_arguments(L):
     assert _pre(L, N.dims(), qkv=None) == 1
     assert _pre(L, N.dims(), qkv=FAKE + 8) == 3
     assert _pre(L, N.dims(), cu=None) == 1
-    # outputs overlapping inputs or each other
-    assert _pre(L, N.dims(), hist_out=FAKE) == 1
+    # outputs overlapping inputs or each other (hist_out == hist_in exactly is allowed: the in-place
+    # history; a partial overlap is not)
+    assert _pre(L, N.dims(), hist_in=2 * FAKE, hist_out=2 * FAKE + 16) == 1
+    assert _pre(L, N.dims(), hist_in=2 * FAKE, hist_out=2 * FAKE, vc=2 * FAKE + 32) == 1
     assert _pre(L, N.dims(), kn=3 * FAKE) == 1
     msg = L.gdn_last_error_string().decode()
     assert "overlaps" in msg

@@ -55,6 +55,8 @@ def test_scan_check_reports_ok_after_normal_runs():
     gdn.gdn_layer(d, x["cu"], T, x["qkv"], x["conv_w"], x["hist"], torch.empty_like(x["hist"]), x["a"], x["b"],
                   x["z"], x["A_log"], x["dt_bias"], x["gamma"], x["S0"], torch.empty_like(x["S0"]), False, y, lws)
     gdn.gdn_layer_check(d, inp.n_seq, T, lws)
+    # and no fault that would leave the context unusable was seen (a non-synchronising check)
+    gdn.gdn_last_async_error()
 
 
 def test_expired_wait_is_reported_and_the_context_stays_usable():

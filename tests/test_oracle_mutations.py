@@ -23,6 +23,8 @@ MUTATIONS = [
     ("no_q_scale", "const double qi = qt[i] * qscale;", "const double qi = qt[i];"),
     ("key_head_modulo", "const int64_t j = h / group;", "const int64_t j = h % hk;"),
     ("rms_sum_not_mean", "double inv = 1.0 / sqrt(ss / (double)dv + eps);", "double inv = 1.0 / sqrt(ss + eps);"),
+    ("post_eps_outside_sqrt", "double inv = 1.0 / sqrt(ss / (double)dv + eps);",
+     "double inv = 1.0 / (sqrt(ss / (double)dv) + eps);"),
     ("post_sigmoid_gate", "gamma[i] * gdn_oracle_silu_scalar(zrow[i]);", "gamma[i] * gdn_oracle_sigmoid(zrow[i]);"),
 ]
 

@@ -305,6 +305,10 @@ def test_post_hand_worked():
     z = ex["z_is_large"]
     y2 = oracle.post([ex["o2"]], [[z] * 4], ex["gamma2"], ex["eps"])
     np.testing.assert_allclose(y2[0] / z, ex["y2_over_z"], rtol=1e-15)
+    # eps comparable to mean(o^2): it sits inside the square root, added to the mean
+    z3 = ex["z3_is_large"]
+    y3 = oracle.post([ex["o3"]], [[z3] * 4], ex["gamma3"], ex["eps3"])
+    np.testing.assert_allclose(y3[0] / z3, ex["y3_over_z"], rtol=1e-12)
 
 
 def test_post_scale_invariance_and_rms():

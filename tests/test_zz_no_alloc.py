@@ -55,6 +55,7 @@ def test_noalloc_scan_matches_workspace_scan_twice():
         o = torch.full_like(v, float("nan"))
         S_out = torch.full_like(S_in, float("nan"))
         gdn.gdn_scan_noalloc(d, cu, T, q, k, v, lam, beta, S_in, S_out, o)
+        gdn.gdn_scan_noalloc_check()  # no bounded wait of the scan ran out (synchronises)
         torch.cuda.synchronize()
         assert u.max_rel(o.cpu().numpy(), o_ref) <= u.TOL_F32
         assert u.max_rel(S_out.cpu().numpy(), S_ref) <= u.TOL_F32
