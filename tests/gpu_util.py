@@ -12,6 +12,12 @@ import gated_deltanet_linear_pre_gb300 as gdn
 TOL_F16 = 2e-3      # fp16 outputs
 TOL_F32 = 1e-4      # fp32 outputs and the final fp32 state
 TOL_STAGE = 1e-5    # fp32 stage tensors of gdn_pre (no accumulation involved)
+# The same metric per (sequence, head) slice is stricter than the contract's per-tensor one: the split
+# bf16 products' absolute error scales with their operands, not with the slice's own largest output,
+# so a head whose outputs are small next to the tensor's largest value shows a larger ratio.  Slices
+# are held to 5x the per-tensor bars.
+TOL_SLICE_F32 = 5e-4
+TOL_SLICE_F16 = 1e-2
 
 
 def max_rel(x, ref) -> float:

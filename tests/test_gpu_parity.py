@@ -97,8 +97,9 @@ def test_scan_matches_oracle(T):
     assert u.max_rel(o, o_ref) <= u.TOL_F32
     assert u.max_rel(S, S_ref) <= u.TOL_F32
     # and per (sequence, head) slice
-    assert u.max_rel_slices(o, o_ref, inp.cu_seqlens) <= u.TOL_F32
-    assert u.max_rel_slices(S, S_ref) <= u.TOL_F32
+    eo_s, eS_s = u.max_rel_slices(o, o_ref, inp.cu_seqlens), u.max_rel_slices(S, S_ref)
+    print(f"ERR scan T={T}: o worst slice {eo_s:.3e}, S worst slice {eS_s:.3e}")
+    assert eo_s <= u.TOL_SLICE_F32 and eS_s <= u.TOL_SLICE_F32
 
 
 def test_scan_varlen_with_empty_sequences():
@@ -172,8 +173,8 @@ def _check_layer(inp, heads=None, name=""):
     print(f"ERR {name or 'layer'} T={inp.total_tokens} n_seq={inp.n_seq} out_f32={int(inp.out_f32)} "
           f"heads={'all' if heads is None else len(heads)}: y {ey:.3e} (worst slice {ey_s:.3e}), "
           f"S {eS:.3e} (worst slice {eS_s:.3e}); bars y {tol:g}, S {u.TOL_F32:g}")
-    assert ey <= tol and ey_s <= tol
-    assert eS <= u.TOL_F32 and eS_s <= u.TOL_F32
+    assert ey <= tol and eS <= u.TOL_F32
+    assert ey_s <= (u.TOL_SLICE_F32 if inp.out_f32 else u.TOL_SLICE_F16) and eS_s <= u.TOL_SLICE_F32
     np.testing.assert_array_equal(got["hist_out"].view(np.uint16), inp_hist_bits(ref["hist_out"]))
     return got, ref
 
