@@ -91,6 +91,8 @@ def lib():
             L.gdn_scan_selftest_timeout.argtypes = [D, _i32, _i32] + [_p] * 10 + [_sz, _p]
             L.gdn_scan_selftest_one_taker.restype = ctypes.c_int
             L.gdn_scan_selftest_one_taker.argtypes = [D, _i32, _i32] + [_p] * 10 + [_sz, _p]
+            L.gdn_scan_selftest_withhold_flag.restype = ctypes.c_int
+            L.gdn_scan_selftest_withhold_flag.argtypes = [D, _i32, _i32] + [_p] * 10 + [_sz, _p]
             L.gdn_step.restype = ctypes.c_int
             L.gdn_step.argtypes = [D, _i32] + [_p] * 12 + [_i32, _p, _p]
             _lib = L
@@ -313,3 +315,19 @@ def gdn_scan_selftest_one_taker(d: gdn_dims, cu_seqlens, total_tokens, qn, kn, v
         _ptr(workspace, "workspace", torch.uint8), workspace.numel() if workspace is not None else 0,
         _stream(stream))
     _check("gdn_scan_selftest_one_taker", st)
+
+
+def gdn_scan_selftest_withhold_flag(d: gdn_dims, cu_seqlens, total_tokens, qn, kn, vc, glog, beta, S_in, S_out, o,
+                                    workspace, stream=None):
+    """Test hook of the wait across kernels: gdn_scan with one prep ready flag left unset (outputs invalid)."""
+    n_seq, T = _batch(cu_seqlens, total_tokens)
+    hk, hv, dk, dv = d.hk, d.hv, d.dk, d.dv
+    f32 = torch.float32
+    st = lib().gdn_scan_selftest_withhold_flag(
+        ctypes.byref(d), n_seq, T, _ptr(cu_seqlens, "cu_seqlens", torch.int32), _ptr(qn, "qn", f32, (T, hk, dk)),
+        _ptr(kn, "kn", f32, (T, hk, dk)), _ptr(vc, "vc", f32, (T, hv, dv)), _ptr(glog, "glog", f32, (T, hv)),
+        _ptr(beta, "beta", f32, (T, hv)), _ptr(S_in, "S_in", f32, (n_seq, hv, dk, dv)),
+        _ptr(S_out, "S_out", f32, (n_seq, hv, dk, dv)), _ptr(o, "o", f32, (T, hv, dv)),
+        _ptr(workspace, "workspace", torch.uint8), workspace.numel() if workspace is not None else 0,
+        _stream(stream))
+    _check("gdn_scan_selftest_withhold_flag", st)

@@ -9,6 +9,7 @@
 #include <string>
 
 #include "gdn.h"
+#include "gdn_testing.h"
 #include "gdn_internal.cuh"
 
 namespace {
@@ -533,6 +534,19 @@ gdn_status gdn_scan_selftest_timeout(const gdn_dims* dims, int32_t n_seq, int32_
                               workspace_bytes, p);
     if (st != GDN_OK) return st;
     p.withhold_first_copy = 1;
+    return run_scan(p, stream);
+}
+
+gdn_status gdn_scan_selftest_withhold_flag(const gdn_dims* dims, int32_t n_seq, int32_t T, const int32_t* cu_seqlens,
+                                           const float* qn, const float* kn, const float* vc, const float* glog,
+                                           const float* beta, const float* S_in, float* S_out, float* o,
+                                           void* workspace, size_t workspace_bytes, struct CUstream_st* stream)
+{
+    gdn::ScanParams p;
+    gdn_status st = prep_scan(dims, n_seq, T, cu_seqlens, qn, kn, vc, glog, beta, S_in, S_out, o, workspace,
+                              workspace_bytes, p);
+    if (st != GDN_OK) return st;
+    p.withhold_flag = 1;
     return run_scan(p, stream);
 }
 

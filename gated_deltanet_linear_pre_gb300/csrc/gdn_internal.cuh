@@ -61,6 +61,7 @@ struct ScanParams {
     size_t workspace_bytes;
     int withhold_first_copy;  // failure-report self-test only (gdn_scan_selftest_timeout)
     int prep_no_keepers;      // prep fallback self-test only (gdn_scan_selftest_one_taker)
+    int withhold_flag;        // cross-kernel wait self-test only (gdn_scan_selftest_withhold_flag)
     int fast;                 // one-pass bf16 products (gdn_scan_fast / gdn_layer_fast)
     int prep_sms, prep_keep;  // SMs of the device; SMs whose prep CTAs stay after round one (set by launch_scan)
     int kq_written;           // the pre kernel wrote the [K; Q] images (qn and kn unused; gdn_layer)

@@ -221,6 +221,13 @@ __device__ __forceinline__ unsigned long long* ready_flag(const ScanParams& p, s
            slot * p.hv + h;
 }
 
+// the ready flag that the failure-report self-test of the cross-kernel wait leaves unset: chunk slot 1,
+// value head 0 (the chain's copy warp for that head then waits for it until its bound runs out)
+__device__ __forceinline__ bool withheld(const ScanParams& p, int slot, int h)
+{
+    return p.withhold_flag && slot == 1 && h == 0;
+}
+
 __device__ __forceinline__ void flag_publish(unsigned long long* f, unsigned long long v)
 {
     asm volatile("st.release.gpu.global.u64 [%0], %1;" ::"l"(f), "l"(v) : "memory");
@@ -782,7 +789,7 @@ __global__ void __launch_bounds__(kPrepThreads, 4) scan_prep_kernel(ScanParams p
             // this task's loads, in a warp that only loads here
             if (tid == kPrepThreads - 32 && pend_slot >= 0) {
                 __threadfence();
-                flag_publish(ready_flag(p, (size_t)pend_slot, pend_h), 1ull);
+                if (!withheld(p, pend_slot, pend_h)) flag_publish(ready_flag(p, (size_t)pend_slot, pend_h), 1ull);
             }
             pend_slot = -1;
             __syncthreads();
@@ -1002,7 +1009,7 @@ __global__ void __launch_bounds__(kPrepThreads, 4) scan_prep_kernel(ScanParams p
                 pend_h = h;
             } else if (tid == 0) {
                 __threadfence();
-                flag_publish(ready_flag(p, slot, h), 1ull);
+                if (!withheld(p, slot, h)) flag_publish(ready_flag(p, slot, h), 1ull);
             }
         }  // used slot
         // thread 0 fetches the next task (after round one, counted for the fallback above)
@@ -1018,7 +1025,7 @@ __global__ void __launch_bounds__(kPrepThreads, 4) scan_prep_kernel(ScanParams p
 
     if (tid == kPrepThreads - 32 && pend_slot >= 0) {  // the last task's flag
         __threadfence();
-        flag_publish(ready_flag(p, (size_t)pend_slot, pend_h), 1ull);
+        if (!withheld(p, pend_slot, pend_h)) flag_publish(ready_flag(p, (size_t)pend_slot, pend_h), 1ull);
     }
     umma::fence_before_sync();
     __syncthreads();

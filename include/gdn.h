@@ -289,34 +289,6 @@ GDN_API gdn_status gdn_layer_check(const gdn_dims* dims, int32_t n_seq, int32_t 
                                    const void* workspace, struct CUstream_st* stream);
 
 /*
- * gdn_scan_selftest_timeout -- test hook of the failure report, not a
- * computation: runs gdn_scan with the recurrence kernel's first operand copy
- * withheld, so that a bounded wait in every CTA of that kernel expires (no
- * fault, no trap, no unbounded wait).  Arguments as for gdn_scan; the
- * outputs are invalid and gdn_scan_check on the workspace returns
- * GDN_ERR_TIMEOUT.  Takes about two seconds.
- */
-GDN_API gdn_status gdn_scan_selftest_timeout(const gdn_dims* dims, int32_t n_seq, int32_t total_tokens,
-                                             const int32_t* cu_seqlens, const float* qn, const float* kn,
-                                             const float* vc, const float* glog, const float* beta,
-                                             const float* S_in, float* S_out, float* o, void* workspace,
-                                             size_t workspace_bytes, struct CUstream_st* stream);
-
-/*
- * gdn_scan_selftest_one_taker -- test hook of the prep kernel's progress
- * guarantee: runs gdn_scan with no SM chosen to keep taking prep tasks after
- * the first round, so the one CTA that the fallback keeps (the last to finish
- * round one) takes every remaining task alone.  Arguments and results as for
- * gdn_scan (bit for bit: each task computes the same values wherever it runs);
- * only slower.
- */
-GDN_API gdn_status gdn_scan_selftest_one_taker(const gdn_dims* dims, int32_t n_seq, int32_t total_tokens,
-                                               const int32_t* cu_seqlens, const float* qn, const float* kn,
-                                               const float* vc, const float* glog, const float* beta,
-                                               const float* S_in, float* S_out, float* o, void* workspace,
-                                               size_t workspace_bytes, struct CUstream_st* stream);
-
-/*
  * gdn_step -- one decode step: a single new token for each of n_seq
  * sequences through the whole layer (pre, the recurrence for that token, and
  * post), fused into one launch.  Per token it computes exactly what gdn_layer

@@ -10,6 +10,7 @@ import pytest
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 HEADER = os.path.join(ROOT, "include", "gdn.h")
+TESTING_HEADER = os.path.join(ROOT, "include", "gdn_testing.h")
 
 
 @pytest.fixture(scope="module")
@@ -20,9 +21,16 @@ def L():
     return _native.lib()
 
 
-def declared_symbols():
-    text = open(HEADER).read()
+def declared_symbols(path=HEADER):
+    text = open(path).read()
     return sorted(set(re.findall(r"GDN_API\s+[\w\s\*]+?\b(gdn_\w+)\s*\(", text)))
+
+
+def test_hooks_stay_out_of_the_product_header():
+    # the self-test entry points are declared in gdn_testing.h only
+    assert not [s for s in declared_symbols() if "selftest" in s]
+    assert set(declared_symbols(TESTING_HEADER)) == {"gdn_scan_selftest_timeout", "gdn_scan_selftest_one_taker",
+                                                     "gdn_scan_selftest_withhold_flag"}
 
 
 def test_header_declares_the_boundary():
@@ -38,10 +46,11 @@ def test_library_exports_every_declared_symbol(L):
     out = subprocess.run(["nm", "-D", "--defined-only", build.LIB], capture_output=True, text=True,
                          check=True).stdout
     exported = set(re.findall(r"\bT\s+(gdn_\w+)", out))
-    assert set(declared_symbols()) <= exported
-    # nothing but the ABI is exported under the gdn_ prefix
-    assert exported == set(declared_symbols())
-    for name in declared_symbols():
+    declared = set(declared_symbols()) | set(declared_symbols(TESTING_HEADER))
+    assert declared <= exported
+    # nothing but the ABI and its declared test hooks is exported under the gdn_ prefix
+    assert exported == declared
+    for name in declared:
         assert hasattr(L, name)
 
 
@@ -53,7 +62,7 @@ def test_status_strings(L):
 
 def test_header_compiles_as_c(tmp_path):
     src = tmp_path / "t.c"
-    src.write_text('#include "gdn.h"\nint main(void){ gdn_dims d = {16,48,128,128,1e-6f};'
+    src.write_text('#include "gdn.h"\n#include "gdn_testing.h"\nint main(void){ gdn_dims d = {16,48,128,128,1e-6f};'
                    ' return (int)gdn_layer_workspace_bytes(&d, 1, 0) & 0; }\n')
     subprocess.run(["gcc", "-std=c99", "-Wall", "-Werror", "-c", "-I", os.path.join(ROOT, "include"), str(src),
                     "-o", str(tmp_path / "t.o")], check=True)

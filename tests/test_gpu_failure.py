@@ -78,6 +78,28 @@ def test_expired_wait_is_reported_and_the_context_stays_usable():
     assert u.max_rel(S_out.cpu().numpy(), ref["S_out"]) <= u.TOL_F32
 
 
+def test_expired_wait_across_kernels_is_reported():
+    """The recurrence kernel waits, bounded, on the prep kernel's per-(chunk, value head) ready flags.
+    With one flag left unset (chunk slot 1, value head 0) that wait runs out in the CTAs of head 0:
+    the check reports GDN_ERR_TIMEOUT, and the same context then computes a correct scan."""
+    import gpu_util as u
+    import gated_deltanet_linear_pre_gb300 as gdn
+    inp = gin.make_layer(93, [200], hist_nonzero=True, S0_std=0.02)
+    ref, d, T, a, ws = _scan_args(inp)
+    o = torch.empty((T, d.hv, d.dv), device="cuda")
+    S_out = torch.empty_like(a["S_in"])
+    gdn.gdn_scan_selftest_withhold_flag(d, a["cu"], T, a["q"], a["k"], a["v"], a["lam"], a["beta"], a["S_in"],
+                                        S_out, o, ws)
+    with pytest.raises(gdn.GdnError) as ei:
+        gdn.gdn_scan_check(ws)
+    assert ei.value.status == 6
+    gdn.gdn_last_async_error()  # an expired wait is reported, not a fault: the context is intact
+    gdn.gdn_scan(d, a["cu"], T, a["q"], a["k"], a["v"], a["lam"], a["beta"], a["S_in"], S_out, o, ws)
+    gdn.gdn_scan_check(ws)
+    assert u.max_rel(o.cpu().numpy(), ref["o"]) <= u.TOL_F32
+    assert u.max_rel(S_out.cpu().numpy(), ref["S_out"]) <= u.TOL_F32
+
+
 @pytest.mark.parametrize("lens", [[2048], [1000, 700, 350]])
 def test_prep_fallback_alone_gives_the_same_scan(lens):
     """With no SM kept for prep after its first round, the one CTA the fallback keeps takes every
