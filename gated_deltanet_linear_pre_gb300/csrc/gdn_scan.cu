@@ -661,24 +661,29 @@ constexpr int kRound1PerSm = 1;
 constexpr int kDeferFlagsAbove = 64;
 constexpr int kRound1PerSmFast = 3;
 
+constexpr int kTS = 36;  // fp32 row stride of the 32x32 blocks of A and T (16-byte rows, no bank conflicts)
+
 struct __align__(1024) PrepSmem {
-    uint16_t ap[2][64 * 64];   // P (K-major, 64 rows); an M = 128 descriptor reads its rows 64-127 from
-    union {                    //   the next 16 KB (here), whose products are never read
-        float A[64 * 68];      // fp32 A (rows padded to 68 floats), until the solve is done
-        uint16_t bt[2][64 * 64];  // then T split (MN-major B tile)
+    uint16_t ap[2][128 * 64];  // [A; P] split (K-major, 128 rows x 64; hi plane, lo plane); once its
+                               // product is done, the operands of the correction product
+    union {
+        float A[2][32 * kTS];        // fp32 diagonal 32x32 blocks of A, for the substitution steps
+        uint16_t tb[2][2][32 * 32];  // then T1 and T2 split, MN-major B tiles: [block][hi / lo]
     } u;
-    float T[64 * 68];          // fp32 T
-    float W[32 * 32];          // off-diagonal block products of the solve
+    float T[2][32 * kTS];      // fp32 T1, T2 (the inverses of A's diagonal 32x32 blocks plus I)
+    float W[2 * 16 * 16];      // 16x16 block products of the substitution
     float G[64], beta[64];
     uint32_t tmem_base;
     int abort_flag;
     uint32_t next[2];  // the next task, broadcast from thread 0 (alternating slots)
     uint64_t mbar;
 };
-// operand tiles (tensor-core descriptors, 16-byte vector accesses) on 16-byte boundaries
+// operand tiles (tensor-core descriptors, 16-byte vector accesses) on 16-byte boundaries; four
+// CTAs fit an SM
 static_assert(offsetof(PrepSmem, ap) % 16 == 0 && offsetof(PrepSmem, u) % 16 == 0 && offsetof(PrepSmem, T) % 16 == 0 &&
                   offsetof(PrepSmem, W) % 16 == 0 && offsetof(PrepSmem, mbar) % 8 == 0,
               "prep shared-memory alignment");
+static_assert(4 * (sizeof(PrepSmem) + 1024) <= 232448, "four prep CTAs per SM");
 
 __global__ void __launch_bounds__(kPrepThreads, 4) scan_prep_kernel(ScanParams p)
 {
@@ -689,10 +694,9 @@ __global__ void __launch_bounds__(kPrepThreads, 4) scan_prep_kernel(ScanParams p
     uint32_t* err = reinterpret_cast<uint32_t*>(p.workspace);
     pdl_launch_dependents();
     pdl_wait();
-    constexpr int ST = 68;  // fp32 row stride of A and T
     const float qscale = rsqrtf((float)kHeadDim);
 
-    if (warp == 0) umma::tmem_alloc(&sm.tmem_base, 64);
+    if (warp == 0) umma::tmem_alloc(&sm.tmem_base, 128);  // [A; P] Tb in columns 0-63, the correction in 64-95
     if (tid == 0) {
         umma::mbar_init(&sm.mbar, 1);
         sm.abort_flag = 0;
@@ -796,75 +800,74 @@ __global__ void __launch_bounds__(kPrepThreads, 4) scan_prep_kernel(ScanParams p
             umma::fence_after_sync();
             const uint32_t tmem = sm.tmem_base;
             const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
-            const uint32_t a_p[2] = {umma::smem_u32(sm.ap[0]), umma::smem_u32(sm.ap[1])};
-            const uint32_t b_t[2] = {umma::smem_u32(sm.u.bt[0]), umma::smem_u32(sm.u.bt[1])};
-            float* A = sm.u.A;
-            float* Tm = sm.T;
+            constexpr uint32_t kIdN32 = umma::idesc_bf16(128, 32, false, true);  // M = 128, N = 32, B MN-major
 
             {
-                // A (fp32, rows L < 64) and P (split, rows L - 64 for L >= 64), columns of wg
+                // A (rows i = L < 64) and P (rows i = L - 64), columns [cb, cb + 32): A's diagonal 32x32
+                // blocks in fp32 for the substitution steps, its lower-left block A21 and P split into the
+                // [A; P] tile (the tensor core's A operand; of its rows 0-63 only A21 reaches a product
+                // that is read, so the other blocks are not written).  P is zero above its diagonal.
                 {
                     const int i = L & 63, cb = 32 * wg;
+                    const bool is_a = L < 64;
+                    const bool diag_blk = is_a && (i >> 5) == wg;
+                    const bool to_tile = is_a ? (wg == 0 && i >= 32) : true;
                     const float Gi = sm.G[i];
                     const float4* G4 = reinterpret_cast<const float4*>(sm.G + cb);
-                    // (a warp's 32 rows lie in one half, so for rows < 32 the columns of wg = 1 are all above
-                    // the diagonal: A's block there is never read, P's is zero)
-                    if (L < 64) {
-                        const float bi = sm.beta[i];
-                        if (cb <= i)
-#pragma unroll
-                        for (int q = 0; q < 8; ++q) {
-                            const float4 g = G4[q];
-                            const float gg[4] = {g.x, g.y, g.z, g.w};
-                            float a[4];
-#pragma unroll
-                            for (int e = 0; e < 4; ++e) {
-                                const int jj = cb + 4 * q + e;
-                                a[e] = jj < i ? bi * __expf(Gi - gg[e]) * d[4 * q + e] : 0.0f;
-                            }
-                            *reinterpret_cast<float4*>(&A[i * ST + cb + 4 * q]) = make_float4(a[0], a[1], a[2], a[3]);
-                        }
-                    } else if (cb > i) {
+                    const int row = is_a ? i : 64 + i;
+                    if (!is_a && cb > i) {
 #pragma unroll
                         for (int q = 0; q < 4; ++q) {
-                            *reinterpret_cast<uint4*>(&sm.ap[0][kmaj(i, cb + 8 * q, 64)]) = make_uint4(0u, 0u, 0u, 0u);
-                            *reinterpret_cast<uint4*>(&sm.ap[1][kmaj(i, cb + 8 * q, 64)]) = make_uint4(0u, 0u, 0u, 0u);
+                            *reinterpret_cast<uint4*>(&sm.ap[0][kmaj(row, cb + 8 * q, 64)]) = make_uint4(0u, 0u, 0u, 0u);
+                            *reinterpret_cast<uint4*>(&sm.ap[1][kmaj(row, cb + 8 * q, 64)]) = make_uint4(0u, 0u, 0u, 0u);
                         }
-                    } else {
+                    } else if (diag_blk || to_tile) {
+                        // A: beta_i e^{G_i - G_j} (k_i . k_j) for j < i;  P: e^{G_i - G_j} (q_i . k_j) / sqrt(dk) for j <= i
+                        const float f = is_a ? sm.beta[i] : qscale;
+                        float* a32 = sm.u.A[wg] + (i & 31) * kTS;
 #pragma unroll
                         for (int q = 0; q < 4; ++q) {
                             const float4 ga = G4[2 * q], gb = G4[2 * q + 1];
                             const float gg[8] = {ga.x, ga.y, ga.z, ga.w, gb.x, gb.y, gb.z, gb.w};
-                            float pr[8];
+                            float x[8];
 #pragma unroll
                             for (int e = 0; e < 8; ++e) {
                                 const int jj = cb + 8 * q + e;
-                                pr[e] = jj <= i ? __expf(Gi - gg[e]) * d[8 * q + e] * qscale : 0.0f;
+                                x[e] = (is_a ? jj < i : jj <= i) ? f * __expf(Gi - gg[e]) * d[8 * q + e] : 0.0f;
                             }
-                            store_split8(&sm.ap[0][kmaj(i, cb + 8 * q, 64)], &sm.ap[1][kmaj(i, cb + 8 * q, 64)], pr);
+                            if (to_tile)
+                                store_split8(&sm.ap[0][kmaj(row, cb + 8 * q, 64)], &sm.ap[1][kmaj(row, cb + 8 * q, 64)], x);
+                            else {
+                                *reinterpret_cast<float4*>(a32 + 8 * q) = make_float4(x[0], x[1], x[2], x[3]);
+                                *reinterpret_cast<float4*>(a32 + 8 * q + 4) = make_float4(x[4], x[5], x[6], x[7]);
+                            }
                         }
                     }
                 }
-                // A's writers (warps 0, 1, 4, 5) meet before the diagonal solve (warps 0, 1); the P warps
-                // join at the barrier after it
+                // the writers of A's diagonal blocks (warps 0 and 5) meet the substitution warps (0, 1)
                 if (L < 64) asm volatile("bar.sync 1, 128;" ::: "memory");
 
-                // T = (I + A)^-1 (A strictly lower), recursively by halves: T = [[T1, 0], [-T2 A21 T1, T2]].
+                // T = (I + A)^-1 (A strictly lower), by halves: with T1, T2 the inverses of the diagonal
+                // 32-blocks, T = [[T1, 0], [T21, T2]], T21 = -T2 A21 T1.
                 // (1) the four 16x16 diagonal blocks by forward substitution (thread (b, c): column c;
                 //     col[r] = [r == c] - sum_{m<r} A[r][m] col[m], the entries above c come out zero);
-                // (2) the two 32x32 halves: T_(b,b-1) = -T_(b,b) A_(b,b-1) T_(b-1,b-1) for b = 1, 3;
-                // (3) the 32x32 off-diagonal block: T21 = -T2 (A21 T1).
-                // Only the block lower triangle of T is written; readers treat the rest as zero.
+                // (2) T1 and T2: their lower-left 16x16 blocks, -T_(b,b) A_(b,b-1) T_(b-1,b-1) (CUDA cores);
+                // (3) on the tensor core, with Tb = diag(T1, T2) and [T; P T] = [Tb; P Tb] [[I, 0], [-W, I]],
+                //     W = A21 T1: one product [A; P] Tb gives W (rows 32-63, columns 0-31 of A Tb) and
+                //     P Tb, a second C = [Tb; P Tb][:, 32:64] W gives the correction of columns 0-31:
+                //     T21 = -C (rows 32-63), (P T)[:, 0:32] = (P Tb)[:, 0:32] - C (rows 64-127).
+                // Only the block lower triangle of T1 and T2 is written; readers treat the rest as zero.
                 {
                     if (tid < 64) {
-                        const int b = tid >> 4, c = tid & 15, o = 16 * b;
+                        const int b = tid >> 4, c = tid & 15, blk = b >> 1, o = 16 * (b & 1);
+                        const float* Ab = sm.u.A[blk];
                         float col[16];
 #pragma unroll
                         for (int r = 0; r < 16; ++r) {
                             float acc = (r == c) ? 1.0f : 0.0f;
 #pragma unroll
                             for (int m4 = 0; m4 < r; m4 += 4) {
-                                const float4 a4 = *reinterpret_cast<const float4*>(&A[(o + r) * ST + o + m4]);
+                                const float4 a4 = *reinterpret_cast<const float4*>(&Ab[(o + r) * kTS + o + m4]);
                                 if (m4 + 0 < r) acc = fmaf(-a4.x, col[m4 + 0], acc);
                                 if (m4 + 1 < r) acc = fmaf(-a4.y, col[m4 + 1], acc);
                                 if (m4 + 2 < r) acc = fmaf(-a4.z, col[m4 + 2], acc);
@@ -873,17 +876,18 @@ __global__ void __launch_bounds__(kPrepThreads, 4) scan_prep_kernel(ScanParams p
                             col[r] = acc;
                         }
 #pragma unroll
-                        for (int r = 0; r < 16; ++r) Tm[(o + r) * ST + o + c] = col[r];
+                        for (int r = 0; r < 16; ++r) sm.T[blk][(o + r) * kTS + o + c] = col[r];
                     }
                     __syncthreads();
-                    {   // (2) pairs b = 1 (rows 16-31 x cols 0-15) and b = 3 (rows 48-63 x cols 32-47)
+                    {   // (2) the lower-left 16x16 block of T1 (pr = 0) and of T2 (pr = 1)
                         const int pr = tid >> 7, r = (tid >> 3) & 15, c2 = 2 * (tid & 7);
-                        const int ro = 32 * pr + 16, co = 32 * pr;  // block (b, b-1) origin
+                        const float* Ab = sm.u.A[pr];
+                        float* Tb = sm.T[pr];
                         float w0 = 0.f, w1 = 0.f;
 #pragma unroll
                         for (int m = 0; m < 16; ++m) {
-                            const float a = A[(ro + r) * ST + co + m];
-                            const float2 t2 = *reinterpret_cast<const float2*>(&Tm[(co + m) * ST + co + c2]);
+                            const float a = Ab[(16 + r) * kTS + m];
+                            const float2 t2 = *reinterpret_cast<const float2*>(&Tb[m * kTS + c2]);
                             w0 = fmaf(a, t2.x, w0);
                             w1 = fmaf(a, t2.y, w1);
                         }
@@ -892,59 +896,28 @@ __global__ void __launch_bounds__(kPrepThreads, 4) scan_prep_kernel(ScanParams p
                         float t0 = 0.f, t1 = 0.f;
 #pragma unroll
                         for (int m = 0; m < 16; ++m) {
-                            const float a = Tm[(ro + r) * ST + ro + m];
+                            const float a = Tb[(16 + r) * kTS + 16 + m];
                             const float2 w2 = *reinterpret_cast<const float2*>(&sm.W[pr * 256 + m * 16 + c2]);
                             t0 = fmaf(a, w2.x, t0);
                             t1 = fmaf(a, w2.y, t1);
                         }
-                        *reinterpret_cast<float2*>(&Tm[(ro + r) * ST + co + c2]) = make_float2(-t0, -t1);
+                        *reinterpret_cast<float2*>(&Tb[(16 + r) * kTS + c2]) = make_float2(-t0, -t1);
                     }
                     __syncthreads();
-                    {   // (3) rows 32-63 x cols 0-31; T1 and T2 are block lower triangular.  Both loops are
-                        // fully unrolled; the structurally zero 16-wide blocks (never written, so they may
-                        // hold any bits) are selected away, not multiplied, so every load is in flight at once
-                        const int r = tid >> 3, c4 = 4 * (tid & 7);
-                        const bool hi_c = (c4 >> 4) != 0;  // T1[m][c] for m < 16 is zero when c >= 16
-                        const float4 z4 = make_float4(0.f, 0.f, 0.f, 0.f);
-                        float acc[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-                        for (int m = 0; m < 32; ++m) {
-                            const float a = A[(32 + r) * ST + m];
-                            const float4 t4l = *reinterpret_cast<const float4*>(&Tm[m * ST + c4]);
-                            const float4 t4 = (m < 16 && hi_c) ? z4 : t4l;
-                            acc[0] = fmaf(a, t4.x, acc[0]); acc[1] = fmaf(a, t4.y, acc[1]);
-                            acc[2] = fmaf(a, t4.z, acc[2]); acc[3] = fmaf(a, t4.w, acc[3]);
-                        }
-                        *reinterpret_cast<float4*>(&sm.W[r * 32 + c4]) = make_float4(acc[0], acc[1], acc[2], acc[3]);
-                        __syncthreads();
-                        const bool lo_r = (r >> 4) == 0;  // T2[r][m] for m >= 16 is zero when r < 16
-                        float t[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-                        for (int m = 0; m < 32; ++m) {
-                            const float al = Tm[(32 + r) * ST + 32 + m];
-                            const float a = (m >= 16 && lo_r) ? 0.0f : al;
-                            const float4 w4 = *reinterpret_cast<const float4*>(&sm.W[m * 32 + c4]);
-                            t[0] = fmaf(a, w4.x, t[0]); t[1] = fmaf(a, w4.y, t[1]);
-                            t[2] = fmaf(a, w4.z, t[2]); t[3] = fmaf(a, w4.w, t[3]);
-                        }
-                        *reinterpret_cast<float4*>(&Tm[(32 + r) * ST + c4]) = make_float4(-t[0], -t[1], -t[2], -t[3]);
-                    }
-                    __syncthreads();
-                    // T -> MN-major B tile (element (n = column, k = row)); row fastest across
-                    // lanes; column groups right of the row's diagonal block are zero
-                    for (int u = tid; u < 64 * 8; u += kPrepThreads) {
-                        const int m = u & 63, g = u >> 6;
+                    {   // T1, T2 -> split MN-major B tiles (element (n = column, k = row)), over A's fp32 blocks;
+                        // the upper-right 16x16 block of each is zero
+                        const int blk = tid >> 7, m = (tid >> 2) & 31, g = tid & 3;
                         float tr[8];
-                        if ((g >> 1) <= (m >> 4)) {
-                            const float4 x0 = *reinterpret_cast<const float4*>(&Tm[m * ST + g * 8]);
-                            const float4 x1 = *reinterpret_cast<const float4*>(&Tm[m * ST + g * 8 + 4]);
-                            tr[0] = x0.x; tr[1] = x0.y; tr[2] = x0.z; tr[3] = x0.w;
-                            tr[4] = x1.x; tr[5] = x1.y; tr[6] = x1.z; tr[7] = x1.w;
-                        } else {
+                        if (m < 16 && g >= 2) {
 #pragma unroll
                             for (int e = 0; e < 8; ++e) tr[e] = 0.0f;
+                        } else {
+                            const float4 x0 = *reinterpret_cast<const float4*>(&sm.T[blk][m * kTS + 8 * g]);
+                            const float4 x1 = *reinterpret_cast<const float4*>(&sm.T[blk][m * kTS + 8 * g + 4]);
+                            tr[0] = x0.x; tr[1] = x0.y; tr[2] = x0.z; tr[3] = x0.w;
+                            tr[4] = x1.x; tr[5] = x1.y; tr[6] = x1.z; tr[7] = x1.w;
                         }
-                        store_split8(&sm.u.bt[0][mnmaj(g * 8, m, 64)], &sm.u.bt[1][mnmaj(g * 8, m, 64)], tr);
+                        store_split8(&sm.u.tb[blk][0][mnmaj(8 * g, m, 32)], &sm.u.tb[blk][1][mnmaj(8 * g, m, 32)], tr);
                     }
                 }
                 umma::fence_proxy_async();
@@ -952,13 +925,20 @@ __global__ void __launch_bounds__(kPrepThreads, 4) scan_prep_kernel(ScanParams p
                 __syncthreads();
                 umma::fence_after_sync();
 
-                // P T  (M = 128 descriptor over the 64-row P tile; rows 64-127 of the product unused)
+                // [A; P] Tb: columns 0-31 (K = 32: [A; P][:, 0:32] T1) into TMEM columns 0-31, columns 32-63
+                // ([A; P][:, 32:64] T2) into 32-63.  [A; P] is K-major (K = 64: core matrices 128 B apart
+                // along K, 1 KB along M); the T tiles MN-major (K = 32: 128 B along K, 512 B along N).
                 if (tid == 0) {
-                    if (p.fast)
-                        mma_one(tmem, a_p[0], 128, 1024, 256, b_t[0], 1024, 256, 4, umma::idesc_bf16(128, 64, false, true));
-                    else
-                        mma_split(tmem, a_p[0], a_p[1], 128, 1024, 256, b_t[0], b_t[1], 1024, 256, 4,
-                                  umma::idesc_bf16(128, 64, false, true));
+                    const uint32_t a0 = umma::smem_u32(sm.ap[0]), a1 = umma::smem_u32(sm.ap[1]);
+                    const uint32_t t1h = umma::smem_u32(sm.u.tb[0][0]), t1l = umma::smem_u32(sm.u.tb[0][1]);
+                    const uint32_t t2h = umma::smem_u32(sm.u.tb[1][0]), t2l = umma::smem_u32(sm.u.tb[1][1]);
+                    if (p.fast) {
+                        mma_one(tmem, a0, 128, 1024, 256, t1h, 512, 256, 2, kIdN32);
+                        mma_one(tmem + 32, a0 + 512, 128, 1024, 256, t2h, 512, 256, 2, kIdN32);
+                    } else {
+                        mma_split(tmem, a0, a1, 128, 1024, 256, t1h, t1l, 512, 256, 2, kIdN32);
+                        mma_split(tmem + 32, a0 + 512, a1 + 512, 128, 1024, 256, t2h, t2l, 512, 256, 2, kIdN32);
+                    }
                     umma::commit(&sm.mbar);
                 }
                 if (!umma::mbar_wait(&sm.mbar, phase)) { sm.abort_flag = 1; atomicOr(err, kErrTimeout); }
@@ -967,32 +947,108 @@ __global__ void __launch_bounds__(kPrepThreads, 4) scan_prep_kernel(ScanParams p
                 if (sm.abort_flag) break;
                 umma::fence_after_sync();
 
-                // [T; P T] image (K-major, split; [P T; T] for odd chunks): threads L >= 64 copy T row L - 64
-                // from the split T tile (its 8-column groups are contiguous there), threads L < 64 split and
-                // write P T row L from TMEM lane L; columns of wg
-                {
-                    unsigned char* img = am_image(p, slot, h);
-                    const int cb = 32 * wg;
-                    if (L < 64) {
+                // operands of the correction, over the consumed [A; P] tile: [Tb; P Tb][:, 32:64] (K-major,
+                // 128 rows x K = 32: rows 0-31 zero, 32-63 T2, 64-127 P Tb from TMEM columns 32-63) and W
+                // (MN-major B, 32 x 32, from TMEM lanes 32-63, columns 0-31)
+                uint16_t* c_hi = sm.ap[0];
+                uint16_t* c_lo = sm.ap[0] + 128 * 32;
+                uint16_t* w_hi = sm.ap[1];
+                uint16_t* w_lo = sm.ap[1] + 32 * 32;
+                if (wg == 0) {
+                    if (L >= 32) {
                         float x[32];
-                        umma::tmem_ld32(tmem + lane_off + cb, x);
+                        umma::tmem_ld32(tmem + lane_off + (L >= 64 ? 32u : 0u), x);
                         umma::tmem_wait_ld();
 #pragma unroll
                         for (int q = 0; q < 4; ++q) {
+                            if (L >= 64)
+                                store_split8(&c_hi[kmaj(L, 8 * q, 32)], &c_lo[kmaj(L, 8 * q, 32)], x + 8 * q);
+                            else
+                                store_split8(&w_hi[mnmaj(8 * q, L - 32, 32)], &w_lo[mnmaj(8 * q, L - 32, 32)], x + 8 * q);
+                        }
+                    }
+                } else if (L < 64) {
+                    const int m = L - 32;  // row of T2
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) {
+                        float x[8];
+                        if (L < 32 || (m < 16 && q >= 2)) {
+#pragma unroll
+                            for (int e = 0; e < 8; ++e) x[e] = 0.0f;
+                        } else {
+                            const float4 x0 = *reinterpret_cast<const float4*>(&sm.T[1][m * kTS + 8 * q]);
+                            const float4 x1 = *reinterpret_cast<const float4*>(&sm.T[1][m * kTS + 8 * q + 4]);
+                            x[0] = x0.x; x[1] = x0.y; x[2] = x0.z; x[3] = x0.w;
+                            x[4] = x1.x; x[5] = x1.y; x[6] = x1.z; x[7] = x1.w;
+                        }
+                        store_split8(&c_hi[kmaj(L, 8 * q, 32)], &c_lo[kmaj(L, 8 * q, 32)], x);
+                    }
+                }
+                umma::fence_proxy_async();
+                umma::fence_before_sync();
+                __syncthreads();
+                umma::fence_after_sync();
+
+                // C = [Tb; P Tb][:, 32:64] W into TMEM columns 64-95 (K = 32: 128 B along K, 512 B along M/N)
+                if (tid == 0) {
+                    const uint32_t ch = umma::smem_u32(c_hi), cl = umma::smem_u32(c_lo);
+                    const uint32_t wh = umma::smem_u32(w_hi), wl = umma::smem_u32(w_lo);
+                    if (p.fast) mma_one(tmem + 64, ch, 128, 512, 256, wh, 512, 256, 2, kIdN32);
+                    else mma_split(tmem + 64, ch, cl, 128, 512, 256, wh, wl, 512, 256, 2, kIdN32);
+                    umma::commit(&sm.mbar);
+                }
+                if (!umma::mbar_wait(&sm.mbar, phase)) { sm.abort_flag = 1; atomicOr(err, kErrTimeout); }
+                phase ^= 1u;
+                __syncthreads();
+                if (sm.abort_flag) break;
+                umma::fence_after_sync();
+
+                // [T; P T] image (K-major, split; [P T; T] for odd chunks), columns [cb, cb + 32) of row L:
+                // T rows L < 64 (T1 / T21 = -C for wg 0, zero / T2 for wg 1), P T rows L - 64 ((P Tb - C) for
+                // wg 0, P Tb for wg 1)
+                {
+                    unsigned char* img = am_image(p, slot, h);
+                    const int irow = L < 64 ? (odd ? 64 + L : L) : (odd ? L - 64 : L);
+                    const bool from_tmem = L >= 32 && (wg == 0 || L >= 64);  // warp-uniform
+                    const bool zero = wg == 1 && L < 32;
+                    const float* src = sm.T[wg] + (L & 31) * kTS;  // T1 row (wg 0), T2 row (wg 1)
+#pragma unroll
+                    for (int hq = 0; hq < 2; ++hq) {  // 16 columns at a time
+                        const int cl = 16 * hq;
+                        float x[16];
+                        if (from_tmem) {
+                            if (wg == 0) {
+                                umma::tmem_ld16(tmem + lane_off + 64 + cl, x);  // C
+                                if (L >= 64) {
+                                    float y[16];
+                                    umma::tmem_ld16(tmem + lane_off + cl, y);  // P Tb, columns 0-31
+                                    umma::tmem_wait_ld();
+#pragma unroll
+                                    for (int e = 0; e < 16; ++e) x[e] = y[e] - x[e];
+                                } else {
+                                    umma::tmem_wait_ld();
+#pragma unroll
+                                    for (int e = 0; e < 16; ++e) x[e] = -x[e];
+                                }
+                            } else {
+                                umma::tmem_ld16(tmem + lane_off + 32 + cl, x);  // P Tb, columns 32-63
+                                umma::tmem_wait_ld();
+                            }
+                        } else {
+                            // rows 0-15 of a 32-block have their columns 16-31 in the zero block
+                            const bool z = zero || (hq == 1 && (L & 31) < 16);
+#pragma unroll
+                            for (int e = 0; e < 16; e += 4) {
+                                const float4 v = z ? make_float4(0.f, 0.f, 0.f, 0.f)
+                                                   : *reinterpret_cast<const float4*>(src + cl + e);
+                                x[e] = v.x; x[e + 1] = v.y; x[e + 2] = v.z; x[e + 3] = v.w;
+                            }
+                        }
+#pragma unroll
+                        for (int q = 0; q < 2; ++q) {
                             uint4 vh, vl;
                             split8(x + 8 * q, vh, vl);
-                            const int off = kmaj(odd ? L : 64 + L, cb + 8 * q, 64);
-                            *reinterpret_cast<uint4*>(img + off * 2) = vh;
-                            *reinterpret_cast<uint4*>(img + kAmBytes / 2 + off * 2) = vl;
-                        }
-                    } else {
-                        const int m = L - 64;
-#pragma unroll
-                        for (int q = 0; q < 4; ++q) {
-                            const int e = mnmaj(cb + 8 * q, m, 64);
-                            const uint4 vh = *reinterpret_cast<const uint4*>(&sm.u.bt[0][e]);
-                            const uint4 vl = *reinterpret_cast<const uint4*>(&sm.u.bt[1][e]);
-                            const int off = kmaj(odd ? 64 + m : m, cb + 8 * q, 64);
+                            const int off = kmaj(irow, 32 * wg + cl + 8 * q, 64);
                             *reinterpret_cast<uint4*>(img + off * 2) = vh;
                             *reinterpret_cast<uint4*>(img + kAmBytes / 2 + off * 2) = vl;
                         }
@@ -1029,7 +1085,7 @@ __global__ void __launch_bounds__(kPrepThreads, 4) scan_prep_kernel(ScanParams p
     }
     umma::fence_before_sync();
     __syncthreads();
-    if (warp == 0) umma::tmem_dealloc(sm.tmem_base, 64);
+    if (warp == 0) umma::tmem_dealloc(sm.tmem_base, 128);
 }
 
 // =======================================================================================
