@@ -18,7 +18,7 @@
 // x = hi + lo (hi = bf16(x), lo = bf16(x - hi)) and three MMAs hi*hi + hi*lo
 // + lo*hi accumulated in fp32 in TMEM (about 16 significant bits per operand).
 // Products are stacked to fill the 128 rows of one MMA:
-//   [K; Q] K^T -> (K K^T ; Q K^T)          P T (rows 0-63 of an M=128 MMA)
+//   [K; Q] K^T -> (K K^T ; Q K^T)          [A; P] diag(T1, T2) -> (A diag(T1, T2) ; P diag(T1, T2))
 //   [K; Q] S0  -> (K S0 ; Q S0)            [T; P T] X -> (U ; P U)
 // so (Q S0) and (P U) land in the same TMEM lanes and O needs no exchange.
 //
@@ -30,11 +30,11 @@
 //    kernel writes the images itself and scan_gram_img_kernel (one CTA per
 //    (chunk, key head)) copies them in and forms the same products.
 //  * scan_prep_kernel, persistent CTAs taking (chunk, value head) tasks in
-//    order, beside the chain once it runs: A and
-//    P from the key head's gram rows and the head's gates, the inverse of
-//    I + A (recursive halving with 16x16 diagonal blocks by forward
-//    substitution, on CUDA cores) and P T on the tensor core; writes the
-//    [T; P T] image and the chain's gate row.
+//    order, beside the chain once it runs: A and P from the key head's gram
+//    rows and the head's gates; the inverse T of I + A by halves (16x16
+//    diagonal blocks by forward substitution and their 16x16 couplings on CUDA
+//    cores, the 32x32 coupling and P T as two products on the tensor core);
+//    writes the [T; P T] image and the chain's gate row.
 //  * scan_chain_kernel, one CTA per (sequence, value head, 64-column slice):
 //    the state-dependent part, chunk after chunk, with the fp32 state slice
 //    in registers.  The next chunk's [K; Q] S is split into a part issued a
