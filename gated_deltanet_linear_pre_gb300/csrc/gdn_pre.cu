@@ -22,7 +22,7 @@
 namespace gdn {
 namespace {
 
-constexpr int kTokBlk = 8;    // tokens per warp task
+constexpr int kTokBlk = 16;   // tokens per warp task
 constexpr int kWarps = 4;     // warps (heads) per block (128-thread blocks schedule finer than 256)
 constexpr int kThreads = kWarps * 32;
 constexpr int kHistThreads = kThreads;  // one history channel per thread
@@ -100,35 +100,37 @@ __device__ __forceinline__ void store_kq(unsigned char* img_j, size_t slot_strid
     *reinterpret_cast<uint4*>(dst) = out;
 }
 
-// A whole block inside one sequence: no per-token checks, the output pointer
-// advances by a fixed row stride.  kNorm: a q/k head (L2-normalised).
-template <bool kNorm>
-__device__ __forceinline__ void conv_block(const uint2 (&cur)[kTokBlk], F4 win0, F4 win1, F4 win2, const float4& w0,
-                                           const float4& w1, const float4& w2, const float4& w3, float* dst,
-                                           size_t dstride, float eps)
+// The token rows of one warp task, one head of each: the 3 rows before the block (when they lie
+// inside the sequence) and the block's kTokBlk rows, 256 bytes each, copied in by 16-byte
+// asynchronous copies so that many rows are in flight per SM without holding registers.
+constexpr int kStageRows = kTokBlk + 3;
+constexpr int kRowBytes = kHeadDim * 2;
+
+// copy rows [r_lo, r_hi) of the stage (row r = token t_begin - 3 + r, channels of head `slot`) as
+// one commit group: 16 bytes per lane and copy, a warp moving two rows per instruction
+__device__ __forceinline__ void stage_rows(unsigned char* stage, const __half* qkv, int C, int slot, int t_begin,
+                                           int r_lo, int r_hi, int lane)
 {
-#pragma unroll
-    for (int i = 0; i < kTokBlk; ++i) {
-        const F4 x = unpack_half4(cur[i]);
-        float y0 = silu_fast(conv4(w0.x, w0.y, w0.z, w0.w, win0.x, win1.x, win2.x, x.x));
-        float y1 = silu_fast(conv4(w1.x, w1.y, w1.z, w1.w, win0.y, win1.y, win2.y, x.y));
-        float y2 = silu_fast(conv4(w2.x, w2.y, w2.z, w2.w, win0.z, win1.z, win2.z, x.z));
-        float y3 = silu_fast(conv4(w3.x, w3.y, w3.z, w3.w, win0.w, win1.w, win2.w, x.w));
-        win0 = win1;
-        win1 = win2;
-        win2 = x;
-        if (kNorm) {
-            const float inv = rsqrtf(warp_sum(y0 * y0 + y1 * y1 + y2 * y2 + y3 * y3) + eps);
-            y0 *= inv; y1 *= inv; y2 *= inv; y3 *= inv;
-        }
-        *reinterpret_cast<float4*>(dst) = make_float4(y0, y1, y2, y3);
-        dst += dstride;
+    const int pieces = (r_hi - r_lo) * (kRowBytes / 16);
+    for (int i = lane; i < pieces; i += 32) {
+        const int r = r_lo + i / (kRowBytes / 16), k = i % (kRowBytes / 16);
+        const __half* src = qkv + (size_t)(t_begin - 3 + r) * C + slot * kHeadDim + 8 * k;
+        asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"((uint32_t)__cvta_generic_to_shared(
+                         stage + r * kRowBytes + 16 * k)),
+                     "l"(src)
+                     : "memory");
     }
+    asm volatile("cp.async.commit_group;" ::: "memory");
+}
+
+__device__ __forceinline__ F4 stage_row(const unsigned char* stage, int r, int lane)
+{
+    return unpack_half4(*reinterpret_cast<const uint2*>(stage + r * kRowBytes + lane * 8));
 }
 
 // kImg: q and k go to the scan's [K; Q] images (inside gdn_layer) instead of qn / kn
 template <bool kImg>
-__global__ void __launch_bounds__(kThreads, 8)
+__global__ void __launch_bounds__(kThreads, kImg ? 6 : 8)
 pre_kernel(PreParams p, int n_slots, int head_groups, int n_conv_blocks)
 {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -162,21 +164,6 @@ pre_kernel(PreParams p, int n_slots, int head_groups, int n_conv_blocks)
     const int t_begin = tb * kTokBlk;
     const int t_end = min(p.T, t_begin + kTokBlk);
 
-    // taps of my 4 channels
-    const float4 w0 = __ldg(reinterpret_cast<const float4*>(p.conv_w) + c + 0);
-    const float4 w1 = __ldg(reinterpret_cast<const float4*>(p.conv_w) + c + 1);
-    const float4 w2 = __ldg(reinterpret_cast<const float4*>(p.conv_w) + c + 2);
-    const float4 w3 = __ldg(reinterpret_cast<const float4*>(p.conv_w) + c + 3);
-
-    // issue every row load of the block first (memory-level parallelism);
-    // kept as raw fp16 pairs to hold register use down
-    uint2 cur[kTokBlk];
-#pragma unroll
-    for (int i = 0; i < kTokBlk; ++i)
-        cur[i] = t_begin + i < t_end
-                     ? __ldg(reinterpret_cast<const uint2*>(p.qkv + (size_t)(t_begin + i) * p.C + c))
-                     : make_uint2(0u, 0u);
-
     const int hk = p.hk;
     const bool is_q = slot < hk, is_k = !is_q && slot < 2 * hk;
     const int vh = slot - 2 * hk;  // value head (valid when >= 0)
@@ -184,79 +171,120 @@ pre_kernel(PreParams p, int n_slots, int head_groups, int n_conv_blocks)
     int seq = find_seq(p.cu_seqlens, p.n_seq, t_begin);
     int seq_start = min(cu_at(p.cu_seqlens, seq, p.T), t_begin);
     int seq_end = cu_at(p.cu_seqlens, seq + 1, p.T);
+    const bool whole = t_end - t_begin == kTokBlk && t_end <= seq_end;  // the common case
+    const int pos0 = t_begin - seq_start;
+    __shared__ __align__(16) unsigned char in_stage[kWarps][kStageRows * kRowBytes];
+    unsigned char* stage = in_stage[warp];
+    if (whole) {
+        // the block's rows in two commit groups (the first half with the 3 rows before it, when those
+        // lie in the sequence; otherwise the window comes from the carried history below)
+        const int r0 = pos0 >= 3 ? 0 : 3;
+        stage_rows(stage, p.qkv, p.C, slot, t_begin, r0, 3 + kTokBlk / 2, lane);
+        stage_rows(stage, p.qkv, p.C, slot, t_begin, 3 + kTokBlk / 2, kStageRows, lane);
+    }
+
+    // taps of my 4 channels
+    const float4 w0 = __ldg(reinterpret_cast<const float4*>(p.conv_w) + c + 0);
+    const float4 w1 = __ldg(reinterpret_cast<const float4*>(p.conv_w) + c + 1);
+    const float4 w2 = __ldg(reinterpret_cast<const float4*>(p.conv_w) + c + 2);
+    const float4 w3 = __ldg(reinterpret_cast<const float4*>(p.conv_w) + c + 3);
+
     F4 win0, win1, win2;  // inputs at positions pos-3, pos-2, pos-1
-    {
-        const int pos = t_begin - seq_start;
-        win0 = tap4(p, seq, seq_start, pos - 3, c);
-        win1 = tap4(p, seq, seq_start, pos - 2, c);
-        win2 = tap4(p, seq, seq_start, pos - 1, c);
+    if (!whole || pos0 < 3) {
+        win0 = tap4(p, seq, seq_start, pos0 - 3, c);
+        win1 = tap4(p, seq, seq_start, pos0 - 2, c);
+        win2 = tap4(p, seq, seq_start, pos0 - 1, c);
     }
 
     // inside gdn_layer, q and k go to the scan's images
     const size_t slot_stride = (size_t)hk * kKqImageBytes;
     unsigned char* img_j = kImg ? p.kq_images + (size_t)(is_q ? slot : slot - hk) * kKqImageBytes : nullptr;
 
-    if (kImg && t_end - t_begin == kTokBlk && t_end <= seq_end && vh < 0) {  // the common case, image output
-        // When the 8 tokens are one 8-row group of one chunk's image (the sequence starts at a multiple
-        // of 8), that group is 4 contiguous KB (hi plane, lo plane): stage the split rows in shared
-        // memory (row-major, 272-byte rows so that neither side's accesses conflict) and write the
-        // 4 KB with 512 contiguous bytes per warp store.  Otherwise each token goes out on its own.
-        constexpr int kRow = 272, kPlane = kTokBlk * kRow;
-        __shared__ __align__(16) unsigned char kq_stage[kWarps][2 * kPlane];
-        unsigned char* stg = kq_stage[warp];
-        const int pos0 = t_begin - seq_start, slot0 = seq_start / kChunk + seq;
+    if (whole) {
+        asm volatile("cp.async.wait_group 1;" ::: "memory");  // the first half (and the rows before it)
+        __syncwarp();
+        if (pos0 >= 3) {
+            win0 = stage_row(stage, 0, lane);
+            win1 = stage_row(stage, 1, lane);
+            win2 = stage_row(stage, 2, lane);
+        }
+        // output of one token: a normalised q/k row or a v row
+        float* dst = nullptr;
+        size_t dstride = 0;
+        if (vh >= 0) {
+            dst = p.vc + ((size_t)t_begin * p.hv + vh) * kHeadDim + lane * 4;
+            dstride = (size_t)p.hv * kHeadDim;
+        } else if (!kImg) {
+            dst = (is_k ? p.kn : p.qn) + ((size_t)t_begin * hk + (is_q ? slot : slot - hk)) * kHeadDim + lane * 4;
+            dstride = (size_t)hk * kHeadDim;
+        }
+        // image output: when the sequence starts at a multiple of 8, each 8 tokens of the block are one
+        // 8-row group of one chunk's image, 4 contiguous KB (hi plane, lo plane): staged in shared memory
+        // (row-major, 272-byte rows so that neither side's accesses conflict) and written with 512
+        // contiguous bytes per warp store.  Otherwise each token goes out on its own.
+        constexpr int kRow = 272, kPlane = 8 * kRow;
+        __shared__ __align__(16) unsigned char kq_stage[kImg ? kWarps : 1][kImg ? 2 * kPlane : 16];
         const bool grouped = (pos0 & 7) == 0;
+        const int slot0 = seq_start / kChunk + seq;
 #pragma unroll
-        for (int i = 0; i < kTokBlk; ++i) {
-            const F4 x = unpack_half4(cur[i]);
-            float y0 = silu_fast(conv4(w0.x, w0.y, w0.z, w0.w, win0.x, win1.x, win2.x, x.x));
-            float y1 = silu_fast(conv4(w1.x, w1.y, w1.z, w1.w, win0.y, win1.y, win2.y, x.y));
-            float y2 = silu_fast(conv4(w2.x, w2.y, w2.z, w2.w, win0.z, win1.z, win2.z, x.z));
-            float y3 = silu_fast(conv4(w3.x, w3.y, w3.z, w3.w, win0.w, win1.w, win2.w, x.w));
-            win0 = win1;
-            win1 = win2;
-            win2 = x;
-            const float inv = rsqrtf(warp_sum(y0 * y0 + y1 * y1 + y2 * y2 + y3 * y3) + p.eps);
-            y0 *= inv; y1 *= inv; y2 *= inv; y3 *= inv;
-            if (grouped) {
-                const __nv_bfloat162 h01 = __floats2bfloat162_rn(y0, y1), h23 = __floats2bfloat162_rn(y2, y3);
-                const float2 f01 = __bfloat1622float2(h01), f23 = __bfloat1622float2(h23);
-                const __nv_bfloat162 l01 = __floats2bfloat162_rn(y0 - f01.x, y1 - f01.y);
-                const __nv_bfloat162 l23 = __floats2bfloat162_rn(y2 - f23.x, y3 - f23.y);
-                *reinterpret_cast<uint2*>(stg + i * kRow + lane * 8) =
-                    make_uint2(*reinterpret_cast<const uint32_t*>(&h01), *reinterpret_cast<const uint32_t*>(&h23));
-                *reinterpret_cast<uint2*>(stg + kPlane + i * kRow + lane * 8) =
-                    make_uint2(*reinterpret_cast<const uint32_t*>(&l01), *reinterpret_cast<const uint32_t*>(&l23));
-            } else {
-                store_kq(img_j, slot_stride, slot0, pos0 + i, is_k, lane, y0, y1, y2, y3);
+        for (int h8 = 0; h8 < kTokBlk / 8; ++h8) {
+            if (h8 == 1) {
+                asm volatile("cp.async.wait_group 0;" ::: "memory");
+                __syncwarp();
+            }
+#pragma unroll
+            for (int i8 = 0; i8 < 8; ++i8) {
+                const int i = 8 * h8 + i8;
+                const F4 x = stage_row(stage, 3 + i, lane);
+                float y0 = silu_fast(conv4(w0.x, w0.y, w0.z, w0.w, win0.x, win1.x, win2.x, x.x));
+                float y1 = silu_fast(conv4(w1.x, w1.y, w1.z, w1.w, win0.y, win1.y, win2.y, x.y));
+                float y2 = silu_fast(conv4(w2.x, w2.y, w2.z, w2.w, win0.z, win1.z, win2.z, x.z));
+                float y3 = silu_fast(conv4(w3.x, w3.y, w3.z, w3.w, win0.w, win1.w, win2.w, x.w));
+                win0 = win1;
+                win1 = win2;
+                win2 = x;
+                if (vh < 0) {
+                    const float inv = rsqrtf(warp_sum(y0 * y0 + y1 * y1 + y2 * y2 + y3 * y3) + p.eps);
+                    y0 *= inv; y1 *= inv; y2 *= inv; y3 *= inv;
+                }
+                if (kImg && vh < 0) {
+                    if (grouped) {
+                        unsigned char* stg = kq_stage[warp];
+                        const __nv_bfloat162 h01 = __floats2bfloat162_rn(y0, y1), h23 = __floats2bfloat162_rn(y2, y3);
+                        const float2 f01 = __bfloat1622float2(h01), f23 = __bfloat1622float2(h23);
+                        const __nv_bfloat162 l01 = __floats2bfloat162_rn(y0 - f01.x, y1 - f01.y);
+                        const __nv_bfloat162 l23 = __floats2bfloat162_rn(y2 - f23.x, y3 - f23.y);
+                        *reinterpret_cast<uint2*>(stg + i8 * kRow + lane * 8) =
+                            make_uint2(*reinterpret_cast<const uint32_t*>(&h01), *reinterpret_cast<const uint32_t*>(&h23));
+                        *reinterpret_cast<uint2*>(stg + kPlane + i8 * kRow + lane * 8) =
+                            make_uint2(*reinterpret_cast<const uint32_t*>(&l01), *reinterpret_cast<const uint32_t*>(&l23));
+                    } else {
+                        store_kq(img_j, slot_stride, slot0, pos0 + i, is_k, lane, y0, y1, y2, y3);
+                    }
+                } else {
+                    *reinterpret_cast<float4*>(dst) = make_float4(y0, y1, y2, y3);
+                    dst += dstride;
+                }
+            }
+            if (kImg && vh < 0 && grouped) {
+                __syncwarp();
+                const unsigned char* stg = kq_stage[warp];
+                const int pg = pos0 + 8 * h8, ci = pg >> 6;
+                const int row0 = ((is_k == ((ci & 1) != 0)) ? 64 : 0) + (pg & 63);
+                unsigned char* gdst = img_j + (size_t)(slot0 + ci) * slot_stride + (row0 >> 3) * 4096;
+                // 16-byte piece `lane` of each 512-byte run: plane k / 4, core matrix 4 (k % 4) + lane / 8
+                // (columns 8 m .. 8 m + 7), row lane % 8
+#pragma unroll
+                for (int k = 0; k < 8; ++k) {
+                    const int m = (k & 3) * 4 + (lane >> 3), r = lane & 7;
+                    *reinterpret_cast<uint4*>(gdst + k * 512 + lane * 16) =
+                        *reinterpret_cast<const uint4*>(stg + (k >> 2) * kPlane + r * kRow + m * 16);
+                }
+                __syncwarp();  // the stage is refilled by the next 8 tokens
             }
         }
-        if (grouped) {
-            __syncwarp();
-            const int ci = pos0 >> 6;
-            const int row0 = ((is_k == ((ci & 1) != 0)) ? 64 : 0) + (pos0 & 63);
-            unsigned char* dst = img_j + (size_t)(slot0 + ci) * slot_stride + (row0 >> 3) * 4096;
-            // 16-byte piece `lane` of each 512-byte run: plane k / 4, core matrix 4 (k % 4) + lane / 8
-            // (columns 8 m .. 8 m + 7), row lane % 8
-#pragma unroll
-            for (int k = 0; k < 8; ++k) {
-                const int m = (k & 3) * 4 + (lane >> 3), i = lane & 7;
-                *reinterpret_cast<uint4*>(dst + k * 512 + lane * 16) =
-                    *reinterpret_cast<const uint4*>(stg + (k >> 2) * kPlane + i * kRow + m * 16);
-            }
-        }
-    } else if (t_end - t_begin == kTokBlk && t_end <= seq_end) {  // the common case
-        if (vh >= 0)
-            conv_block<false>(cur, win0, win1, win2, w0, w1, w2, w3,
-                              p.vc + ((size_t)t_begin * p.hv + vh) * kHeadDim + lane * 4, (size_t)p.hv * kHeadDim,
-                              p.eps);
-        else
-            conv_block<true>(cur, win0, win1, win2, w0, w1, w2, w3,
-                             (is_k ? p.kn : p.qn) + ((size_t)t_begin * hk + (is_q ? slot : slot - hk)) * kHeadDim +
-                                 lane * 4,
-                             (size_t)hk * kHeadDim, p.eps);
     } else {
-#pragma unroll
+    // a block that crosses a sequence end or is cut by T: token by token
     for (int i = 0; i < kTokBlk; ++i) {
         const int t = t_begin + i;
         if (t >= t_end) break;
@@ -272,7 +300,7 @@ pre_kernel(PreParams p, int n_slots, int head_groups, int n_conv_blocks)
             win1 = tap4(p, seq, seq_start, -2, c);
             win2 = tap4(p, seq, seq_start, -1, c);
         }
-        const F4 x = unpack_half4(cur[i]);
+        const F4 x = load_half4(p.qkv + (size_t)t * p.C + c);
         float y0 = silu_fast(conv4(w0.x, w0.y, w0.z, w0.w, win0.x, win1.x, win2.x, x.x));
         float y1 = silu_fast(conv4(w1.x, w1.y, w1.z, w1.w, win0.y, win1.y, win2.y, x.y));
         float y2 = silu_fast(conv4(w2.x, w2.y, w2.z, w2.w, win0.z, win1.z, win2.z, x.z));
