@@ -22,7 +22,7 @@
 namespace gdn {
 namespace {
 
-constexpr int kTokBlk = 16;   // tokens per warp task
+constexpr int kTokBlk = 16;   // tokens per warp task (a multiple of 8, at most 32)
 constexpr int kWarps = 4;     // warps (heads) per block (128-thread blocks schedule finer than 256)
 constexpr int kThreads = kWarps * 32;
 constexpr int kHistThreads = kThreads;  // one history channel per thread
@@ -104,6 +104,7 @@ __device__ __forceinline__ void store_kq(unsigned char* img_j, size_t slot_strid
 // inside the sequence) and the block's kTokBlk rows, 256 bytes each, copied in by 16-byte
 // asynchronous copies so that many rows are in flight per SM without holding registers.
 constexpr int kStageRows = kTokBlk + 3;
+static_assert(kTokBlk % 8 == 0 && kTokBlk <= 32, "one commit group per 8 tokens, at most 4 in flight; one gate lane per token");
 constexpr int kRowBytes = kHeadDim * 2;
 
 // copy rows [r_lo, r_hi) of the stage (row r = token t_begin - 3 + r, channels of head `slot`) as
@@ -121,6 +122,17 @@ __device__ __forceinline__ void stage_rows(unsigned char* stage, const __half* q
                      : "memory");
     }
     asm volatile("cp.async.commit_group;" ::: "memory");
+}
+
+// wait until at most n of this thread's commit groups are still in flight (n < 4)
+__device__ __forceinline__ void cp_async_wait_groups(int n)
+{
+    switch (n) {
+        case 0: asm volatile("cp.async.wait_group 0;" ::: "memory"); break;
+        case 1: asm volatile("cp.async.wait_group 1;" ::: "memory"); break;
+        case 2: asm volatile("cp.async.wait_group 2;" ::: "memory"); break;
+        default: asm volatile("cp.async.wait_group 3;" ::: "memory"); break;
+    }
 }
 
 __device__ __forceinline__ F4 stage_row(const unsigned char* stage, int r, int lane)
@@ -176,11 +188,12 @@ pre_kernel(PreParams p, int n_slots, int head_groups, int n_conv_blocks)
     __shared__ __align__(16) unsigned char in_stage[kWarps][kStageRows * kRowBytes];
     unsigned char* stage = in_stage[warp];
     if (whole) {
-        // the block's rows in two commit groups (the first half with the 3 rows before it, when those
-        // lie in the sequence; otherwise the window comes from the carried history below)
+        // the block's rows in one commit group per 8 tokens (the first with the 3 rows before the block,
+        // when those lie in the sequence; otherwise the window comes from the carried history below)
         const int r0 = pos0 >= 3 ? 0 : 3;
-        stage_rows(stage, p.qkv, p.C, slot, t_begin, r0, 3 + kTokBlk / 2, lane);
-        stage_rows(stage, p.qkv, p.C, slot, t_begin, 3 + kTokBlk / 2, kStageRows, lane);
+#pragma unroll
+        for (int g = 0; g < kTokBlk / 8; ++g)
+            stage_rows(stage, p.qkv, p.C, slot, t_begin, g == 0 ? r0 : 3 + 8 * g, 3 + 8 * (g + 1), lane);
     }
 
     // taps of my 4 channels
@@ -201,7 +214,7 @@ pre_kernel(PreParams p, int n_slots, int head_groups, int n_conv_blocks)
     unsigned char* img_j = kImg ? p.kq_images + (size_t)(is_q ? slot : slot - hk) * kKqImageBytes : nullptr;
 
     if (whole) {
-        asm volatile("cp.async.wait_group 1;" ::: "memory");  // the first half (and the rows before it)
+        cp_async_wait_groups(kTokBlk / 8 - 1);  // the first 8 rows (and the rows before them)
         __syncwarp();
         if (pos0 >= 3) {
             win0 = stage_row(stage, 0, lane);
@@ -228,8 +241,8 @@ pre_kernel(PreParams p, int n_slots, int head_groups, int n_conv_blocks)
         const int slot0 = seq_start / kChunk + seq;
 #pragma unroll
         for (int h8 = 0; h8 < kTokBlk / 8; ++h8) {
-            if (h8 == 1) {
-                asm volatile("cp.async.wait_group 0;" ::: "memory");
+            if (h8 > 0) {
+                cp_async_wait_groups(kTokBlk / 8 - 1 - h8);
                 __syncwarp();
             }
 #pragma unroll
