@@ -450,6 +450,11 @@ def main():
         "scan": lambda l, x, t: scan_fn(d, cu, T, t["qn"], t["kn"], t["vc"], t["glog"], t["beta"], x["S0"],
                                             S_out[l], t["o"], scan_ws),
         "post": lambda l, x, t: gdn.gdn_post(d, T, t["o"], x["z"], x["gamma"], out_f32, y[l]),
+        # the pre kernel inside gdn_layer (writes the scan's bf16 operand images), run alone on the
+        # layer workspace through the stage-subset test hook
+        "pre_img": lambda l, x, t: gdn.gdn_layer_selftest_stages(
+            d, cu, T, x["qkv"], x["conv_w"], x["hist"], hist_out[l], x["a"], x["b"], x["z"], x["A_log"],
+            x["dt_bias"], x["gamma"], x["S0"], S_out[l], out_f32, y[l], layer_ws, bool(args.fast), 1),
     }
 
     def stage_group(name):
@@ -489,7 +494,7 @@ def main():
     total_ms = e_start.elapsed_time(e_end)
     launches = args.steps * LAYERS
     per_launch_ms = {k: ev_st[k][0].elapsed_time(ev_st[k][1]) / launches for k in stage_calls}
-    staged_ms = sum(per_launch_ms.values()) * launches
+    staged_ms = sum(per_launch_ms[k] for k in ("pre", "scan", "post")) * launches
     total_ms = max_over_ranks(total_ms, world)
     ms_per_step = total_ms / args.steps
     value = world * T * args.steps / (total_ms / 1e3)
@@ -588,12 +593,13 @@ def main():
     hbm_peak, tf_peak, peak_src = load_peaks()
     stage_bytes = {"pre": PRE_BYTES_TOK * T + PRE_BYTES_SEQ, "scan": SCAN_BYTES_TOK * T + SCAN_BYTES_SEQ,
                    "post": (POST_BYTES_TOK + (HV * DV * 2 if out_f32 else 0)) * T + DV * 4}
+    stage_bytes["pre_img"] = stage_bytes["pre"]  # the q/k images (bf16 hi + lo) are as large as fp32 q/k
     stages = {}
-    for k in ("pre", "scan", "post"):
+    for k in ("pre", "pre_img", "scan", "post"):
         gbs = stage_bytes[k] / (per_launch_ms[k] * 1e-3) / 1e9
         stages[k] = {"ms_per_launch": per_launch_ms[k], "alg_bytes_per_launch": stage_bytes[k],
                      "achieved_gbs": gbs, "frac_of_hbm": gbs / hbm_peak}
-    dom = max(per_launch_ms, key=per_launch_ms.get)
+    dom = max(("pre", "scan", "post"), key=per_launch_ms.get)
     traffic = None if (args.fast and dom == "scan") else stage_traffic(dom)  # captures are of the split path
     roofline = {"bound": "hbm", "kernel": f"gdn_{dom}", "achieved": stages[dom]["achieved_gbs"], "peak": hbm_peak,
                 "unit": "GB/s", "frac": stages[dom]["frac_of_hbm"], "traffic": traffic,
@@ -617,7 +623,8 @@ def main():
                 "timed_call": layer_fn.__name__,
                 "stage_timing": "each stage's launches for all layers back to back, through the stage calls gdn_pre, "
                                 "gdn_scan and gdn_post (gdn_layer runs the same prep, chain and post kernels; its "
-                                "pre writes the scan's bf16 operand images and its gram copies them in)", "staged_ms_per_step": staged_ms / args.steps,
+                                "pre writes the scan's bf16 operand images and its gram copies them in); pre_img: "
+                                "gdn_layer's own pre kernel alone, through the stage-subset test hook", "staged_ms_per_step": staged_ms / args.steps,
                 "cpu_baseline": cpu, "e2e": e2e,
                 # per layer: pre, the scan's gram, prep and chain kernels, post (timed pass 1)
                 "gpu_launches": 5 * LAYERS * args.steps, "clocks": clocks.summary()}

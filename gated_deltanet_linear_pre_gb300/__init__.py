@@ -11,7 +11,7 @@ its thin ctypes binding under the ABI's names:
 method on the CPU.
 """
 _BINDING = ("gdn_pre", "gdn_scan", "gdn_scan_fast", "gdn_layer_fast", "gdn_scan_noalloc", "gdn_post", "gdn_layer", "gdn_step", "gdn_scan_check", "gdn_layer_check", "gdn_scan_noalloc_check", "gdn_last_async_error",
-            "gdn_scan_selftest_timeout", "gdn_scan_selftest_one_taker", "gdn_scan_selftest_withhold_flag", "gdn_scan_workspace_bytes",
+            "gdn_scan_selftest_timeout", "gdn_scan_selftest_one_taker", "gdn_scan_selftest_withhold_flag", "gdn_layer_selftest_stages", "gdn_scan_workspace_bytes",
             "gdn_layer_workspace_bytes", "dims", "gdn_dims", "GdnError", "lib", "library_path")
 
 __all__ = list(_BINDING) + ["inputs", "build"]

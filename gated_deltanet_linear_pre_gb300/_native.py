@@ -93,6 +93,8 @@ def lib():
             L.gdn_scan_selftest_one_taker.argtypes = [D, _i32, _i32] + [_p] * 10 + [_sz, _p]
             L.gdn_scan_selftest_withhold_flag.restype = ctypes.c_int
             L.gdn_scan_selftest_withhold_flag.argtypes = [D, _i32, _i32] + [_p] * 10 + [_sz, _p]
+            L.gdn_layer_selftest_stages.restype = ctypes.c_int
+            L.gdn_layer_selftest_stages.argtypes = [D, _i32, _i32] + [_p] * 13 + [_i32, _p, _p, _sz, _i32, _i32, _p]
             L.gdn_step.restype = ctypes.c_int
             L.gdn_step.argtypes = [D, _i32] + [_p] * 12 + [_i32, _p, _p]
             _lib = L
@@ -226,8 +228,16 @@ def gdn_layer_fast(d: gdn_dims, cu_seqlens, total_tokens, qkv, conv_w, hist_in, 
            gamma, S_in, S_out, out_f32, y, workspace, stream)
 
 
+def gdn_layer_selftest_stages(d: gdn_dims, cu_seqlens, total_tokens, qkv, conv_w, hist_in, hist_out, a, b, z,
+                              A_log, dt_bias, gamma, S_in, S_out, out_f32: bool, y, workspace, fast: bool,
+                              stages: int, stream=None):
+    """Test and timing hook: only the gdn_layer stages in the mask `stages` (1 pre, 2 scan, 4 post)."""
+    _layer("gdn_layer_selftest_stages", d, cu_seqlens, total_tokens, qkv, conv_w, hist_in, hist_out, a, b, z, A_log,
+           dt_bias, gamma, S_in, S_out, out_f32, y, workspace, stream, extra=(1 if fast else 0, int(stages)))
+
+
 def _layer(name, d, cu_seqlens, total_tokens, qkv, conv_w, hist_in, hist_out, a, b, z, A_log, dt_bias,
-           gamma, S_in, S_out, out_f32, y, workspace, stream):
+           gamma, S_in, S_out, out_f32, y, workspace, stream, extra=()):
     n_seq, T = _batch(cu_seqlens, total_tokens)
     C, hv, dk, dv = _C(d), d.hv, d.dk, d.dv
     f16, f32 = torch.float16, torch.float32
@@ -241,7 +251,7 @@ def _layer(name, d, cu_seqlens, total_tokens, qkv, conv_w, hist_in, hist_out, a,
                          _ptr(gamma, "gamma", f32, (dv,)), _ptr(S_in, "S_in", f32, (n_seq, hv, dk, dv)),
                          _ptr(S_out, "S_out", f32, (n_seq, hv, dk, dv)), 1 if out_f32 else 0,
                          _ptr(y, "y", ydt, (T, hv, dv)), _ptr(workspace, "workspace", torch.uint8),
-                         workspace.numel() if workspace is not None else 0, _stream(stream))
+                         workspace.numel() if workspace is not None else 0, *extra, _stream(stream))
     _check(name, st)
 
 

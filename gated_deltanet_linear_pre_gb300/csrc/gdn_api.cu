@@ -387,9 +387,10 @@ static gdn_status layer_impl(const gdn_dims* dims, int32_t n_seq, int32_t T, con
                              const uint16_t* a, const uint16_t* b, const uint16_t* z, const float* A_log,
                              const float* dt_bias, const float* gamma, const float* S_in, float* S_out,
                              int32_t out_f32, void* y, void* workspace, size_t workspace_bytes,
-                             struct CUstream_st* stream, int fast)
+                             struct CUstream_st* stream, int fast, int stages)
 {
     gdn_status st;
+    if (stages < 0 || stages > 7) return fail(GDN_ERR_INVALID_ARG, "stage mask %d outside 0..7", stages);
     if ((st = check_dims(dims)) != GDN_OK) return st;
     if ((st = check_batch(n_seq, T, cu_seqlens)) != GDN_OK) return st;
     const size_t need = gdn_layer_workspace_bytes(dims, n_seq, T);
@@ -430,9 +431,9 @@ static gdn_status layer_impl(const gdn_dims* dims, int32_t n_seq, int32_t T, con
         pp.kq_images = static_cast<unsigned char*>(sws) + gdn::scan_kq_images_offset(dims->hk, dims->hv, n_seq, T);
         sp.kq_written = 1;
     }
-    if ((st = run_pre(pp, stream)) != GDN_OK) return st;
-    if ((st = run_scan(sp, stream)) != GDN_OK) return st;
-    return run_post(op, stream);
+    if ((stages & 1) && (st = run_pre(pp, stream)) != GDN_OK) return st;
+    if ((stages & 2) && (st = run_scan(sp, stream)) != GDN_OK) return st;
+    return (stages & 4) ? run_post(op, stream) : GDN_OK;
 }
 
 gdn_status gdn_layer(const gdn_dims* dims, int32_t n_seq, int32_t T, const int32_t* cu_seqlens,
@@ -443,7 +444,7 @@ gdn_status gdn_layer(const gdn_dims* dims, int32_t n_seq, int32_t T, const int32
                      struct CUstream_st* stream)
 {
     return layer_impl(dims, n_seq, T, cu_seqlens, qkv, conv_w, hist_in, hist_out, a, b, z, A_log, dt_bias, gamma,
-                      S_in, S_out, out_f32, y, workspace, workspace_bytes, stream, 0);
+                      S_in, S_out, out_f32, y, workspace, workspace_bytes, stream, 0, 7);
 }
 
 gdn_status gdn_layer_fast(const gdn_dims* dims, int32_t n_seq, int32_t T, const int32_t* cu_seqlens,
@@ -454,7 +455,18 @@ gdn_status gdn_layer_fast(const gdn_dims* dims, int32_t n_seq, int32_t T, const 
                           struct CUstream_st* stream)
 {
     return layer_impl(dims, n_seq, T, cu_seqlens, qkv, conv_w, hist_in, hist_out, a, b, z, A_log, dt_bias, gamma,
-                      S_in, S_out, out_f32, y, workspace, workspace_bytes, stream, 1);
+                      S_in, S_out, out_f32, y, workspace, workspace_bytes, stream, 1, 7);
+}
+
+gdn_status gdn_layer_selftest_stages(const gdn_dims* dims, int32_t n_seq, int32_t T, const int32_t* cu_seqlens,
+                                     const uint16_t* qkv, const float* conv_w, const uint16_t* hist_in,
+                                     uint16_t* hist_out, const uint16_t* a, const uint16_t* b, const uint16_t* z,
+                                     const float* A_log, const float* dt_bias, const float* gamma, const float* S_in,
+                                     float* S_out, int32_t out_f32, void* y, void* workspace, size_t workspace_bytes,
+                                     int32_t fast, int32_t stages, struct CUstream_st* stream)
+{
+    return layer_impl(dims, n_seq, T, cu_seqlens, qkv, conv_w, hist_in, hist_out, a, b, z, A_log, dt_bias, gamma,
+                      S_in, S_out, out_f32, y, workspace, workspace_bytes, stream, fast ? 1 : 0, stages);
 }
 
 }  // extern "C"

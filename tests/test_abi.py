@@ -30,7 +30,7 @@ def test_hooks_stay_out_of_the_product_header():
     # the self-test entry points are declared in gdn_testing.h only
     assert not [s for s in declared_symbols() if "selftest" in s]
     assert set(declared_symbols(TESTING_HEADER)) == {"gdn_scan_selftest_timeout", "gdn_scan_selftest_one_taker",
-                                                     "gdn_scan_selftest_withhold_flag"}
+                                                     "gdn_scan_selftest_withhold_flag", "gdn_layer_selftest_stages"}
 
 
 def test_header_declares_the_boundary():

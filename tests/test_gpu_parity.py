@@ -408,3 +408,37 @@ def test_layer_equals_the_three_stage_calls_bitwise(case, fast):
     staged, layer = _stages_then_layer(LAYER_EQ_CASES[case](), fast)
     for name, a, b in zip(("y", "S_out", "hist_out"), staged, layer):
         assert torch.equal(a, b), name
+
+
+@pytest.mark.parametrize("fast", [False, True], ids=["precise", "fast"])
+def test_layer_stage_by_stage_hook_equals_the_layer_bitwise(fast):
+    """gdn_layer_selftest_stages with the masks 1 (pre), 2 (scan), 4 (post) in turn on one workspace
+    (the path the bench times the image-writing pre on) gives gdn_layer's outputs bit for bit; a
+    mask outside 0..7 is rejected."""
+    torch = pytest.importorskip("torch")
+    import gpu_util as u
+    import gated_deltanet_linear_pre_gb300 as gdn
+    inp = gin.make_layer(77, [300, 1, 130], hist_nonzero=True, S0_std=0.02)
+    d = u.dims_of(inp)
+    x = u.device_inputs(inp)
+    T, n_seq = inp.total_tokens, inp.n_seq
+    layer_fn = gdn.gdn_layer_fast if fast else gdn.gdn_layer
+    outs = []
+    for staged in (False, True):
+        y = torch.empty((T, d.hv, d.dv), device="cuda", dtype=torch.float16)
+        hist_out, S_out = torch.empty_like(x["hist"]), torch.empty_like(x["S0"])
+        ws = torch.empty(gdn.gdn_layer_workspace_bytes(d, n_seq, T), device="cuda", dtype=torch.uint8)
+        args = (d, x["cu"], T, x["qkv"], x["conv_w"], x["hist"], hist_out, x["a"], x["b"], x["z"], x["A_log"],
+                x["dt_bias"], x["gamma"], x["S0"], S_out, False, y, ws)
+        if staged:
+            for mask in (1, 2, 4):
+                gdn.gdn_layer_selftest_stages(*args, fast, mask)
+        else:
+            layer_fn(*args)
+        gdn.gdn_layer_check(d, n_seq, T, ws)
+        outs.append((y, S_out, hist_out))
+    for name, a, b in zip(("y", "S_out", "hist_out"), *outs):
+        assert torch.equal(a, b), name
+    with pytest.raises(gdn.GdnError) as ei:
+        gdn.gdn_layer_selftest_stages(*args, fast, 8)
+    assert ei.value.status == 1  # GDN_ERR_INVALID_ARG
