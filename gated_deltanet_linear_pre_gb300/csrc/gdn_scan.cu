@@ -506,9 +506,11 @@ __global__ void __launch_bounds__(kGramThreads, 2) scan_gram_kernel(ScanParams p
             umma::tmem_ld32(tmem + lane_off + 32 * wg, d);
             umma::tmem_wait_ld();
             float4* dst = reinterpret_cast<float4*>(gram_rows(p, slot, j));
+            // only the groups prep reads: A and P are lower triangular, so row i's columns up to i
 #pragma unroll
             for (int q = 0; q < 8; ++q)
-                dst[gram_f4(L, 8 * wg + q)] = make_float4(d[4 * q], d[4 * q + 1], d[4 * q + 2], d[4 * q + 3]);
+                if (4 * (8 * wg + q) <= (L & 63))
+                    dst[gram_f4(L, 8 * wg + q)] = make_float4(d[4 * q], d[4 * q + 1], d[4 * q + 2], d[4 * q + 3]);
             if (has_prev[t]) {  // M rows -> split K-major image (K = 64 tokens of the previous chunk), Q rows first for odd chunks
                 const int mrow = odd[t] ? (L ^ 64) : L;
                 umma::tmem_ld32(tmem + lane_off + 64 + 32 * wg, d);
@@ -622,9 +624,11 @@ __global__ void __launch_bounds__(kGramThreads, 2) scan_gram_img_kernel(ScanPara
             // gram rows in (K K^T ; Q K^T) order: image row L of an odd chunk is row L ^ 64 there
             float4* dst = reinterpret_cast<float4*>(gram_rows(p, (size_t)slot, j));
             const int grow = odd ? (L ^ 64) : L;
+            // only the groups prep reads: A and P are lower triangular, so row i's columns up to i
 #pragma unroll
             for (int q = 0; q < 8; ++q)
-                dst[gram_f4(grow, 8 * wg + q)] = make_float4(d[4 * q], d[4 * q + 1], d[4 * q + 2], d[4 * q + 3]);
+                if (4 * (8 * wg + q) <= (L & 63))
+                    dst[gram_f4(grow, 8 * wg + q)] = make_float4(d[4 * q], d[4 * q + 1], d[4 * q + 2], d[4 * q + 3]);
             if (has_prev) {  // M rows, already in stacking order -> split K-major image (K = 64 previous tokens)
                 umma::tmem_ld32(tmem + lane_off + 64 + 32 * wg, d);
                 umma::tmem_wait_ld();
@@ -779,13 +783,15 @@ __global__ void __launch_bounds__(kPrepThreads, 4) scan_prep_kernel(ScanParams p
                 if (lane == 0) gr->gL = __expf(GL);
             }
             // this thread's 32 entries of the gram rows of the key head: row L (K K^T for
-            // L < 64, Q K^T for L >= 64), columns [32 wg, 32 wg + 32)
+            // L < 64, Q K^T for L >= 64), columns [32 wg, 32 wg + 32); gram writes only the groups
+            // that reach the diagonal or below (the rest enter A and P as zeros)
             float d[32];
             {
                 const float4* src = reinterpret_cast<const float4*>(gram_rows(p, slot, j));
 #pragma unroll
                 for (int q = 0; q < 8; ++q) {
-                    const float4 x = __ldg(src + gram_f4(L, 8 * wg + q));
+                    const float4 x = 4 * (8 * wg + q) <= (L & 63) ? __ldg(src + gram_f4(L, 8 * wg + q))
+                                                                   : make_float4(0.f, 0.f, 0.f, 0.f);
                     d[4 * q] = x.x; d[4 * q + 1] = x.y; d[4 * q + 2] = x.z; d[4 * q + 3] = x.w;
                 }
             }
