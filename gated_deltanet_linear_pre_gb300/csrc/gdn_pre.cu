@@ -10,11 +10,14 @@
 // order, vectorised tap loads, history kept channel by channel.)
 //
 // HBM-bound.  One warp owns one 128-channel head for a block of kTokBlk
-// consecutive tokens: each lane holds 4 channels' taps in registers, reads
-// each qkv row once (8-byte loads, 256 B per warp per row, fully coalesced),
-// slides the 3-token window in registers and writes 16-byte fp32 stores.
-// The q/k norms are warp reductions.  A separate row of blocks writes the
-// carried history of every sequence.
+// consecutive tokens.  It first copies the block's rows of its head (and the 3
+// rows before them) into shared memory with 16-byte asynchronous copies, one
+// commit group per 8 tokens, so that many rows are in flight per SM without
+// holding registers; then each lane, holding 4 channels' taps in registers,
+// reads its 8 bytes of each row from shared memory, slides the 3-token window
+// in registers and writes 16-byte fp32 stores.  The q/k norms are warp
+// reductions.  A separate row of blocks writes the carried history of every
+// sequence.
 #include <cuda_bf16.h>
 
 #include "gdn_internal.cuh"
