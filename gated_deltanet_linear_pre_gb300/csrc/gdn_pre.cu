@@ -9,8 +9,9 @@
 // vectorization and scan", variants: four multiply-adds per output in tap
 // order, vectorised tap loads, history kept channel by channel.)
 //
-// HBM-bound.  One warp owns one 128-channel head for a block of kTokBlk
-// consecutive tokens.  It first copies the block's rows of its head (and the 3
+// HBM-bound.  One warp owns one 128-channel head for a block of 16 consecutive
+// tokens (8 in the variant that writes the scan's images, whose extra staging
+// would otherwise cap it at 6 blocks per SM).  It first copies the block's rows of its head (and the 3
 // rows before them) into shared memory with 16-byte asynchronous copies, one
 // commit group per 8 tokens, so that many rows are in flight per SM without
 // holding registers; then each lane, holding 4 channels' taps in registers,
@@ -25,7 +26,10 @@
 namespace gdn {
 namespace {
 
-constexpr int kTokBlk = 16;   // tokens per warp task (a multiple of 8, at most 32)
+// tokens per warp task (a multiple of 8, at most 32): 16 for the plain variant; 8 for the image
+// variant, so that its two stages fit 8 blocks per SM
+template <bool kImg>
+constexpr int kTokBlkFor = kImg ? 8 : 16;
 constexpr int kWarps = 4;     // warps (heads) per block (128-thread blocks schedule finer than 256)
 constexpr int kThreads = kWarps * 32;
 constexpr int kHistThreads = kThreads;  // one history channel per thread
@@ -104,10 +108,10 @@ __device__ __forceinline__ void store_kq(unsigned char* img_j, size_t slot_strid
 }
 
 // The token rows of one warp task, one head of each: the 3 rows before the block (when they lie
-// inside the sequence) and the block's kTokBlk rows, 256 bytes each, copied in by 16-byte
-// asynchronous copies so that many rows are in flight per SM without holding registers.
-constexpr int kStageRows = kTokBlk + 3;
-static_assert(kTokBlk % 8 == 0 && kTokBlk <= 32, "one commit group per 8 tokens, at most 4 in flight; one gate lane per token");
+// inside the sequence) and the block's rows, 256 bytes each, copied in by 16-byte asynchronous
+// copies so that many rows are in flight per SM without holding registers.
+static_assert(kTokBlkFor<false> % 8 == 0 && kTokBlkFor<false> <= 32 && kTokBlkFor<true> % 8 == 0 && kTokBlkFor<true> <= 32,
+              "one commit group per 8 tokens, at most 4 in flight; one gate lane per token");
 constexpr int kRowBytes = kHeadDim * 2;
 
 // copy rows [r_lo, r_hi) of the stage (row r = token t_begin - 3 + r, channels of head `slot`) as
@@ -145,7 +149,7 @@ __device__ __forceinline__ F4 stage_row(const unsigned char* stage, int r, int l
 
 // kImg: q and k go to the scan's [K; Q] images (inside gdn_layer) instead of qn / kn
 template <bool kImg>
-__global__ void __launch_bounds__(kThreads, kImg ? 6 : 8)
+__global__ void __launch_bounds__(kThreads, 8)
 pre_kernel(PreParams p, int n_slots, int head_groups, int n_conv_blocks)
 {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -176,6 +180,8 @@ pre_kernel(PreParams p, int n_slots, int head_groups, int n_conv_blocks)
     const int tb = blockIdx.x / head_groups;
     if (slot >= n_slots) return;
     const int c = slot * kHeadDim + lane * 4;
+    constexpr int kTokBlk = kTokBlkFor<kImg>;
+    constexpr int kStageRows = kTokBlk + 3;
     const int t_begin = tb * kTokBlk;
     const int t_end = min(p.T, t_begin + kTokBlk);
 
@@ -236,9 +242,10 @@ pre_kernel(PreParams p, int n_slots, int head_groups, int n_conv_blocks)
         }
         // image output: when the sequence starts at a multiple of 8, each 8 tokens of the block are one
         // 8-row group of one chunk's image, 4 contiguous KB (hi plane, lo plane): staged in shared memory
-        // (row-major, 272-byte rows so that neither side's accesses conflict) and written with 512
-        // contiguous bytes per warp store.  Otherwise each token goes out on its own.
-        constexpr int kRow = 272, kPlane = 8 * kRow;
+        // (row-major 256-byte rows whose 16-byte pieces are permuted by the row index, piece m of row
+        // r at m ^ r, so that neither side's accesses conflict) and written with 512 contiguous bytes
+        // per warp store.  Otherwise each token goes out on its own.
+        constexpr int kRow = 256, kPlane = 8 * kRow;
         __shared__ __align__(16) unsigned char kq_stage[kImg ? kWarps : 1][kImg ? 2 * kPlane : 16];
         const bool grouped = (pos0 & 7) == 0;
         const int slot0 = seq_start / kChunk + seq;
@@ -270,9 +277,10 @@ pre_kernel(PreParams p, int n_slots, int head_groups, int n_conv_blocks)
                         const float2 f01 = __bfloat1622float2(h01), f23 = __bfloat1622float2(h23);
                         const __nv_bfloat162 l01 = __floats2bfloat162_rn(y0 - f01.x, y1 - f01.y);
                         const __nv_bfloat162 l23 = __floats2bfloat162_rn(y2 - f23.x, y3 - f23.y);
-                        *reinterpret_cast<uint2*>(stg + i8 * kRow + lane * 8) =
+                        const int so = i8 * kRow + (((lane >> 1) ^ i8) << 4) + (lane & 1) * 8;
+                        *reinterpret_cast<uint2*>(stg + so) =
                             make_uint2(*reinterpret_cast<const uint32_t*>(&h01), *reinterpret_cast<const uint32_t*>(&h23));
-                        *reinterpret_cast<uint2*>(stg + kPlane + i8 * kRow + lane * 8) =
+                        *reinterpret_cast<uint2*>(stg + kPlane + so) =
                             make_uint2(*reinterpret_cast<const uint32_t*>(&l01), *reinterpret_cast<const uint32_t*>(&l23));
                     } else {
                         store_kq(img_j, slot_stride, slot0, pos0 + i, is_k, lane, y0, y1, y2, y3);
@@ -294,7 +302,7 @@ pre_kernel(PreParams p, int n_slots, int head_groups, int n_conv_blocks)
                 for (int k = 0; k < 8; ++k) {
                     const int m = (k & 3) * 4 + (lane >> 3), r = lane & 7;
                     *reinterpret_cast<uint4*>(gdst + k * 512 + lane * 16) =
-                        *reinterpret_cast<const uint4*>(stg + (k >> 2) * kPlane + r * kRow + m * 16);
+                        *reinterpret_cast<const uint4*>(stg + (k >> 2) * kPlane + r * kRow + ((m ^ r) << 4));
                 }
                 __syncwarp();  // the stage is refilled by the next 8 tokens
             }
@@ -361,7 +369,8 @@ pre_kernel(PreParams p, int n_slots, int head_groups, int n_conv_blocks)
 cudaError_t launch_pre(const PreParams& p, cudaStream_t stream)
 {
     const int n_slots = 2 * p.hk + p.hv;
-    const long long n_tblocks = (p.T + kTokBlk - 1) / kTokBlk;
+    const int tok_blk = p.kq_images ? kTokBlkFor<true> : kTokBlkFor<false>;
+    const long long n_tblocks = (p.T + tok_blk - 1) / tok_blk;
     const int head_groups = (n_slots + kWarps - 1) / kWarps;
     const long long n_conv_blocks = n_tblocks * head_groups;
     const long long n_hist_blocks = ((long long)p.n_seq * p.C + kHistThreads - 1) / kHistThreads;
