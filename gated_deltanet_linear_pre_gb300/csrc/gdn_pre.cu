@@ -10,9 +10,8 @@
 // order, vectorised tap loads, history kept channel by channel.)
 //
 // HBM-bound.  One warp owns one 128-channel head for a block of 16 consecutive
-// tokens (8 in the variant that writes the scan's images, whose extra staging
-// would otherwise cap it at 6 blocks per SM).  It first copies the block's rows of its head (and the 3
-// rows before them) into shared memory with 16-byte asynchronous copies, one
+// tokens.  It first copies the block's rows of its head (and the 3 rows before
+// them) into shared memory with 16-byte asynchronous copies, one
 // commit group per 8 tokens, so that many rows are in flight per SM without
 // holding registers; then each lane, holding 4 channels' taps in registers,
 // reads its 8 bytes of each row from shared memory, slides the 3-token window
@@ -26,10 +25,9 @@
 namespace gdn {
 namespace {
 
-// tokens per warp task (a multiple of 8, at most 32): 16 for the plain variant; 8 for the image
-// variant, so that its two stages fit 8 blocks per SM
+// tokens per warp task (a multiple of 8, at most 32)
 template <bool kImg>
-constexpr int kTokBlkFor = kImg ? 8 : 16;
+constexpr int kTokBlkFor = 16;
 constexpr int kWarps = 4;     // warps (heads) per block (128-thread blocks schedule finer than 256)
 constexpr int kThreads = kWarps * 32;
 constexpr int kHistThreads = kThreads;  // one history channel per thread
@@ -182,6 +180,10 @@ pre_kernel(PreParams p, int n_slots, int head_groups, int n_conv_blocks)
     const int c = slot * kHeadDim + lane * 4;
     constexpr int kTokBlk = kTokBlkFor<kImg>;
     constexpr int kStageRows = kTokBlk + 3;
+    // the image variant stages each 8-row output group in the same array: its hi plane over input rows
+    // 0-7 (token i writes row i, whose input token i - 3 has been read), its lo plane in 8 rows behind
+    // the inputs
+    constexpr int kAllRows = kStageRows + (kImg ? 8 : 0);
     const int t_begin = tb * kTokBlk;
     const int t_end = min(p.T, t_begin + kTokBlk);
 
@@ -194,7 +196,7 @@ pre_kernel(PreParams p, int n_slots, int head_groups, int n_conv_blocks)
     int seq_end = cu_at(p.cu_seqlens, seq + 1, p.T);
     const bool whole = t_end - t_begin == kTokBlk && t_end <= seq_end;  // the common case
     const int pos0 = t_begin - seq_start;
-    __shared__ __align__(16) unsigned char in_stage[kWarps][kStageRows * kRowBytes];
+    __shared__ __align__(16) unsigned char in_stage[kWarps][kAllRows * kRowBytes];
     unsigned char* stage = in_stage[warp];
     if (whole) {
         // the block's rows in one commit group per 8 tokens (the first with the 3 rows before the block,
@@ -245,11 +247,10 @@ pre_kernel(PreParams p, int n_slots, int head_groups, int n_conv_blocks)
         // (row-major 256-byte rows whose 16-byte pieces are permuted by the row index, piece m of row
         // r at m ^ r, so that neither side's accesses conflict) and written with 512 contiguous bytes
         // per warp store.  Otherwise each token goes out on its own.
-        constexpr int kRow = 256, kPlane = 8 * kRow;
-        __shared__ __align__(16) unsigned char kq_stage[kImg ? kWarps : 1][kImg ? 2 * kPlane : 16];
+        constexpr int kRow = 256, kPlane = kStageRows * kRow;  // the lo plane's offset from the hi plane
         const bool grouped = (pos0 & 7) == 0;
         const int slot0 = seq_start / kChunk + seq;
-#pragma unroll
+#pragma unroll(kImg ? 1 : kTokBlk / 8)
         for (int h8 = 0; h8 < kTokBlk / 8; ++h8) {
             if (h8 > 0) {
                 cp_async_wait_groups(kTokBlk / 8 - 1 - h8);
@@ -272,7 +273,7 @@ pre_kernel(PreParams p, int n_slots, int head_groups, int n_conv_blocks)
                 }
                 if (kImg && vh < 0) {
                     if (grouped) {
-                        unsigned char* stg = kq_stage[warp];
+                        unsigned char* stg = stage;
                         const __nv_bfloat162 h01 = __floats2bfloat162_rn(y0, y1), h23 = __floats2bfloat162_rn(y2, y3);
                         const float2 f01 = __bfloat1622float2(h01), f23 = __bfloat1622float2(h23);
                         const __nv_bfloat162 l01 = __floats2bfloat162_rn(y0 - f01.x, y1 - f01.y);
@@ -292,7 +293,7 @@ pre_kernel(PreParams p, int n_slots, int head_groups, int n_conv_blocks)
             }
             if (kImg && vh < 0 && grouped) {
                 __syncwarp();
-                const unsigned char* stg = kq_stage[warp];
+                const unsigned char* stg = stage;
                 const int pg = pos0 + 8 * h8, ci = pg >> 6;
                 const int row0 = ((is_k == ((ci & 1) != 0)) ? 64 : 0) + (pg & 63);
                 unsigned char* gdst = img_j + (size_t)(slot0 + ci) * slot_stride + (row0 >> 3) * 4096;
