@@ -656,8 +656,9 @@ constexpr int kPrepThreads = 256;  // two warpgroups: each covers all 128 TMEM l
 // round-one CTAs per SM the chain takes (of the four resident): the fewer, the sooner those SMs
 // are free, but the smaller the lead the staying CTAs start with over a chain that consumes
 // tasks faster than they produce them (T=2048, split products: scan 134.4 us with none, 130.7
-// with 1, 134.2 with 2, and 141.7 with 4 before the solve's coupling went to the tensor core;
-// one-pass products, whose chain consumes faster, layer 162.0 us with 2, 159.9 with 3, 162.4 with 4)
+// with 1, 134.2 with 2, and 141.7 with 4 before the solve's coupling went to the tensor core, and
+// 130.3 us with 1 against 133.2 with 2 since; one-pass products, whose chain consumes faster,
+// layer 162.0 us with 2, 159.9 with 3, 162.4 with 4)
 constexpr int kRound1PerSm = 1;
 // chunk slots above which prep defers each task's ready flag into its next task (T=32768: layer
 // 2459-2489 -> 2400-2454 us, the 8-sequence varlen batch 1213 -> 1200 us; one T=2048 prompt, 33
