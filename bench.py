@@ -62,6 +62,8 @@ def parse():
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-graph", action="store_true",
+                    help="time the metric with direct launches instead of replaying one captured step")
     ap.add_argument("--layers", type=int, default=LAYERS,
                     help="layers in the stack (fewer only for profiling captures; the metric is 36)")
     ap.add_argument("--mode", default="prefill", choices=["prefill", "decode"])
@@ -405,6 +407,9 @@ def main():
     gbuild.build()
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
+    # every launch and copy of this arm goes to one non-default stream, which a CUDA graph can capture
+    stream = torch.cuda.Stream(dev)
+    torch.cuda.set_stream(stream)
     d = gdn.dims(HK, HV, DK, DV, 1e-6)
 
     global LAYERS
@@ -427,7 +432,6 @@ def main():
     scan_ws_bytes = gdn.gdn_scan_workspace_bytes(d, 1, T)
     scan_ws = torch.empty(max(scan_ws_bytes, 1), device=dev, dtype=torch.uint8) if scan_ws_bytes else None
     layer_ws = torch.empty(gdn.gdn_layer_workspace_bytes(d, 1, T), device=dev, dtype=torch.uint8)
-    stream = torch.cuda.current_stream(dev)
 
     scan_fn = gdn.gdn_scan_fast if args.fast else gdn.gdn_scan
     layer_fn = gdn.gdn_layer_fast if args.fast else gdn.gdn_layer
@@ -463,6 +467,16 @@ def main():
 
     for _ in range(args.warmup):
         step()
+    # the metric replays one captured step (every launch of the 36 layers, without the per-call host
+    # work of the binding and the C ABI's argument checks); --no-graph times direct launches
+    graph = None
+    if not args.no_graph:
+        torch.cuda.synchronize()
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=stream):
+            step()
+        for _ in range(args.warmup):
+            graph.replay()
     for name in stage_calls:
         stage_group(name)
     torch.cuda.synchronize()
@@ -480,7 +494,10 @@ def main():
         torch.cuda.synchronize()
         e_start.record(stream)
         for k in range(args.steps):
-            step()
+            if graph is not None:
+                graph.replay()
+            else:
+                step()
         e_end.record(stream)
         torch.cuda.synchronize()
         barrier(world)
@@ -618,7 +635,8 @@ def main():
                 "data": "synthetic",
                 "config": {"workload": WORKLOAD.replace("fp16 output", "fp32 output") if out_f32 else WORKLOAD,
                            "layers": LAYERS, "seq_len": T, "global_batch": world,
-                           "parallelism": f"replicas{world}", "l2": "inputs larger than L2 (36-layer set ~2.3 GB)"},
+                           "parallelism": f"replicas{world}", "l2": "inputs larger than L2 (36-layer set ~2.3 GB)",
+                           "launch": "direct" if graph is None else "cuda graph of one step, replayed"},
                 "roofline": roofline, "stages": stages,
                 "timed_call": layer_fn.__name__,
                 "stage_timing": "each stage's launches for all layers back to back, through the stage calls gdn_pre, "
